@@ -1,0 +1,126 @@
+// C-ABI entry points that compose the kernels: W13, W2 + combine, the whole layer, status.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+using namespace moe;
+
+namespace {
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" size_t moe_workspace_bytes(const moe_shape* s) {
+  if (!shape_ok(s)) return 0;
+  return workspace_layout(s).total;
+}
+
+extern "C" int moe_w13_swiglu_grouped(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13,
+                                      const uint8_t* w13_s, const int32_t* expert_offsets,
+                                      const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* swiglu_debug,
+                                      void* ws, size_t ws_bytes, void* stream) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int rc = ws_check(s, ws, ws_bytes);
+  if (rc) return rc;
+  if (s->T == 0) return MOE_OK;
+  if (!xq || !xs || !w13 || !w13_s || !expert_offsets || !slot_of_row || !hq || !hs) return MOE_ERR_INVALID_ARG;
+  if (!aligned(xq, 16) || !aligned(xs, 4) || !aligned(w13, 32) || !aligned(w13_s, 16)) return MOE_ERR_INVALID_ARG;
+  const Workspace L = workspace_layout(s);
+  return launch_w13(s, xq, xs, w13, w13_s, expert_offsets, slot_of_row, hq, hs,
+                    (s->flags & 1) ? swiglu_debug : nullptr, ws_ptr<uint32_t>(ws, L.status),
+                    static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_w2_combine_grouped(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2,
+                                      const uint8_t* w2_s, const float* topk_w, const int32_t* expert_offsets,
+                                      const int32_t* slot_of_row, const int32_t* row_of_slot, uint16_t* out,
+                                      void* ws, size_t ws_bytes, void* stream) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int rc = ws_check(s, ws, ws_bytes);
+  if (rc) return rc;
+  if (s->T == 0) return MOE_OK;
+  if (!hq || !hs || !w2 || !w2_s || !topk_w || !expert_offsets || !slot_of_row || !row_of_slot || !out)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(hq, 16) || !aligned(hs, 4) || !aligned(w2, 32) || !aligned(w2_s, 16) || !aligned(out, 16))
+    return MOE_ERR_INVALID_ARG;
+  const Workspace L = workspace_layout(s);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* y = ws_ptr<float>(ws, L.y);
+  rc = launch_w2(s, hq, hs, w2, w2_s, topk_w, expert_offsets, slot_of_row, y, ws_ptr<uint32_t>(ws, L.status), st);
+  if (rc) return rc;
+  return launch_combine(s, y, row_of_slot, out, st);
+}
+
+extern "C" int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* bias,
+                           const uint8_t* dead, const uint8_t* w13, const uint8_t* w13_s, const uint8_t* w2,
+                           const uint8_t* w2_s, uint16_t* out, const moe_intermediates* inter, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int rc = ws_check(s, ws, ws_bytes);
+  if (rc) return rc;
+  if (s->T == 0) return MOE_OK;
+  if (!x || !w_router || !bias || !w13 || !w13_s || !w2 || !w2_s || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(w13, 32) || !aligned(w2, 32) || !aligned(w13_s, 16) ||
+      !aligned(w2_s, 16) || !aligned(out, 16))
+    return MOE_ERR_INVALID_ARG;
+  const Workspace L = workspace_layout(s);
+  moe_intermediates im{};
+  if (inter) im = *inter;
+  auto pick = [&](auto* user, size_t off) {
+    using Tp = std::remove_pointer_t<decltype(user)>;
+    return user ? user : ws_ptr<Tp>(ws, off);
+  };
+  int32_t* topk_idx = pick(im.topk_idx, L.topk_idx);
+  float* topk_w = pick(im.topk_w, L.topk_w);
+  int32_t* counts = pick(im.expert_counts, L.counts);
+  int32_t* offsets = pick(im.expert_offsets, L.offsets);
+  uint8_t* xq = pick(im.xq, L.xq);
+  uint8_t* xs = pick(im.xs, L.xs);
+  uint8_t* hq = pick(im.hq, L.hq);
+  uint8_t* hs = pick(im.hs, L.hs);
+  int32_t* slot_of_row = ws_ptr<int32_t>(ws, L.slot_of_row);
+  int32_t* row_of_slot = ws_ptr<int32_t>(ws, L.row_of_slot);
+  float* y = ws_ptr<float>(ws, L.y);
+  uint32_t* status = ws_ptr<uint32_t>(ws, L.status);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  rc = launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, ws, st);
+  if (rc) return rc;
+  rc = launch_quant_mxfp8(s->T, s->H, x, xq, xs, st);
+  if (rc) return rc;
+  rc = launch_w13(s, xq, xs, w13, w13_s, offsets, slot_of_row, hq, hs, im.swiglu, status, st);
+  if (rc) return rc;
+  rc = launch_w2(s, hq, hs, w2, w2_s, topk_w, offsets, slot_of_row, y, status, st);
+  if (rc) return rc;
+  return launch_combine(s, y, row_of_slot, out, st);
+}
+
+extern "C" int moe_check_device_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t h = 0;
+  if (cudaMemcpyAsync(&h, ws, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h != 0) {
+    if (cudaMemsetAsync(ws, 0, 4, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_ERR_TIMEOUT;
+  }
+  return MOE_OK;
+}

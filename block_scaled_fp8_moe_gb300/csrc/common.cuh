@@ -1,0 +1,109 @@
+// Host-side helpers shared by the translation units of libmoe: shape checks, workspace layout,
+// launch-error mapping.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kRouterChunk = 64;       // fixed reduction chunk of the router logits
+constexpr int kPlanBlock = 256;        // tokens per plan-count block
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kTileK = 128;            // K elements per packed tile / pipeline stage
+constexpr int kTileRows = 128;         // weight rows per packed tile
+constexpr int kTileCodeBytes = kTileRows * kTileK / 2;   // 8192
+constexpr int kTileScaleBytes = 512;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+inline bool shape_ok(const moe_shape* s) {
+  if (!s) return false;
+  if (s->T < 0 || s->H <= 0 || s->E <= 0 || s->k <= 0 || s->I <= 0) return false;
+  if (s->H % 128 || s->I % 64) return false;
+  if (s->k > kMaxK || s->k > s->E || s->E > kMaxE) return false;
+  if (s->H > 16384 || s->I > 16384) return false;
+  if ((int64_t)s->T * s->k > (int64_t)1 << 30) return false;
+  return true;
+}
+
+inline int hs_pitch(int I) { return (int)(align_up((size_t)I, 128) / 32); }
+
+// Workspace carve-up. Every piece 256-byte aligned; the status word sits at offset 0.
+struct Workspace {
+  size_t status, score, key, cnt, base, rank;                  // router scratch
+  size_t topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot;
+  size_t xq, xs, hq, hs, y;                                    // forward intermediates
+  size_t total;
+};
+
+inline Workspace workspace_layout(const moe_shape* s) {
+  Workspace w{};
+  size_t T = (size_t)s->T, E = (size_t)s->E, k = (size_t)s->k, H = (size_t)s->H, I = (size_t)s->I;
+  size_t nb = (T + kPlanBlock - 1) / kPlanBlock;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + (bytes ? bytes : 1), 256); return o; };
+  w.status = take(256);
+  w.score = take(T * E * 4);
+  w.key = take(T * E * 4);
+  w.cnt = take(nb * E * 4);
+  w.base = take(nb * E * 4);
+  w.rank = take(T * k * 4);
+  w.topk_idx = take(T * k * 4);
+  w.topk_w = take(T * k * 4);
+  w.counts = take(E * 4);
+  w.offsets = take((E + 1) * 4);
+  w.slot_of_row = take(T * k * 4);
+  w.row_of_slot = take(T * k * 4);
+  w.xq = take(T * H);
+  w.xs = take(T * H / 32);
+  w.hq = take(T * k * I);
+  w.hs = take(T * k * (size_t)hs_pitch((int)I));
+  w.y = take(T * k * H * 4);
+  w.total = off;
+  return w;
+}
+
+inline int ws_check(const moe_shape* s, void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < workspace_layout(s).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+template <typename T>
+inline T* ws_ptr(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+inline int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+inline int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+// Internal launchers (defined in the .cu files), all asynchronous on `st`.
+int launch_quant_mxfp8(int rows, int cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st);
+int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, const uint8_t* dead,
+                 int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
+                 int32_t* row_of_slot, void* ws, cudaStream_t st);
+int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
+               const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
+               uint32_t* status, cudaStream_t st);
+int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2s,
+              const float* topk_w, const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
+              cudaStream_t st);
+int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, uint16_t* out, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,529 @@
+// Grouped block-scaled GEMMs of the routed experts on tcgen05 (sm_103a).
+//
+// "New Deepseek 4.1 flash recipe", post 6 "How it works" items 1-2: routed experts run FP8
+// activations x FP4 weights through a block-scaled MMA (kind::mxf8f6f4); decode rows run on
+// 16/32/64-row tiles; prefill rasterises weights larger than L2 in panels. Post 4 "Fenced
+// pipeline stages": a stage may be refilled only after every read of it has completed.
+// TP4 serving profile README, "Experts" row: per-slot output buffer, fixed-order sum.
+//
+// Shape of one CTA work item: 128 weight rows (MMA M) x BN plan rows (MMA N, tokens), K looped in
+// 128-element chunks. Weights sit on the A side so decode and prefill share one accumulation
+// order for every output element: the K loop is identical, never split, and a token's column
+// position does not change the arithmetic of its column.
+//
+// Roles (256 threads):
+//   warp 0      TMA producer: packed weight tile (FP4, unpacked to 8-bit containers by the TMA)
+//               and its 512-byte scale block (bulk copy); one mbarrier transaction per stage.
+//   warps 1, 3  gather producers: cp.async of the BN activation rows (128 B each, 128B-swizzled
+//               in shared memory) and their scale bytes; arrive on the same stage mbarrier.
+//   warp 2      TMEM owner and MMA issuer: tcgen05.cp of both scale blocks to TMEM, four
+//               K=32 MMAs per stage, tcgen05.commit releases the stage only after the MMAs
+//               (and copies) that read it are complete.
+//   warps 4-7   epilogue: tcgen05.ld of the fp32 accumulator, SwiGLU + MXFP8 requant (W13) or
+//               routing-weight scaling into the per-slot buffer (W2).
+// Work items (expert, weight panel, token tile) are walked with the token tile fastest, so CTAs
+// running at the same time share one weight panel through L2.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+constexpr int kThreads = 256;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
+constexpr int kSfCol0 = 128;                        // first TMEM column of the scale ring
+constexpr int kTmemCols = 256;
+
+struct GemmParams {
+  // B side (activations)
+  const uint8_t* bq;        // W13: xq [T, H];  W2: hq [S, I]
+  const uint8_t* bs;        // W13: xs [T, H/32]; W2: hs [S, HS_PITCH]
+  int b_row_bytes;          // K in bytes (= elements)
+  int b_scale_pitch;        // bytes per scale row
+  // A side (packed weights)
+  const uint8_t* a_scales;  // packed 512-byte scale blocks
+  // plan
+  const int32_t* offsets;   // [E + 1]
+  const int32_t* slot_of_row;
+  int E, k, K, KC, MT;      // MT = weight panels (of 128 packed rows) per expert
+  int I, H;
+  // W13 outputs
+  uint8_t* hq;
+  uint8_t* hs;
+  int hs_pitch;
+  float* dbg;
+  // W2 outputs
+  const float* topk_w;
+  float* y;
+  uint32_t* status;
+};
+
+template <int BN>
+struct Smem {
+  static constexpr int kStageA = 16384;
+  static constexpr int kStageB = BN * 128;
+  static constexpr int kStageBytes = kStageA + kStageB + 1024;   // + 512 B A scales + 512 B B scales
+  static constexpr int kStages = (BN <= 16) ? 5 : (BN <= 64 ? 4 : 3);
+  static constexpr int kTiles = kStages * kStageBytes;
+  static constexpr int kXchg = 64 * 16 * 4;                     // W13 epilogue exchange
+  static constexpr int kMisc = 1024;                            // barriers, flags
+  static constexpr int kRows = 128 * 8;                         // gather row table
+  static constexpr int kFixed = 1024 + kTiles + kXchg + kMisc + kRows;
+  // + (E + 1) * 8 bytes of plan tables, sized per launch
+  static int total(int E) { return kFixed + (int)align_up((size_t)(E + 1) * 8, 16); }
+};
+
+// One lane waits (bounded), the whole warp learns the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort, uint32_t* err,
+                                          uint32_t code) {
+  uint32_t ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, kWaitLimitNs, abort, err, code) ? 1u : 0u;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ int find_expert(const int* cum, int E, int w) {
+  // largest e with cum[e] <= w (cum non-decreasing, cum[E] > w)
+  int lo = 0, hi = E;           // invariant: cum[lo] <= w < cum[hi]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (cum[mid] <= w) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+__device__ __forceinline__ uint32_t e4m3_pair(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ int mx8_scale_exp(float amax) {
+  uint32_t b = __float_as_uint(amax);
+  if (b == 0) return -127;
+  int e = (int)((b >> 23) & 0xFF);
+  uint32_t man = b & 0x7FFFFF;
+  if (e == 0) {
+    int sh = __clz(man) - 8;
+    man = (man << sh) & 0x7FFFFF;
+    e = 1 - sh;
+  }
+  int s = (e - 127) - 8 + (man > 0x600000u ? 1 : 0);
+  return max(-127, min(126, s));
+}
+
+template <int BN, bool W13>
+__global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                                                    const GemmParams p) {
+  using L = Smem<BN>;
+  constexpr int S = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = base;
+  float* xchg = reinterpret_cast<float*>(base + L::kTiles);
+  uint8_t* misc = base + L::kTiles + L::kXchg;
+  uint64_t* full = reinterpret_cast<uint64_t*>(misc);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  long long* s_rows = reinterpret_cast<long long*>(misc + L::kMisc);   // [BN] gather row or -1
+  int* s_off = reinterpret_cast<int*>(misc + L::kMisc + L::kRows);      // expert offsets [E+1]
+  int* s_cum = s_off + (p.E + 1);                                       // MT * tile starts [E+1]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+
+  // ---- prologue: plan tables, barriers, TMEM ----
+  for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets[i];
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1 + 64);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    mbar_init(drain, 1);
+    mbar_fence_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // tile starts: warp-parallel prefix sum of ceil(count_e / BN), times MT
+    const int per = (E + 31) / 32;
+    const int e0 = lane * per;
+    int local = 0;
+    for (int e = e0; e < min(E, e0 + per); ++e) local += (s_off[e + 1] - s_off[e] + BN - 1) / BN;
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int run = incl - local;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      s_cum[e] = run * p.MT;
+      run += (s_off[e + 1] - s_off[e] + BN - 1) / BN;
+    }
+    if (lane == 31) s_cum[E] = incl * p.MT;
+    if (threadIdx.x == 0) prefetch_tmap(&tmap_a);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int total = s_cum[E];
+
+  // decode work item w -> (e, m, nt)
+  auto decode = [&](int w, int& e, int& m, int& nt, int& row0, int& nrows) {
+    e = find_expert(s_cum, E, w);
+    const int cnt = s_off[e + 1] - s_off[e];
+    const int ntiles = (cnt + BN - 1) / BN;
+    const int local = w - s_cum[e];
+    m = local / ntiles;
+    nt = local - m * ntiles;
+    row0 = s_off[e] + nt * BN;
+    nrows = min(BN, cnt - nt * BN);
+  };
+
+  if (warp == 0) {
+    // ===================== TMA producer: weights =====================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        int e, m, nt, row0, nrows;
+        decode(w, e, m, nt, row0, nrows);
+        const int tile0 = (e * p.MT + m) * p.KC;
+        for (int kc = 0; kc < p.KC; ++kc) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_EMPTY)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = tiles + stage * L::kStageBytes;
+          uint8_t* sSFA = sA + L::kStageA + L::kStageB;
+          mbar_arrive_expect_tx(&full[stage], kTileCodeBytes + kTileScaleBytes);
+          tma_load_2d(sA, &tmap_a, 0, (tile0 + kc) * 128, &full[stage]);
+          bulk_load(sSFA, p.a_scales + (size_t)(tile0 + kc) * kTileScaleBytes, kTileScaleBytes, &full[stage]);
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1 || warp == 3) {
+    // ===================== gather producers: activations =====================
+    // After an expired wait the loops keep running (doing nothing) so that both warps meet at
+    // every named barrier.
+    const int pb = (warp == 1 ? 0 : 32) + lane;       // 0..63
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total; w += gridDim.x) {
+      int e, m, nt, row0, nrows;
+      decode(w, e, m, nt, row0, nrows);
+      named_bar_sync(2, 64);                          // previous item's table no longer in use
+      for (int c = pb; c < BN; c += 64) {
+        long long r = -1;
+        if (c < nrows) {
+          const int prow = row0 + c;
+          r = W13 ? (long long)(p.slot_of_row[prow] / p.k) : (long long)prow;
+        }
+        s_rows[c] = r;
+      }
+      named_bar_sync(2, 64);
+      for (int kc = 0; kc < p.KC; ++kc) {
+        if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
+        if (ok) {
+          uint8_t* sB = tiles + stage * L::kStageBytes + L::kStageA;
+          uint8_t* sSFB = sB + L::kStageB + 512;
+          for (int i = pb; i < BN * 8; i += 64) {
+            const int c = i >> 3, j = i & 7;
+            const long long r = s_rows[c];
+            const int kbyte = kc * 128 + j * 16;
+            const bool valid = (r >= 0) && (kbyte < p.b_row_bytes);
+            const uint8_t* src = valid ? p.bq + r * p.b_row_bytes + kbyte : p.bq;
+            cp_async_16(sB + c * 128 + ((j ^ (c & 7)) << 4), src, valid ? 16u : 0u);
+          }
+          for (int c = pb; c < BN; c += 64) {
+            const long long r = s_rows[c];
+            const bool valid = r >= 0;
+            const uint8_t* src = valid ? p.bs + r * p.b_scale_pitch + kc * 4 : p.bs;
+            cp_async_4(sSFB + (c & 31) * 16 + (c >> 5) * 4, src, valid ? 4u : 0u);
+          }
+          cp_async_arrive_noinc(&full[stage]);
+        }
+        if (++stage == S) { stage = 0; phase ^= 1; }
+      }
+    }
+    cp_async_wait_all();
+  } else if (warp == 2) {
+    // ===================== MMA issuer =====================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      const uint32_t idesc_base = idesc_mxf8f6f4(5 /*E2M1*/, 0 /*E4M3*/, 128, BN, 0, 0);
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it) {
+        if (it > 0 &&
+            !mbar_wait(acc_empty, (it - 1) & 1, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_DRAIN)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kc = 0; kc < p.KC; ++kc) {
+          if (!mbar_wait(&full[stage], phase, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_FULL)) {
+            ok = false;
+            break;
+          }
+          fence_async_smem();
+          tc_fence_after();
+          uint8_t* sA = tiles + stage * L::kStageBytes;
+          uint8_t* sB = sA + L::kStageA;
+          uint8_t* sSFA = sB + L::kStageB;
+          uint8_t* sSFB = sSFA + 512;
+          const uint32_t tsfa = tmem + kSfCol0 + stage * 8;
+          const uint32_t tsfb = tsfa + 4;
+          tc_cp_32x128b_warpx4(tsfa, smem_desc(smem_u32(sSFA), 16, 128, 0));
+          tc_cp_32x128b_warpx4(tsfb, smem_desc(smem_u32(sSFB), 16, 128, 0));
+          const int nk = min(4, (p.K - kc * 128) / 32);
+          for (int kb = 0; kb < nk; ++kb) {
+            const uint64_t ad = smem_desc(smem_u32(sA) + kb * 32, 16, 1024, 2);
+            const uint64_t bd = smem_desc(smem_u32(sB) + kb * 32, 16, 1024, 2);
+            const uint32_t id = idesc_base | ((uint32_t)kb << 4) | ((uint32_t)kb << 29);
+            mma_mxf8f6f4(tmem, ad, bd, id, tsfa, tsfb, (kc > 0 || kb > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+      }
+      // every MMA this thread issued has completed before TMEM is released
+      tc_commit(drain);
+      mbar_wait(drain, 0, kWaitLimitNs, abort_flag, nullptr, 0);
+    }
+    __syncwarp();
+  } else {
+    // ===================== epilogue (warps 4..7 -> TMEM lanes 32 (warp - 4)) =====================
+    // As above, an expired wait turns the remaining iterations into no-ops that still meet at the
+    // named barriers.
+    const int q = warp - 4;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    int it = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total; w += gridDim.x, ++it) {
+      int e, m, nt, row0, nrows;
+      decode(w, e, m, nt, row0, nrows);
+      if (ok) ok = warp_wait(acc_full, it & 1, abort_flag, p.status, DEV_TIMEOUT_ACCUM);
+      tc_fence_after();
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t r[16];
+        if (ok) {
+          tmem_ld16(tmem + lane_base + c0, r);
+          tmem_ld_wait();
+        }
+        if constexpr (W13) {
+          // q 0,1: gate features 64m + 32q + lane; q 2,3: the matching up features
+          if (q >= 2 && ok) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) xchg[c * 64 + 32 * (q - 2) + lane] = __uint_as_float(r[c]);
+          }
+          named_bar_sync(1, 128);
+          if (q < 2 && ok) {
+            const int feat = 64 * m + 32 * q + lane;
+#pragma unroll 4
+            for (int c = 0; c < 16; ++c) {
+              const int col = c0 + c;
+              const float g = __uint_as_float(r[c]);
+              const float u = xchg[c * 64 + 32 * q + lane];
+              const float a = silu_mul(g, u);
+              float am = fabsf(a);
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+              const int se = mx8_scale_exp(am);
+              const float sc = __uint_as_float((uint32_t)(127 - se) << 23);
+              const uint32_t code = e4m3_pair(a * sc, 0.f) & 0xFF;
+              if (col < nrows) {
+                const size_t prow = (size_t)(row0 + col);
+                p.hq[prow * p.I + feat] = (uint8_t)code;
+                if (lane == 0) p.hs[prow * p.hs_pitch + (feat >> 5)] = (uint8_t)(se + 127);
+                if (p.dbg) p.dbg[prow * p.I + feat] = a;
+              }
+            }
+          }
+          named_bar_sync(1, 128);
+        } else {
+          if (ok) {
+            const int feat = 128 * m + 32 * q + lane;
+#pragma unroll 4
+            for (int c = 0; c < 16; ++c) {
+              const int col = c0 + c;
+              if (col < nrows) {
+                const int slot = p.slot_of_row[row0 + col];
+                const float wgt = p.topk_w[slot];
+                p.y[(size_t)slot * p.H + feat] = __fmul_rn(wgt, __uint_as_float(r[c]));
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && ok) mbar_arrive(acc_empty);
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // give copies still in flight time to land before the CTA's shared memory goes away
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000) {
+    }
+  }
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// Packed weight codes viewed as [tiles * 128 rows, 128 FP4 elements], 64 bytes per row.
+static int make_weight_tmap(CUtensorMap* m, const uint8_t* codes, long long tiles) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return MOE_ERR_CUDA;
+  cuuint64_t gdim[2] = {128, (cuuint64_t)tiles * 128};
+  cuuint64_t gstride[1] = {64};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t*>(codes), gdim, gstride, box,
+                   estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+static int pick_bn(const moe_shape* s) {
+  const double avg = (double)s->T * s->k / s->E;
+  if (avg <= 16) return 16;
+  if (avg <= 32) return 32;
+  if (avg <= 64) return 64;
+  return 128;
+}
+
+template <int BN, bool W13>
+static int launch_gemm_bn(const CUtensorMap& tm, const GemmParams& gp, long long max_items, cudaStream_t st) {
+  using L = Smem<BN>;
+  auto kern = grouped_gemm_kernel<BN, W13>;
+  const int smem = L::total(gp.E);
+  static int attr = 0;
+  if (attr < smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total(kMaxE)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr = L::total(kMaxE);
+  }
+  const long long grid = std::min<long long>(max_items, 2LL * num_sms());
+  if (grid <= 0) return MOE_OK;
+  kern<<<(int)grid, kThreads, smem, st>>>(tm, gp);
+  return launch_status();
+}
+
+template <bool W13>
+static int launch_gemm(const moe_shape* s, const CUtensorMap& tm, const GemmParams& gp, cudaStream_t st) {
+  const long long slots = (long long)s->T * s->k;
+  const int bn = pick_bn(s);
+  const long long max_items = (long long)gp.MT * ((slots + bn - 1) / bn + std::min<long long>(s->E, slots));
+  switch (bn) {
+    case 16: return launch_gemm_bn<16, W13>(tm, gp, max_items, st);
+    case 32: return launch_gemm_bn<32, W13>(tm, gp, max_items, st);
+    case 64: return launch_gemm_bn<64, W13>(tm, gp, max_items, st);
+    default: return launch_gemm_bn<128, W13>(tm, gp, max_items, st);
+  }
+}
+
+int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
+               const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
+               uint32_t* status, cudaStream_t st) {
+  if (s->T == 0) return MOE_OK;
+  GemmParams gp{};
+  gp.bq = xq;
+  gp.bs = xs;
+  gp.b_row_bytes = s->H;
+  gp.b_scale_pitch = s->H / 32;
+  gp.a_scales = w13s;
+  gp.offsets = offsets;
+  gp.slot_of_row = slot_of_row;
+  gp.E = s->E;
+  gp.k = s->k;
+  gp.K = s->H;
+  gp.KC = s->H / kTileK;
+  gp.MT = s->I / 64;
+  gp.I = s->I;
+  gp.H = s->H;
+  gp.hq = hq;
+  gp.hs = hs;
+  gp.hs_pitch = hs_pitch(s->I);
+  gp.dbg = dbg;
+  gp.status = status;
+  CUtensorMap tm;
+  int rc = make_weight_tmap(&tm, w13, (long long)s->E * gp.MT * gp.KC);
+  if (rc) return rc;
+  return launch_gemm<true>(s, tm, gp, st);
+}
+
+int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2s,
+              const float* topk_w, const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
+              cudaStream_t st) {
+  if (s->T == 0) return MOE_OK;
+  GemmParams gp{};
+  gp.bq = hq;
+  gp.bs = hs;
+  gp.b_row_bytes = s->I;
+  gp.b_scale_pitch = hs_pitch(s->I);
+  gp.a_scales = w2s;
+  gp.offsets = offsets;
+  gp.slot_of_row = slot_of_row;
+  gp.E = s->E;
+  gp.k = s->k;
+  gp.K = s->I;
+  gp.KC = ceil_div(s->I, kTileK);
+  gp.MT = s->H / 128;
+  gp.I = s->I;
+  gp.H = s->H;
+  gp.topk_w = topk_w;
+  gp.y = y;
+  gp.status = status;
+  CUtensorMap tm;
+  int rc = make_weight_tmap(&tm, w2, (long long)s->E * gp.MT * gp.KC);
+  if (rc) return rc;
+  return launch_gemm<false>(s, tm, gp, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,475 @@
+// Router (fixed-order fp32 logits, self-written sigmoid, top-k with lowest-index ties), expert
+// plan (deterministic counting sort), and the fixed-order combine.
+//
+// "New Deepseek 4.1 flash recipe": post 6 "How it works" item 3 (TileKernels MoE top-k gate);
+// post 6 "Why TileLang" (every reduction in a fixed order, batch-invariant rows); post 4
+// "Exact indexer selections" (ties break by lowest position); post 2 (dead verification rows).
+// TP4 serving profile README, "Experts" row: per-slot buffer + fixed-order sum instead of atomics.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------------------------
+// Library-independent exp / sigmoid from IEEE fp32 +, -, *, / (each correctly rounded; the
+// _rn intrinsics keep the compiler from contracting them). exp(t), t in [-80, 80]:
+// n = rint(t / ln2); r = (t - n ln2_hi) - n ln2_lo (Cody & Waite); degree-7 Taylor polynomial
+// of exp(r) in Horner form; times 2^n (exact). ln2_hi keeps 16 significant bits so n * ln2_hi
+// is exact. Coefficients are 1/k! rounded to fp32.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ float exp_cw(float t) {
+  const float kLog2e = 1.4426950408889634f;
+  const float kLn2Hi = 0.693145751953125f;              // 45426 / 2^16
+  const float kLn2Lo = 1.4286067653302226e-06f;         // ln2 - kLn2Hi, rounded to fp32
+  float n = rintf(__fmul_rn(t, kLog2e));
+  float r = __fsub_rn(t, __fmul_rn(n, kLn2Hi));
+  r = __fsub_rn(r, __fmul_rn(n, kLn2Lo));
+  float p = 1.9841269841269841e-04f;                    // 1/7!
+  p = __fadd_rn(__fmul_rn(p, r), 1.3888888888888889e-03f);   // 1/6!
+  p = __fadd_rn(__fmul_rn(p, r), 8.3333333333333332e-03f);   // 1/5!
+  p = __fadd_rn(__fmul_rn(p, r), 4.1666666666666664e-02f);   // 1/4!
+  p = __fadd_rn(__fmul_rn(p, r), 1.6666666666666666e-01f);   // 1/3!
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  const float two_n = __int_as_float(((int)n + 127) << 23);
+  return __fmul_rn(p, two_n);
+}
+
+__device__ __forceinline__ float sigmoid_cw(float z) {
+  float t = fminf(fmaxf(-z, -80.0f), 80.0f);
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_cw(t)));
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------------------------------------
+// Logits, small T (decode): one warp per expert. Lane l owns the chunks c = l, l + 32, ...;
+// each chunk is a sequential fma chain from +0; chunk sums go to shared memory and lane t folds
+// them left to right for token t.
+// ---------------------------------------------------------------------------------------------
+constexpr int kSmallT = 16;
+
+__global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __restrict__ x,
+                                                           const uint16_t* __restrict__ wr,
+                                                           const float* __restrict__ bias, int T, int H, int E,
+                                                           float* __restrict__ score, float* __restrict__ key) {
+  __shared__ float part[8][kSmallT][33];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  if (e >= E) return;
+  const int NC = H / kRouterChunk;
+  float acc = 0.f;                                     // lane t < T folds token t
+  for (int c0 = 0; c0 < NC; c0 += 32) {
+    const int c = c0 + lane;
+    if (c < NC) {
+      const uint4* wp = reinterpret_cast<const uint4*>(wr + (size_t)e * H + (size_t)c * kRouterChunk);
+      uint4 wv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) wv[i] = __ldg(wp + i);
+      for (int t = 0; t < T; ++t) {
+        const uint4* xp = reinterpret_cast<const uint4*>(x + (size_t)t * H + (size_t)c * kRouterChunk);
+        float p = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint4 xv = __ldg(xp + i);
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+          const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            p = __fmaf_rn(bf_lo(xw[q]), bf_lo(ww[q]), p);
+            p = __fmaf_rn(bf_hi(xw[q]), bf_hi(ww[q]), p);
+          }
+        }
+        part[warp][t][lane] = p;
+      }
+    }
+    __syncwarp();
+    if (lane < T) {
+      const int n = min(32, NC - c0);
+      for (int i = 0; i < n; ++i) acc = __fadd_rn(acc, part[warp][lane][i]);
+    }
+    __syncwarp();
+  }
+  if (lane < T) {
+    const float sc = sigmoid_cw(acc);
+    score[(size_t)lane * E + e] = sc;
+    key[(size_t)lane * E + e] = __fadd_rn(sc, bias[e]);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Logits, large T: 64 tokens x 64 experts per CTA, 4 x 4 outputs per thread, one 64-wide h chunk
+// per shared-memory stage. Each output keeps its chunk partial (sequential fma from +0 over the
+// chunk) and adds it to the running sum after the chunk: the same order as the small kernel.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) router_tiled_kernel(const uint16_t* __restrict__ x,
+                                                           const uint16_t* __restrict__ wr,
+                                                           const float* __restrict__ bias, int T, int H, int E,
+                                                           float* __restrict__ score, float* __restrict__ key) {
+  __shared__ float xs[64][65];
+  __shared__ float ws[64][65];
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
+  float acc[4][4], part[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int h0 = 0; h0 < H; h0 += kRouterChunk) {
+    __syncthreads();
+    // 64 rows x 64 bf16 = 512 uint4 per matrix; 2 per thread per matrix
+#pragma unroll
+    for (int rep = 0; rep < 2; ++rep) {
+      const int idx = tid + rep * 256;
+      const int row = idx >> 3, seg = idx & 7;
+      uint4 xv = make_uint4(0, 0, 0, 0), wv = make_uint4(0, 0, 0, 0);
+      if (t0 + row < T) xv = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + row) * H + h0) + seg);
+      if (e0 + row < E) wv = __ldg(reinterpret_cast<const uint4*>(wr + (size_t)(e0 + row) * H + h0) + seg);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        xs[row][seg * 8 + 2 * q] = bf_lo(xw[q]);
+        xs[row][seg * 8 + 2 * q + 1] = bf_hi(xw[q]);
+        ws[row][seg * 8 + 2 * q] = bf_lo(ww[q]);
+        ws[row][seg * 8 + 2 * q + 1] = bf_hi(ww[q]);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) part[i][j] = 0.f;
+#pragma unroll 8
+    for (int h = 0; h < kRouterChunk; ++h) {
+      float xv[4], wv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xv[i] = xs[ty + 16 * i][h];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) wv[j] = ws[tx + 16 * j][h];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) part[i][j] = __fmaf_rn(xv[i], wv[j], part[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = __fadd_rn(acc[i][j], part[i][j]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty + 16 * i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx + 16 * j;
+      if (e >= E) continue;
+      const float sc = sigmoid_cw(acc[i][j]);
+      score[(size_t)t * E + e] = sc;
+      key[(size_t)t * E + e] = __fadd_rn(sc, bias[e]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Top-k + in-block plan. One CTA per block of kPlanBlock tokens, 16 warps. Each warp routes its
+// tokens one at a time: k rounds of a warp arg-max over (key descending, expert ascending).
+// Then the CTA builds, per expert, a bitmask of the block's live tokens that chose it: the rank
+// of a slot inside its expert is the number of lower token bits set, so the plan order inside an
+// expert is token order, with no atomics whose order matters.
+// With a single block (T <= kPlanBlock) the same CTA also scans and scatters the plan.
+// ---------------------------------------------------------------------------------------------
+constexpr int kTopkWarps = 16;
+
+__device__ __forceinline__ bool better(float ka, int ea, float kb, int eb) {
+  return ka > kb || (ka == kb && ea < eb);
+}
+
+__device__ void block_exclusive_scan(int* vals, int n, int* total) {
+  // vals in shared memory, n <= 1024; blockDim.x == 512
+  __shared__ int tmp[1024];
+  for (int i = threadIdx.x; i < 1024; i += blockDim.x) tmp[i] = i < n ? vals[i] : 0;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    int v[2];
+    for (int q = 0; q < 2; ++q) {
+      int i = threadIdx.x + q * 512;
+      v[q] = (i >= off) ? tmp[i - off] : 0;
+    }
+    __syncthreads();
+    for (int q = 0; q < 2; ++q) tmp[threadIdx.x + q * 512] += v[q];
+    __syncthreads();
+  }
+  // tmp is now the inclusive scan
+  for (int i = threadIdx.x; i < n; i += blockDim.x) vals[i] = i == 0 ? 0 : tmp[i - 1];
+  if (threadIdx.x == 0) *total = n > 0 ? tmp[n - 1] : 0;
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(512) topk_plan_kernel(const float* __restrict__ score, const float* __restrict__ key,
+                                                        const uint8_t* __restrict__ dead, int T, int E, int k,
+                                                        int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                                        int32_t* __restrict__ cnt, int32_t* __restrict__ rank,
+                                                        int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                        int32_t* __restrict__ slot_of_row,
+                                                        int32_t* __restrict__ row_of_slot) {
+  extern __shared__ uint32_t dsm[];
+  uint32_t* mask = dsm;                                         // [E][8]
+  int16_t* sidx = reinterpret_cast<int16_t*>(dsm + E * 8);      // [kPlanBlock][k]
+  __shared__ int scnt[kMaxE];
+  __shared__ int total_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tb0 = blockIdx.x * kPlanBlock;
+  const int nt = min(kPlanBlock, T - tb0);
+  for (int i = threadIdx.x; i < E * 8; i += blockDim.x) mask[i] = 0;
+
+  for (int tl = warp; tl < nt; tl += kTopkWarps) {
+    const int t = tb0 + tl;
+    float kv[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      kv[i] = (e < E) ? key[(size_t)t * E + e] : 0.f;
+    }
+    uint32_t taken = 0;
+    float sel_sum = 0.f;
+    int my_e = -1;
+    float my_s = 0.f;
+    for (int j = 0; j < k; ++j) {
+      float bk = 0.f;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (be == 0x7fffffff || kv[i] > bk)) { bk = kv[i]; be = e; }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        float ok = __shfl_xor_sync(0xffffffffu, bk, off);
+        int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (oe != 0x7fffffff && (be == 0x7fffffff || better(ok, oe, bk, be))) { bk = ok; be = oe; }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      const float s = score[(size_t)t * E + be];
+      sel_sum = __fadd_rn(sel_sum, s);           // rank order, identical on every lane
+      if (lane == j) { my_e = be; my_s = s; }
+      sidx[tl * k + j] = (int16_t)be;
+    }
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = my_e;
+      topk_w[(size_t)t * k + lane] = __fdiv_rn(my_s, sel_sum);
+    }
+  }
+  __syncthreads();
+  // per-expert token bitmasks of this block (bit order = token order)
+  for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
+    const int tl = i / k;
+    if (dead && dead[tb0 + tl]) continue;
+    const int e = sidx[i];
+    atomicOr(&mask[e * 8 + (tl >> 5)], 1u << (tl & 31));
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) c += __popc(mask[e * 8 + w]);
+    scnt[e] = c;
+  }
+  __syncthreads();
+  const bool single = (gridDim.x == 1);
+  if (!single) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[(size_t)blockIdx.x * E + e] = scnt[e];
+  }
+  for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
+    const int tl = i / k;
+    const int t = tb0 + tl;
+    int r = -1;
+    if (!(dead && dead[t])) {
+      const int e = sidx[i];
+      const int w = tl >> 5;
+      r = 0;
+      for (int q = 0; q < w; ++q) r += __popc(mask[e * 8 + q]);
+      r += __popc(mask[e * 8 + w] & ((1u << (tl & 31)) - 1u));
+    }
+    if (!single) rank[(size_t)t * k + (i % k)] = r;
+    else if (r < 0) sidx[i] = -1;     // dead slot: no plan row
+  }
+  if (!single) return;
+  // single block: counts, offsets, scatter
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = scnt[e];
+  __syncthreads();
+  block_exclusive_scan(scnt, E, &total_s);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = scnt[e];
+  if (threadIdx.x == 0) offsets[E] = total_s;
+  for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
+    const int tl = i / k;
+    const int t = tb0 + tl;
+    const int e = sidx[i];
+    if (e < 0) { row_of_slot[(size_t)t * k + (i % k)] = -1; continue; }
+    const int w = tl >> 5;
+    int r = 0;
+    for (int q = 0; q < w; ++q) r += __popc(mask[e * 8 + q]);
+    r += __popc(mask[e * 8 + w] & ((1u << (tl & 31)) - 1u));
+    const int p = scnt[e] + r;
+    slot_of_row[p] = t * k + (i % k);
+    row_of_slot[(size_t)t * k + (i % k)] = p;
+  }
+}
+
+// Multi-block plan, step 2 (one CTA): per-expert totals, offsets, and each block's base row.
+__global__ void __launch_bounds__(512) plan_scan_kernel(const int32_t* __restrict__ cnt, int nb, int E,
+                                                        int32_t* __restrict__ base, int32_t* __restrict__ counts,
+                                                        int32_t* __restrict__ offsets) {
+  __shared__ int tot[kMaxE];
+  __shared__ int total_s;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nb; ++b) {
+      const int c = cnt[(size_t)b * E + e];
+      base[(size_t)b * E + e] = run;
+      run += c;
+    }
+    tot[e] = run;
+    counts[e] = run;
+  }
+  __syncthreads();
+  block_exclusive_scan(tot, E, &total_s);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = tot[e];
+  if (threadIdx.x == 0) offsets[E] = total_s;
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    for (int b = 0; b < nb; ++b) base[(size_t)b * E + e] += tot[e];
+}
+
+// Multi-block plan, step 3: scatter every live slot to its plan row.
+__global__ void plan_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ rank,
+                                    const int32_t* __restrict__ base, int T, int E, int k,
+                                    int32_t* __restrict__ slot_of_row, int32_t* __restrict__ row_of_slot) {
+  const long long n = (long long)T * k;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int r = rank[i];
+    if (r < 0) { row_of_slot[i] = -1; continue; }
+    const int t = (int)(i / k);
+    const int b = t / kPlanBlock;
+    const int e = topk_idx[i];
+    const int p = base[(size_t)b * E + e] + r;
+    slot_of_row[p] = (int)i;
+    row_of_slot[i] = p;
+  }
+}
+
+int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, const uint8_t* dead,
+                 int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
+                 int32_t* row_of_slot, void* ws, cudaStream_t st) {
+  const Workspace L = workspace_layout(s);
+  const int T = s->T, E = s->E, k = s->k, H = s->H;
+  if (T == 0) {
+    cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st);
+    cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), st);
+    return launch_status();
+  }
+  float* score = ws_ptr<float>(ws, L.score);
+  float* key = ws_ptr<float>(ws, L.key);
+  if (T <= kSmallT) {
+    router_small_kernel<<<ceil_div(E, 8), 256, 0, st>>>(x, wr, bias, T, H, E, score, key);
+  } else {
+    dim3 grid(ceil_div(T, 64), ceil_div(E, 64));
+    router_tiled_kernel<<<grid, 256, 0, st>>>(x, wr, bias, T, H, E, score, key);
+  }
+  int rc = launch_status();
+  if (rc) return rc;
+  const int nb = ceil_div(T, kPlanBlock);
+  const size_t smem = (size_t)E * 8 * 4 + (size_t)kPlanBlock * k * 2;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(topk_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    attr_set = true;
+  }
+  int32_t* cnt = ws_ptr<int32_t>(ws, L.cnt);
+  int32_t* base = ws_ptr<int32_t>(ws, L.base);
+  int32_t* rank = ws_ptr<int32_t>(ws, L.rank);
+  topk_plan_kernel<<<nb, 512, smem, st>>>(score, key, dead, T, E, k, topk_idx, topk_w, cnt, rank, counts, offsets,
+                                          slot_of_row, row_of_slot);
+  rc = launch_status();
+  if (rc || nb == 1) return rc;
+  plan_scan_kernel<<<1, 512, 0, st>>>(cnt, nb, E, base, counts, offsets);
+  rc = launch_status();
+  if (rc) return rc;
+  const long long n = (long long)T * k;
+  const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 4);
+  plan_scatter_kernel<<<blocks, 256, 0, st>>>(topk_idx, rank, base, T, E, k, slot_of_row, row_of_slot);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Combine: out[t] = bf16_rne(((y[t,0] + y[t,1]) + ...) + y[t,k-1]) in fp32, slots in rank order;
+// rows without live slots get +0.0. 8 hidden elements per thread.
+// ---------------------------------------------------------------------------------------------
+__global__ void combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_of_slot, int T, int H,
+                               int k, uint16_t* __restrict__ out) {
+  const int H8 = H / 8;
+  const long long n = (long long)T * H8;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / H8), h8 = (int)(i % H8);
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    const bool live = row_of_slot[(size_t)t * k] >= 0;
+    if (live) {
+      for (int j = 0; j < k; ++j) {
+        const float4* yp = reinterpret_cast<const float4*>(y + ((size_t)t * k + j) * H) + 2 * h8;
+        const float4 a = __ldg(yp), b = __ldg(yp + 1);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        if (j == 0) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = v[q];
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], v[q]);
+        }
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * q] + 0.0f));
+      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * q + 1] + 0.0f));
+      o[q] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(out + (size_t)t * H + 8 * h8) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, uint16_t* out, cudaStream_t st) {
+  const long long n = (long long)s->T * (s->H / 8);
+  if (n == 0) return MOE_OK;
+  const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);
+  combine_kernel<<<blocks, 256, 0, st>>>(y, row_of_slot, s->T, s->H, s->k, out);
+  return launch_status();
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_route_topk(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* bias,
+                              const uint8_t* dead, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                              int32_t* expert_offsets, int32_t* slot_of_row, int32_t* row_of_slot, void* ws,
+                              size_t ws_bytes, void* stream) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!expert_counts || !expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0 && (!x || !w_router || !bias || !topk_idx || !topk_w || !slot_of_row || !row_of_slot))
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(w_router) & 15))
+    return MOE_ERR_INVALID_ARG;
+  int rc = ws_check(s, ws, ws_bytes);
+  if (rc) return rc;
+  return launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, expert_counts, expert_offsets, slot_of_row,
+                      row_of_slot, ws, static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,187 @@
+/*
+ * block_scaled_fp8_moe -- routed-expert MoE layer for GB300 (sm_103a), C ABI.
+ *
+ * The layer (one call of moe_forward):
+ *   router   : logits = x Wr^T (fp32, fixed order), sigmoid, + bias, top-k, weights normalised
+ *   quant    : x -> MXFP8 (E4M3 codes, one UE8M0 scale per 32 along H)
+ *   W13      : per live slot, gate/up projection with FP4 (E2M1) weights, SwiGLU, requant to MXFP8
+ *   W2       : down projection per slot, scaled by the slot's routing weight
+ *   combine  : out[t] = bf16( ((y_0 + y_1) + ...) ), slots in rank order
+ *
+ * Sources, cited by page and section:
+ *  - "New Deepseek 4.1 flash recipe" (NVIDIA developer forum thread):
+ *      post 2 "What changed / Speculative decoding": dead verification rows skip the MoE expert
+ *        weight reads;
+ *      post 4 "Quality and correctness": exact top-k ties break by lowest position;
+ *      post 6 "Why TileLang": every kernel reduces in a fixed order, so a row's result does not
+ *        depend on its batch; "How it works" items 1-3: block-scaled MMA for MXFP8 and FP8 x FP4,
+ *        routed experts with FP8 activations x FP4 weights, 16/32/64-row decode tiles, panel
+ *        rasterisation of weights larger than L2, MoE top-k gate and SwiGLU/quantisation casts.
+ *  - TP4 serving profile README, settings table, "Experts" row: deterministic MoE reduction with a
+ *    per-slot buffer and a fixed-order sum instead of atomics.
+ *
+ * Conventions shared by every entry point
+ *  - All pointers are DEVICE pointers unless stated; the caller owns every buffer. The library
+ *    allocates no device memory and keeps no per-call state.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Calls are
+ *    asynchronous and stream ordered; nothing synchronises the host except
+ *    moe_check_device_status.
+ *  - Return value: MOE_OK or an moe_status code. Argument and shape checks happen on the host
+ *    before any launch; on failure nothing is launched. Launch failures return MOE_ERR_CUDA.
+ *  - Device-side waits are bounded (about one second); an expired wait records an error code in
+ *    the first 4 bytes of the workspace, the kernel unwinds, and moe_check_device_status then
+ *    returns MOE_ERR_TIMEOUT. Zero those 4 bytes once before first use (or call
+ *    moe_check_device_status, which clears them).
+ *  - bf16 tensors travel as uint16_t bit patterns.
+ *  - Supported shapes: H % 128 == 0, I % 64 == 0, 1 <= k <= 32, k <= E <= 1024, T >= 0,
+ *    H <= 16384, I <= 16384. T == 0 is a valid no-op. Anything else -> MOE_ERR_UNSUPPORTED_SHAPE.
+ *
+ * Data layouts (row-major, innermost dimension contiguous)
+ *  x            bf16 [T, H]
+ *  w_router     bf16 [E, H]
+ *  bias         fp32 [E]                  added to the sigmoid score for selection only
+ *  dead         u8   [T] or NULL          non-zero = dead verification row
+ *  xq / xs      u8   [T, H] E4M3 codes / u8 [T, H/32] UE8M0 (byte b means 2^(b-127))
+ *  hq / hs      u8   [S_max, I] / u8 [S_max, HS_PITCH] in plan order, S_max = T*k,
+ *               HS_PITCH = roundup(I, 128) / 32 (bytes past I/32 are padding)
+ *  MXFP4 canonical weights (input of moe_pack_*):
+ *   w13 codes   u8 [E, 2I, H/2]  rows 0..I-1 gate, I..2I-1 up; element 2m in the LOW nibble
+ *   w13 scales  u8 [E, 2I, H/32]
+ *   w2 codes    u8 [E, H, I/2],  w2 scales u8 [E, H, I/32]
+ *  Packed weights (what the GEMMs read; produced once by moe_pack_w13 / moe_pack_w2):
+ *   tiles of 128 weight rows x 128 K elements; codes 8192 B per tile (64 B per row), scales one
+ *   512 B block per tile (row r, K-block b at byte (r % 32) * 16 + (r / 32) * 4 + b).
+ *   W13 tile (e, m, kc): rows 0..63 = gate rows 64m..64m+63, rows 64..127 = the matching up rows.
+ *   W2 tile (e, n, kc): rows 128n..128n+127. K past the end of a row is zero-filled.
+ *  Plan (written by moe_route_topk, S = live slots):
+ *   topk_idx    i32 [T, k]   experts in rank order (key descending, ties -> lower index)
+ *   topk_w      f32 [T, k]   score_j / sum of the k scores (summed in rank order)
+ *   expert_counts  i32 [E]   live slots per expert
+ *   expert_offsets i32 [E+1] exclusive prefix sum of expert_counts
+ *   slot_of_row i32 [T*k]    plan row p (< S) -> slot t*k + j; rows inside an expert by token
+ *   row_of_slot i32 [T*k]    slot t*k + j -> plan row, -1 for dead rows
+ */
+#ifndef BLOCK_SCALED_FP8_MOE_H
+#define BLOCK_SCALED_FP8_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_shape {
+  int32_t T;      /* rows (tokens) in this call                      */
+  int32_t H;      /* hidden size                                      */
+  int32_t E;      /* experts                                          */
+  int32_t k;      /* experts per row                                  */
+  int32_t I;      /* expert intermediate size                         */
+  int32_t flags;  /* bit 0: W13 writes the fp32 SwiGLU debug output   */
+} moe_shape;
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,        /* null pointer where one is required, negative size   */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* shape outside the supported set above               */
+  MOE_ERR_WORKSPACE = 3,          /* workspace pointer null/misaligned or too small       */
+  MOE_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed                    */
+  MOE_ERR_TIMEOUT = 5             /* a bounded device-side wait expired                  */
+} moe_status;
+
+typedef struct moe_intermediates {
+  /* Optional outputs of moe_forward; any member may be NULL (then it lives in the workspace). */
+  int32_t* topk_idx;       /* [T, k]   */
+  float* topk_w;           /* [T, k]   */
+  int32_t* expert_counts;  /* [E]      */
+  int32_t* expert_offsets; /* [E + 1]  */
+  uint8_t* xq;             /* [T, H]   */
+  uint8_t* xs;             /* [T, H/32]*/
+  uint8_t* hq;             /* [T*k, I] plan order */
+  uint8_t* hs;             /* [T*k, HS_PITCH]     */
+  float* swiglu;           /* [T*k, I] fp32 pre-requant SwiGLU, plan order */
+} moe_intermediates;
+
+/* Human-readable name of a status code (static string, never NULL). */
+MOE_API const char* moe_status_string(int status);
+
+/* Bytes of device workspace moe_forward needs for `shape` (256-byte aligned pointer required).
+ * The other entry points need at most this much; 0 on an unsupported shape. */
+MOE_API size_t moe_workspace_bytes(const moe_shape* shape);
+
+/* Bytes of packed codes / packed scales for W13 (gate+up) and W2 of all E experts. */
+MOE_API size_t moe_packed_w13_bytes(const moe_shape* shape, size_t* scale_bytes);
+MOE_API size_t moe_packed_w2_bytes(const moe_shape* shape, size_t* scale_bytes);
+
+/* MXFP4 quantisation of fp32 weights, per 32 consecutive elements of a row:
+ *   s = smallest integer with max|w| <= 6 * 2^s (clamped to [-127, 127]; all-zero block -> -127),
+ *   code = E2M1 round-to-nearest-even of w * 2^-s. Scale byte = s + 127.
+ * w fp32 [rows, cols] -> q u8 [rows, cols/2] (element 2m low nibble), s u8 [rows, cols/32].
+ * cols % 32 == 0. A one-time weight-preparation step, not part of the layer's step. */
+MOE_API int moe_quant_mxfp4(int32_t rows, int32_t cols, const float* w, uint8_t* q, uint8_t* s, void* stream);
+
+/* Canonical MXFP4 weights -> packed tiles (layouts above). Outputs must not alias inputs. */
+MOE_API int moe_pack_w13(const moe_shape* shape, const uint8_t* q, const uint8_t* s, uint8_t* q_packed,
+                 uint8_t* s_packed, void* stream);
+MOE_API int moe_pack_w2(const moe_shape* shape, const uint8_t* q, const uint8_t* s, uint8_t* q_packed,
+                uint8_t* s_packed, void* stream);
+
+/* Router: sigmoid gate with bias-selected top-k and the expert plan.
+ * "New Deepseek 4.1 flash recipe", post 6 "How it works" item 3 (TileKernels MoE top-k gate);
+ * post 4 "Exact indexer selections" (ties by lowest index); post 2 (dead verification rows).
+ * logit[t,e]: h cut into chunks of 64; each chunk summed sequentially in fp32 from +0 with fused
+ * multiply-add; chunk sums added left to right from +0. score = 1 / (1 + exp(-logit)) with a
+ * library-independent exp built from fp32 +, -, *, / (Cody-Waite reduction, degree-7 Taylor
+ * polynomial), key = score + bias[e]. Dead rows are routed (topk_idx/topk_w written) but take no
+ * slot. All outputs are required (non-NULL). ws: workspace of moe_workspace_bytes(shape). */
+MOE_API int moe_route_topk(const moe_shape* shape, const uint16_t* x, const uint16_t* w_router, const float* bias,
+                   const uint8_t* dead, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                   int32_t* expert_offsets, int32_t* slot_of_row, int32_t* row_of_slot, void* ws,
+                   size_t ws_bytes, void* stream);
+
+/* MXFP8 quantisation of bf16 rows ("How it works" item 3, quantisation casts):
+ *   s = smallest integer with max|x| <= 448 * 2^s (clamped to [-127, 127]; zero block -> -127),
+ *   code = E4M3 round-to-nearest-even of x * 2^-s (never saturates). cols % 32 == 0. */
+MOE_API int moe_quant_mxfp8(int32_t rows, int32_t cols, const uint16_t* x, uint8_t* q, uint8_t* s, void* stream);
+
+/* Gate/up grouped GEMM fused with SwiGLU and MXFP8 requantisation, for every live slot:
+ *   g = Wg[e] x^, u = Wu[e] x^ (block-scaled FP8 x FP4 tensor-core MMA, fp32 accumulate),
+ *   a = g * sigmoid(g) * u (fp32), then per 32 along I: the MXFP8 rule of moe_quant_mxfp8.
+ * Writes hq/hs rows in plan order (row p = slot slot_of_row[p]); swiglu_debug (nullable) gets a.
+ * expert_offsets / slot_of_row as produced by moe_route_topk. w13 / w13_s are PACKED weights. */
+MOE_API int moe_w13_swiglu_grouped(const moe_shape* shape, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13,
+                           const uint8_t* w13_s, const int32_t* expert_offsets, const int32_t* slot_of_row,
+                           uint8_t* hq, uint8_t* hs, float* swiglu_debug, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* Down grouped GEMM and fixed-order weighted combine (TP4 profile README, "Experts" row):
+ *   y[slot] = topk_w[slot] * (W2[e] h^[slot]) in fp32 (per-slot buffer in the workspace),
+ *   out[t] = bf16_rne( ((y[t,0] + y[t,1]) + ...) ); rows with no live slot (dead) get +0.0.
+ * w2 / w2_s are PACKED weights. */
+MOE_API int moe_w2_combine_grouped(const moe_shape* shape, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2,
+                           const uint8_t* w2_s, const float* topk_w, const int32_t* expert_offsets,
+                           const int32_t* slot_of_row, const int32_t* row_of_slot, uint16_t* out, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* The whole layer: route -> quant -> W13+SwiGLU+requant -> W2 -> combine, on one stream, no host
+ * synchronisation and no allocation (capturable in a CUDA graph for a fixed shape).
+ * `inter` (nullable) receives the intermediates the caller wants to keep. */
+MOE_API int moe_forward(const moe_shape* shape, const uint16_t* x, const uint16_t* w_router, const float* bias,
+                const uint8_t* dead, const uint8_t* w13, const uint8_t* w13_s, const uint8_t* w2,
+                const uint8_t* w2_s, uint16_t* out, const moe_intermediates* inter, void* ws,
+                size_t ws_bytes, void* stream);
+
+/* Test/debug helper: synchronises `stream`, reads and clears the device status word at the start
+ * of `ws`, and returns MOE_OK or MOE_ERR_TIMEOUT (MOE_ERR_CUDA if the stream itself failed). */
+MOE_API int moe_check_device_status(void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BLOCK_SCALED_FP8_MOE_H */

@@ -1,0 +1,121 @@
+"""GPU parity of the whole layer on small shapes that still span several tiles and ragged tails:
+routing and quantisation bit-exact, SwiGLU within 1e-5, requant codes equal except at oracle-flagged
+boundaries, final output within 2e-2 x RMS; plus batch invariance and dead rows."""
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_fp8_moe_gb300 import synth
+from tests import moe_harness as H
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # name,   T,   H,   E,  k,   I
+    ("tiny", 4, 256, 8, 2, 128),        # BN 16
+    ("c37", 37, 512, 16, 4, 192),       # BN 16, 3 W13 panels, ragged tokens
+    ("c300", 300, 384, 32, 3, 128),     # BN 32, multi-block plan
+    ("c130", 130, 256, 8, 2, 576),      # BN 64, W2 K = 576 (partial last chunk)
+    ("c600", 600, 256, 8, 2, 256),      # BN 128
+]
+
+
+def _inputs(name, T, Hd, E, k, I, dead_frac=0.0):
+    if name == "tiny":
+        return synth.make_inputs_cpu(synth.CONFIGS["tiny"])
+    return synth.make_inputs_cpu(synth.custom(name, T, Hd, E, k, I, seed=T + I, dead_frac=dead_frac))
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_layer_steps_match_oracle(case):
+    inp = _inputs(*case, dead_frac=0.25 if case[0] == "c37" else 0.0)
+    g = H.GpuLayer(inp)
+    r = g.run_steps()
+    ref, w13, w2 = H.oracle_forward(inp)
+    cfg = inp.cfg
+    ro = ref.routing
+    S = int(ro.offsets[-1])
+    # routing and plan bit-exact
+    assert np.array_equal(r["plan"].topk_idx.cpu().numpy(), ro.topk_idx)
+    assert np.array_equal(r["plan"].topk_w.cpu().numpy(), ro.topk_w)
+    assert np.array_equal(r["plan"].slot_of_row.cpu().numpy()[:S], ro.slot_of_row)
+    # activation quantisation bit-exact
+    assert np.array_equal(r["xq"].cpu().numpy(), ref.xq)
+    assert np.array_equal(r["xs"].cpu().numpy(), ref.xs)
+    # pre-requant SwiGLU within 1e-5 (relative to max(|a|, row rms))
+    a_ref = ref.w13.a
+    a_gpu = r["dbg"].cpu().numpy()[:S].astype(np.float64)
+    rms = np.sqrt(np.mean(a_ref ** 2, axis=1, keepdims=True))
+    tol = H.SWIGLU_REL * np.maximum(np.abs(a_ref), rms)
+    assert np.all(np.abs(a_gpu - a_ref) <= tol), float(np.max(np.abs(a_gpu - a_ref) / tol))
+    # requant codes equal except at flagged boundaries
+    bad_q, bad_s = H.e4m3_codes_match(r["hq"].cpu().numpy()[:S], r["hs"].cpu().numpy()[:S], ref.w13.hq,
+                                      ref.w13.hs, ref.w13.flip_ok)
+    assert bad_q == 0 and bad_s == 0
+    # final output
+    out = H.bf16_to_np(r["out"])
+    H.assert_out_close(out, ref.out)
+    dead = inp.dead.numpy().astype(bool)
+    assert np.all(out[dead] == 0.0) and not np.any(np.signbit(out[dead]))
+
+
+@pytest.mark.parametrize("case", CASES[:3], ids=[c[0] for c in CASES[:3]])
+def test_forward_equals_steps_and_oracle(case):
+    inp = _inputs(*case)
+    g = H.GpuLayer(inp)
+    out_f = g.forward()
+    out_s = g.run_steps(use_dead=False)["out"]
+    assert torch.equal(out_f, out_s)
+    ref, _, _ = H.oracle_forward(inp, use_dead=False)
+    H.assert_out_close(H.bf16_to_np(out_f), ref.out)
+
+
+def test_batch_invariance_rows_alone_subsets_and_permutation():
+    inp = _inputs("c300", 300, 384, 32, 3, 128)
+    g = H.GpuLayer(inp)
+    full = g.forward()
+    for t in (0, 1, 17, 299):
+        one = g.forward(x=g.x[t:t + 1].contiguous())
+        assert torch.equal(one[0], full[t])
+    for lo, hi in ((0, 6), (5, 53), (100, 300)):
+        part = g.forward(x=g.x[lo:hi].contiguous())
+        assert torch.equal(part, full[lo:hi])
+    perm = torch.randperm(300, generator=torch.Generator().manual_seed(0)).cuda()
+    shuf = g.forward(x=g.x[perm].contiguous())
+    assert torch.equal(shuf, full[perm])
+
+
+def test_dead_rows_zero_and_live_rows_unchanged():
+    inp = _inputs("c37", 37, 512, 16, 4, 192)
+    g = H.GpuLayer(inp)
+    full = g.forward()
+    dead = torch.zeros(37, dtype=torch.uint8, device="cuda")
+    dead[[0, 5, 36]] = 1
+    d = g.forward(dead=dead)
+    assert torch.all(d[dead.bool()] == 0) and not torch.any(torch.signbit(d[dead.bool()].float()))
+    assert torch.equal(d[~dead.bool()], full[~dead.bool()])
+    all_dead = g.forward(dead=torch.ones(37, dtype=torch.uint8, device="cuda"))
+    assert torch.all(all_dead == 0)
+
+
+def test_one_expert_takes_every_slot_and_empty_batch():
+    inp = _inputs("c130", 130, 256, 8, 2, 576)
+    inp.bias[:] = 0.0
+    inp.bias[3] = 50.0
+    inp.bias[6] = 40.0                 # every row picks experts 3 and 6
+    g = H.GpuLayer(inp)
+    r = g.run_steps()
+    counts = r["plan"].expert_counts.cpu().numpy()
+    assert counts[3] == 130 and counts[6] == 130 and counts.sum() == 260
+    ref, _, _ = H.oracle_forward(inp)
+    H.assert_out_close(H.bf16_to_np(r["out"]), ref.out)
+    empty = g.forward(x=g.x[:0].contiguous())
+    assert empty.shape == (0, 256)
+
+
+def test_repeated_calls_bit_identical():
+    inp = _inputs("c600", 600, 256, 8, 2, 256)
+    g = H.GpuLayer(inp)
+    first = g.forward().clone()
+    for _ in range(20):
+        assert torch.equal(g.forward(), first)

@@ -1,0 +1,66 @@
+"""GPU parity: router logits / sigmoid / top-k / weights / plan, bit-exact against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe as M
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _route_case(T, H, E, k, seed, dead_frac=0.0, ties=False, bias_scale=0.1):
+    from block_scaled_fp8_moe_gb300 import binding as B
+    rng = np.random.default_rng(seed)
+    x = _bf16(rng.standard_normal((T, H)))
+    wr = _bf16(rng.standard_normal((E, H)) * 0.02)
+    bias = (rng.standard_normal(E) * bias_scale).astype(np.float32)
+    if ties:
+        wr[E - 1] = wr[1]
+        wr[E // 2] = wr[0]
+        bias[E - 1] = bias[1]
+        bias[E // 2] = bias[0]
+    dead = (rng.random(T) < dead_frac).astype(np.uint8)
+    shp = B.shape(T, H, E, k, 64)
+    ws = B.alloc_workspace(shp)
+    plan = B.moe_route_topk(shp, x.cuda(), wr.cuda(), torch.from_numpy(bias).cuda(),
+                            torch.from_numpy(dead).cuda() if dead_frac > 0 else None, ws)
+    B.moe_check_device_status(ws)
+    ref = M.route(x.float().numpy(), wr.float().numpy(), bias, k, dead.astype(bool) if dead_frac > 0 else None)
+    return plan, ref
+
+
+@pytest.mark.parametrize("T,H,E,k", [
+    (1, 256, 8, 2), (4, 256, 8, 2), (6, 4096, 256, 8), (7, 512, 64, 6), (16, 256, 32, 4), (17, 256, 32, 4),
+    (33, 384, 16, 3), (65, 128, 8, 8), (256, 256, 64, 8), (257, 256, 64, 8), (600, 512, 40, 5),
+])
+def test_route_bit_exact(T, H, E, k):
+    plan, ref = _route_case(T, H, E, k, seed=T * 31 + E)
+    assert np.array_equal(plan.topk_idx.cpu().numpy(), ref.topk_idx)
+    assert np.array_equal(plan.topk_w.cpu().numpy().view(np.uint32), ref.topk_w.view(np.uint32))
+    assert np.array_equal(plan.expert_counts.cpu().numpy(), ref.counts)
+    assert np.array_equal(plan.expert_offsets.cpu().numpy(), ref.offsets)
+    S = int(ref.offsets[-1])
+    assert np.array_equal(plan.slot_of_row.cpu().numpy()[:S], ref.slot_of_row)
+    assert np.array_equal(plan.row_of_slot.cpu().numpy()[:T * k], ref.row_of_slot)
+
+
+@pytest.mark.parametrize("T", [5, 48, 300])
+def test_route_dead_rows_and_ties(T):
+    plan, ref = _route_case(T, 256, 16, 4, seed=T, dead_frac=0.3, ties=True)
+    assert np.array_equal(plan.topk_idx.cpu().numpy(), ref.topk_idx)
+    assert np.array_equal(plan.topk_w.cpu().numpy(), ref.topk_w)
+    assert np.array_equal(plan.expert_offsets.cpu().numpy(), ref.offsets)
+    S = int(ref.offsets[-1])
+    assert np.array_equal(plan.slot_of_row.cpu().numpy()[:S], ref.slot_of_row)
+    assert np.array_equal(plan.row_of_slot.cpu().numpy()[:T * 4], ref.row_of_slot)
+
+
+def test_route_skewed_bias_all_slots_to_few_experts():
+    plan, ref = _route_case(300, 256, 16, 2, seed=9, bias_scale=10.0)
+    assert np.array_equal(plan.topk_idx.cpu().numpy(), ref.topk_idx)
+    assert np.array_equal(plan.expert_counts.cpu().numpy(), ref.counts)
+    assert (ref.counts == 0).sum() >= 10          # most experts empty

@@ -23,6 +23,7 @@ EXPORTED = [
     "moe_status_string", "moe_workspace_bytes", "moe_packed_w13_bytes", "moe_packed_w2_bytes",
     "moe_quant_mxfp4", "moe_pack_w13", "moe_pack_w2", "moe_route_topk", "moe_quant_mxfp8",
     "moe_w13_swiglu_grouped", "moe_w2_combine_grouped", "moe_forward", "moe_check_device_status",
+    "moe_route_topk_noalloc",
 ]
 
 
@@ -58,6 +59,7 @@ lib.moe_w13_swiglu_grouped.argtypes = [_SHP] + [_P] * 9 + [_P, _SZ, _P]
 lib.moe_w2_combine_grouped.argtypes = [_SHP] + [_P] * 9 + [_P, _SZ, _P]
 lib.moe_forward.argtypes = [_SHP] + [_P] * 9 + [ctypes.POINTER(MoeIntermediates), _P, _SZ, _P]
 lib.moe_check_device_status.argtypes = [_P, _P]
+lib.moe_route_topk_noalloc.argtypes = [_SHP] + [_P] * 10 + [_P]
 for _n in EXPORTED:
     if _n not in ("moe_status_string", "moe_workspace_bytes", "moe_packed_w13_bytes", "moe_packed_w2_bytes"):
         getattr(lib, _n).restype = ctypes.c_int
@@ -185,6 +187,19 @@ def moe_route_topk(shp: MoeShape, x, w_router, bias, dead, ws, plan: Plan | None
         _ptr(bias, torch.float32, E, "bias"), _ptr(dead, torch.uint8, T, "dead"),
         _ptr(plan.topk_idx), _ptr(plan.topk_w), _ptr(plan.expert_counts), _ptr(plan.expert_offsets),
         _ptr(plan.slot_of_row), _ptr(plan.row_of_slot), _ptr(ws), ws.numel(), _stream(stream)), "moe_route_topk")
+    return plan
+
+
+def moe_route_topk_noalloc(shp: MoeShape, x, w_router, bias, dead, plan: Plan | None = None,
+                           stream=None) -> Plan:
+    """moe_route_topk without a workspace (scratch inside the library; see include/moe.h)."""
+    plan = Plan(shp, x.device) if plan is None else plan
+    T, H, E = shp.T, shp.H, shp.E
+    _check(lib.moe_route_topk_noalloc(
+        ctypes.byref(shp), _ptr(x, torch.bfloat16, T * H, "x"), _ptr(w_router, torch.bfloat16, E * H, "w_router"),
+        _ptr(bias, torch.float32, E, "bias"), _ptr(dead, torch.uint8, T, "dead"),
+        _ptr(plan.topk_idx), _ptr(plan.topk_w), _ptr(plan.expert_counts), _ptr(plan.expert_offsets),
+        _ptr(plan.slot_of_row), _ptr(plan.row_of_slot), _stream(stream)), "moe_route_topk_noalloc")
     return plan
 
 

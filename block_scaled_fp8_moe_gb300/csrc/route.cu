@@ -473,3 +473,84 @@ extern "C" int moe_route_topk(const moe_shape* s, const uint16_t* x, const uint1
   return launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, expert_counts, expert_offsets, slot_of_row,
                       row_of_slot, ws, static_cast<cudaStream_t>(stream));
 }
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free router entry point.
+//
+// Some callers cannot hand this library a workspace: a serving engine that reserved all of HBM
+// for its own pool at start-up has no bytes left for a cudaMalloc, and code running inside a host
+// framework's custom-op or callback may be forbidden from allocating at all. For them the router
+// keeps its scratch (sigmoid scores and selection keys, 4 bytes each per (row, expert)) in this
+// file-scope device array instead of the caller's workspace. Every GPU that loads the library
+// holds the array (512 KiB) until the process exits. All calls share it, so calls that may overlap
+// on the GPU (different streams, or different host threads) race on it; callers must serialise
+// them. Each call writes every scratch element it reads before reading it, so nothing needs to be
+// cleared between calls.
+// ---------------------------------------------------------------------------------------------
+namespace moe {
+constexpr int kNoAllocMaxRowsTimesExperts = 65536;        // T * E limit (and T <= kPlanBlock)
+static __device__ __align__(256) float g_route_scratch[2 * kNoAllocMaxRowsTimesExperts];
+}  // namespace moe
+
+#include <mutex>
+
+extern "C" int moe_route_topk_noalloc(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
+                                      const float* bias, const uint8_t* dead, int32_t* topk_idx, float* topk_w,
+                                      int32_t* expert_counts, int32_t* expert_offsets, int32_t* slot_of_row,
+                                      int32_t* row_of_slot, void* stream) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (s->T > kPlanBlock || (int64_t)s->T * s->E > kNoAllocMaxRowsTimesExperts) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!expert_counts || !expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0 && (!x || !w_router || !bias || !topk_idx || !topk_w || !slot_of_row || !row_of_slot))
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(w_router) & 15))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = s->T, E = s->E, k = s->k, H = s->H;
+  if (T == 0) {
+    if (cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, st) != cudaSuccess ||
+        cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  // Set-up, once per device and with that device current: the host-side name of the array is
+  // not a device address, so ask the runtime for it.
+  static std::mutex mu;
+  static float* scratch_of_device[64] = {};
+  static bool smem_attr_set = false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  float* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!scratch_of_device[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+      scratch_of_device[dev] = static_cast<float*>(p);
+    }
+    if (!smem_attr_set) {
+      if (cudaFuncSetAttribute(topk_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
+          cudaSuccess)
+        return MOE_ERR_CUDA;
+      smem_attr_set = true;
+    }
+    scratch = scratch_of_device[dev];
+  }
+  float* score = scratch;
+  float* key = scratch + (size_t)T * E;
+  if (T <= kSmallT) {
+    router_small_kernel<<<ceil_div(E, 8), 256, 0, st>>>(x, w_router, bias, T, H, E, score, key);
+  } else {
+    dim3 grid(ceil_div(T, 64), ceil_div(E, 64));
+    router_tiled_kernel<<<grid, 256, 0, st>>>(x, w_router, bias, T, H, E, score, key);
+  }
+  int rc = launch_status();
+  if (rc) return rc;
+  // one plan block (T <= kPlanBlock): the kernel scans and scatters itself and never touches the
+  // multi-block count/rank arrays
+  const size_t smem = (size_t)E * 8 * 4 + (size_t)kPlanBlock * k * 2;
+  topk_plan_kernel<<<1, 512, smem, st>>>(score, key, dead, T, E, k, topk_idx, topk_w, nullptr, nullptr,
+                                         expert_counts, expert_offsets, slot_of_row, row_of_slot);
+  return launch_status();
+}

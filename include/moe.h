@@ -177,6 +177,21 @@ MOE_API int moe_forward(const moe_shape* shape, const uint16_t* x, const uint16_
                 const uint8_t* w2_s, uint16_t* out, const moe_intermediates* inter, void* ws,
                 size_t ws_bytes, void* stream);
 
+/* Allocation-free variant of moe_route_topk, for callers that cannot allocate device memory:
+ * engines that reserved all of HBM for their own pool at start-up, or code running inside a host
+ * framework's callback where allocation is not allowed. It takes no workspace; its scratch lives in
+ * a 512 KiB array inside the library, present on every GPU that loads it until exit. The pages have
+ * no counterpart to this entry point: it is an interface convenience, not part of the method.
+ * Same arguments and results as moe_route_topk without ws/ws_bytes. Limits: T <= 256 and
+ * T * E <= 65536, otherwise MOE_ERR_UNSUPPORTED_SHAPE and nothing is launched. The first call on a
+ * device looks up the array's device address (once per device; make that first call before any
+ * stream capture). All calls share the array: calls that can overlap on the GPU race and must be
+ * serialised by the caller. Nothing in it needs clearing between calls. Allocates nothing. */
+MOE_API int moe_route_topk_noalloc(const moe_shape* shape, const uint16_t* x, const uint16_t* w_router,
+                                   const float* bias, const uint8_t* dead, int32_t* topk_idx, float* topk_w,
+                                   int32_t* expert_counts, int32_t* expert_offsets, int32_t* slot_of_row,
+                                   int32_t* row_of_slot, void* stream);
+
 /* Test/debug helper: synchronises `stream`, reads and clears the device status word at the start
  * of `ws`, and returns MOE_OK or MOE_ERR_TIMEOUT (MOE_ERR_CUDA if the stream itself failed). */
 MOE_API int moe_check_device_status(void* ws, void* stream);

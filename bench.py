@@ -41,8 +41,26 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=1)
+    ap.add_argument("--tokens", type=int, default=0, help="override T of the workload (profiling aid)")
+    ap.add_argument("--experts", type=int, default=0, help="override E of the workload (profiling aid)")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
+
+
+def reduce_max(value: float, device) -> float:
+    """Max over ranks of a per-rank float (identity without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def tokens_per_s(world: int, rows_per_rank: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank processes its own batch of rows each step."""
+    return world * rows_per_rank * steps / (max_ms / 1e3)
 
 
 def workload_name(cfg):
@@ -193,6 +211,9 @@ def gpu_arm(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     cfg = synth.CONFIGS[args.config]
+    if args.tokens or args.experts:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, name=cfg.name + "-reduced", T=args.tokens or cfg.T, E=args.experts or cfg.E)
 
     inp = synth.make_inputs_cuda(cfg, device=dev)
     layer = B.MoeLayer.from_fp32(inp.w_router, inp.bias, inp.w13, inp.w2, cfg.k)
@@ -233,14 +254,38 @@ def gpu_arm(args):
     barrier()
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(sum(step_ms), dev)
     B.moe_check_device_status(ws)
     ms_per_step = total_ms / args.steps
-    value = world * cfg.T * args.steps / (total_ms / 1e3)
+    value = tokens_per_s(world, cfg.T, args.steps, total_ms)
+
+    # ---- the same step replayed from a CUDA graph (launch overhead removed) ----
+    graph_ms = None
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            layer.forward(x, dead=dead, out=out)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layer.forward(x, dead=dead, out=out)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            gev[i][0].record(stream)
+            g.replay()
+            gev[i][1].record(stream)
+        torch.cuda.synchronize()
+        graph_ms = sum(a.elapsed_time(b) for a, b in gev) / args.steps
+        B.moe_check_device_status(ws)
+    except Exception as exc:  # graph capture is a reported variant, not the headline
+        graph_ms = f"unavailable: {type(exc).__name__}: {exc}"
 
     # ---- dominant kernel alone: the four step entry points, events around W13 and W2 ----
     plan = B.Plan(shp, dev)
@@ -313,12 +358,9 @@ def gpu_arm(args):
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
     barrier()
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e2e_ms, dev)
     h2d = x_host.numel() * 2 + (dead_host.numel() if dead_host is not None else 0)
-    e2e = {"value": world * cfg.T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+    e2e = {"value": tokens_per_s(world, cfg.T, args.steps, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_host.numel() * 2}
 
     cpu = None
@@ -337,6 +379,9 @@ def gpu_arm(args):
             "e2e": e2e, "gpu_launches": launches_per_step(cfg) * args.steps, "clocks": clk,
             "roofline": roofline,
             "kernels_ms": {"w13": round(w13_ms, 5), "w2_combine": round(w2_ms, 5)},
+            "graph_replay": ({"ms_per_step": round(graph_ms, 5),
+                              "value": round(world * cfg.T / (graph_ms / 1e3), 2)}
+                             if isinstance(graph_ms, float) else graph_ms),
             "cpu_baseline": cpu,
         }
         print(json.dumps(line))

@@ -23,7 +23,7 @@ EXPORTED = [
     "moe_status_string", "moe_workspace_bytes", "moe_packed_w13_bytes", "moe_packed_w2_bytes",
     "moe_quant_mxfp4", "moe_pack_w13", "moe_pack_w2", "moe_route_topk", "moe_quant_mxfp8",
     "moe_w13_swiglu_grouped", "moe_w2_combine_grouped", "moe_forward", "moe_check_device_status",
-    "moe_route_topk_noalloc",
+    "moe_route_topk_noalloc", "moe_selftest_timeout",
 ]
 
 
@@ -60,6 +60,7 @@ lib.moe_w2_combine_grouped.argtypes = [_SHP] + [_P] * 9 + [_P, _SZ, _P]
 lib.moe_forward.argtypes = [_SHP] + [_P] * 9 + [ctypes.POINTER(MoeIntermediates), _P, _SZ, _P]
 lib.moe_check_device_status.argtypes = [_P, _P]
 lib.moe_route_topk_noalloc.argtypes = [_SHP] + [_P] * 10 + [_P]
+lib.moe_selftest_timeout.argtypes = [_P, ctypes.c_uint64, _P]
 for _n in EXPORTED:
     if _n not in ("moe_status_string", "moe_workspace_bytes", "moe_packed_w13_bytes", "moe_packed_w2_bytes"):
         getattr(lib, _n).restype = ctypes.c_int
@@ -241,6 +242,10 @@ def moe_forward(shp: MoeShape, x, w_router, bias, dead, w13p, w13sp, w2p, w2sp, 
         _ptr(w2p, torch.uint8), _ptr(w2sp, torch.uint8), _ptr(out, torch.bfloat16, shp.T * shp.H, "out"),
         ctypes.byref(im) if im is not None else None, _ptr(ws), ws.numel(), _stream(stream)), "moe_forward")
     return out
+
+
+def moe_selftest_timeout(ws, limit_ns: int, stream=None) -> None:
+    _check(lib.moe_selftest_timeout(_ptr(ws), int(limit_ns), _stream(stream)), "moe_selftest_timeout")
 
 
 def moe_check_device_status(ws, stream=None) -> None:

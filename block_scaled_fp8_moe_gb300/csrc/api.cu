@@ -100,10 +100,14 @@ extern "C" int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t
   uint32_t* status = ws_ptr<uint32_t>(ws, L.status);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  rc = launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, ws, st);
+  bool quant_done = false;
+  rc = launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, ws, st,
+                    xq, xs, &quant_done);
   if (rc) return rc;
-  rc = launch_quant_mxfp8(s->T, s->H, x, xq, xs, st);
-  if (rc) return rc;
+  if (!quant_done) {
+    rc = launch_quant_mxfp8(s->T, s->H, x, xq, xs, st);
+    if (rc) return rc;
+  }
   rc = launch_w13(s, xq, xs, w13, w13_s, offsets, slot_of_row, hq, hs, im.swiglu, status, st);
   if (rc) return rc;
   rc = launch_w2(s, hq, hs, w2, w2_s, topk_w, offsets, slot_of_row, y, status, st);
@@ -123,4 +127,31 @@ extern "C" int moe_check_device_status(void* ws, void* stream) {
     return MOE_ERR_TIMEOUT;
   }
   return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Self-test of the bounded-wait machinery: one thread waits on an mbarrier that nothing ever
+// arrives at, with a caller-chosen limit. The wait expires, records its code in the status word,
+// and the kernel returns normally -- the context stays usable.
+// ---------------------------------------------------------------------------------------------
+#include "ptx.cuh"
+
+namespace moe {
+__global__ void selftest_timeout_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    mbar_wait(&bar, 0, limit_ns, &abort_flag, status, DEV_TIMEOUT_FULL);
+  }
+}
+}  // namespace moe
+
+extern "C" int moe_selftest_timeout(void* ws, uint64_t limit_ns, void* stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return MOE_ERR_WORKSPACE;
+  if (limit_ns > 2000000000ull) return MOE_ERR_INVALID_ARG;
+  selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint32_t*>(ws), limit_ns);
+  return launch_status();
 }

@@ -95,9 +95,11 @@ inline int num_sms() {
 
 // Internal launchers (defined in the .cu files), all asynchronous on `st`.
 int launch_quant_mxfp8(int rows, int cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st);
+// When xq/xs are given and the small-batch router runs, it also writes the MXFP8 quantisation of x
+// and sets *quant_done.
 int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, const uint8_t* dead,
                  int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
-                 int32_t* row_of_slot, void* ws, cudaStream_t st);
+                 int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done);
 int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
                const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
                uint32_t* status, cudaStream_t st);

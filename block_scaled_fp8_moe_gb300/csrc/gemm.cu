@@ -27,14 +27,19 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "mx.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 
 constexpr int kThreads = 256;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
-constexpr int kSfCol0 = 128;                        // first TMEM column of the scale ring
-constexpr int kTmemCols = 256;
+#ifndef MOE_STAGES_SMALL
+#define MOE_STAGES_SMALL 5          // pipeline stages for token tiles <= 16
+#endif
+#ifndef MOE_CTAS_SMALL
+#define MOE_CTAS_SMALL 2            // resident CTAs per SM for token tiles <= 16
+#endif
 
 struct GemmParams {
   // B side (activations)
@@ -65,7 +70,15 @@ struct Smem {
   static constexpr int kStageA = 16384;
   static constexpr int kStageB = BN * 128;
   static constexpr int kStageBytes = kStageA + kStageB + 1024;   // + 512 B A scales + 512 B B scales
-  static constexpr int kStages = (BN <= 16) ? 5 : (BN <= 64 ? 4 : 3);
+  static constexpr int kStages = (BN <= 16) ? MOE_STAGES_SMALL : (BN <= 64 ? 4 : 6);
+  static constexpr int kCtasPerSm = (BN <= 16) ? MOE_CTAS_SMALL : (BN <= 64 ? 2 : 1);
+  // TMEM: two accumulator slots of kAccStride columns, then the ring of scale blocks
+  static constexpr int kAccStride = (BN <= 64) ? 64 : 128;
+  static constexpr int kSfCol = 2 * kAccStride;
+  static constexpr int kTmemCols = (BN <= 64) ? 256 : 512;
+  // wide token tiles read the activation operand with TMA (a 2D box for W2's contiguous plan rows,
+  // four-row gathers for W13's token rows) instead of cp.async
+  static constexpr bool kTmaB = (BN >= 128);
   static constexpr int kTiles = kStages * kStageBytes;
   static constexpr int kXchg = 64 * 16 * 4;                     // W13 epilogue exchange
   static constexpr int kMisc = 1024;                            // barriers, flags
@@ -97,31 +110,14 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-__device__ __forceinline__ uint32_t e4m3_pair(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ int mx8_scale_exp(float amax) {
-  uint32_t b = __float_as_uint(amax);
-  if (b == 0) return -127;
-  int e = (int)((b >> 23) & 0xFF);
-  uint32_t man = b & 0x7FFFFF;
-  if (e == 0) {
-    int sh = __clz(man) - 8;
-    man = (man << sh) & 0x7FFFFF;
-    e = 1 - sh;
-  }
-  int s = (e - 127) - 8 + (man > 0x600000u ? 1 : 0);
-  return max(-127, min(126, s));
-}
-
 template <int BN, bool W13>
 __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                                                    const __grid_constant__ CUtensorMap tmap_b,
                                                                     const GemmParams p) {
   using L = Smem<BN>;
   constexpr int S = L::kStages;
+  constexpr int NACC = 2;                          // accumulator slots in TMEM
+  constexpr bool kTmaB = L::kTmaB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = base;
@@ -129,9 +125,9 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
   uint8_t* misc = base + L::kTiles + L::kXchg;
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);
   uint64_t* empty = full + S;
-  uint64_t* acc_full = empty + S;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* drain = acc_empty + 1;
+  uint64_t* acc_full = empty + S;          // [NACC]
+  uint64_t* acc_empty = acc_full + 2;      // [NACC]
+  uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   long long* s_rows = reinterpret_cast<long long*>(misc + L::kMisc);   // [BN] gather row or -1
@@ -146,16 +142,18 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1 + 64);
+      mbar_init(&full[s], 1 + (kTmaB ? 32 : 64));
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
     mbar_init(drain, 1);
     mbar_fence_init();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc(tmem_slot, L::kTmemCols);
     tmem_relinquish();
   }
   __syncthreads();
@@ -177,7 +175,10 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       run += (s_off[e + 1] - s_off[e] + BN - 1) / BN;
     }
     if (lane == 31) s_cum[E] = incl * p.MT;
-    if (threadIdx.x == 0) prefetch_tmap(&tmap_a);
+    if (threadIdx.x == 0) {
+      prefetch_tmap(&tmap_a);
+      if (kTmaB) prefetch_tmap(&tmap_b);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -203,25 +204,70 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      const int KC = p.KC;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         int e, m, nt, row0, nrows;
         decode(w, e, m, nt, row0, nrows);
-        const int tile0 = (e * p.MT + m) * p.KC;
-        for (int kc = 0; kc < p.KC; ++kc) {
+        const int tile0 = (e * p.MT + m) * KC;
+        for (int kc = 0; kc < KC; ++kc) {
           if (!mbar_wait(&empty[stage], phase ^ 1, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_EMPTY)) {
             ok = false;
             break;
           }
           uint8_t* sA = tiles + stage * L::kStageBytes;
           uint8_t* sSFA = sA + L::kStageA + L::kStageB;
-          mbar_arrive_expect_tx(&full[stage], kTileCodeBytes + kTileScaleBytes);
+          mbar_arrive_expect_tx(&full[stage], kTileCodeBytes + kTileScaleBytes + (kTmaB ? L::kStageB : 0));
           tma_load_2d(sA, &tmap_a, 0, (tile0 + kc) * 128, &full[stage]);
           bulk_load(sSFA, p.a_scales + (size_t)(tile0 + kc) * kTileScaleBytes, kTileScaleBytes, &full[stage]);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
     }
-  } else if (warp == 1 || warp == 3) {
+  } else if (kTmaB && warp == 1) {
+    // ===================== TMA producer: activations (wide token tiles) =====================
+    // W13: lane i gathers plan rows 4i..4i+3 (their token rows of xq) with one four-row TMA gather;
+    // W2: lane 0 loads the tile's contiguous plan rows of hq with one 2D TMA box. Either way the
+    // rows past the tile's end are some other valid row (or TMA's zero fill); their columns are
+    // never stored. Every lane also copies the scale bytes of its rows lane + 32 i.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total; w += gridDim.x) {
+      int e, m, nt, row0, nrows;
+      decode(w, e, m, nt, row0, nrows);
+      int grow[4];
+      long long srow[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = 4 * lane + i;
+        grow[i] = W13 ? p.slot_of_row[row0 + min(c, nrows - 1)] / p.k : 0;
+        const int cs = lane + 32 * i;
+        srow[i] = cs < nrows ? (W13 ? (long long)(p.slot_of_row[row0 + cs] / p.k) : (long long)(row0 + cs)) : -1;
+      }
+      for (int kc = 0; kc < p.KC; ++kc) {
+        if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
+        if (ok) {
+          uint8_t* sB = tiles + stage * L::kStageBytes + L::kStageA;
+          uint8_t* sSFB = sB + L::kStageB + 512;
+          if constexpr (W13) {
+            tma_gather4(sB + 4 * lane * 128, &tmap_b, kc * 128, grow[0], grow[1], grow[2], grow[3], &full[stage]);
+          } else {
+            if (lane == 0) tma_load_2d(sB, &tmap_b, kc * 128, row0, &full[stage]);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = lane + 32 * i;
+            const bool valid = srow[i] >= 0;
+            const uint8_t* src = valid ? p.bs + srow[i] * p.b_scale_pitch + kc * 4 : p.bs;
+            cp_async_4(sSFB + (c & 31) * 16 + (c >> 5) * 4, src, valid ? 4u : 0u);
+          }
+          cp_async_arrive_noinc(&full[stage]);
+        }
+        if (++stage == S) { stage = 0; phase ^= 1; }
+      }
+    }
+    cp_async_wait_all();
+  } else if (!kTmaB && (warp == 1 || warp == 3)) {
     // ===================== gather producers: activations =====================
     // After an expired wait the loops keep running (doing nothing) so that both warps meet at
     // every named barrier.
@@ -276,12 +322,15 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       bool ok = true;
       const uint32_t idesc_base = idesc_mxf8f6f4(5 /*E2M1*/, 0 /*E4M3*/, 128, BN, 0, 0);
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it) {
-        if (it > 0 &&
-            !mbar_wait(acc_empty, (it - 1) & 1, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_DRAIN)) {
+        const int acc = (NACC == 2) ? (it & 1) : 0;
+        const int use = (NACC == 2) ? (it >> 1) : it;       // how many times this slot was used before
+        if (use > 0 &&
+            !mbar_wait(&acc_empty[acc], (use - 1) & 1, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_DRAIN)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * L::kAccStride);
         for (int kc = 0; kc < p.KC; ++kc) {
           if (!mbar_wait(&full[stage], phase, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_FULL)) {
             ok = false;
@@ -293,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
           uint8_t* sB = sA + L::kStageA;
           uint8_t* sSFA = sB + L::kStageB;
           uint8_t* sSFB = sSFA + 512;
-          const uint32_t tsfa = tmem + kSfCol0 + stage * 8;
+          const uint32_t tsfa = tmem + L::kSfCol + stage * 8;
           const uint32_t tsfb = tsfa + 4;
           tc_cp_32x128b_warpx4(tsfa, smem_desc(smem_u32(sSFA), 16, 128, 0));
           tc_cp_32x128b_warpx4(tsfb, smem_desc(smem_u32(sSFB), 16, 128, 0));
@@ -302,20 +351,20 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
             const uint64_t ad = smem_desc(smem_u32(sA) + kb * 32, 16, 1024, 2);
             const uint64_t bd = smem_desc(smem_u32(sB) + kb * 32, 16, 1024, 2);
             const uint32_t id = idesc_base | ((uint32_t)kb << 4) | ((uint32_t)kb << 29);
-            mma_mxf8f6f4(tmem, ad, bd, id, tsfa, tsfb, (kc > 0 || kb > 0) ? 1u : 0u);
+            mma_mxf8f6f4(d_tmem, ad, bd, id, tsfa, tsfb, (kc > 0 || kb > 0) ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        tc_commit(acc_full);
+        tc_commit(&acc_full[acc]);
       }
       // every MMA this thread issued has completed before TMEM is released
       tc_commit(drain);
       mbar_wait(drain, 0, kWaitLimitNs, abort_flag, nullptr, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 4) {
     // ===================== epilogue (warps 4..7 -> TMEM lanes 32 (warp - 4)) =====================
     // As above, an expired wait turns the remaining iterations into no-ops that still meet at the
     // named barriers.
@@ -326,35 +375,47 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
     for (int w = blockIdx.x; w < total; w += gridDim.x, ++it) {
       int e, m, nt, row0, nrows;
       decode(w, e, m, nt, row0, nrows);
-      if (ok) ok = warp_wait(acc_full, it & 1, abort_flag, p.status, DEV_TIMEOUT_ACCUM);
+      const int acc = (NACC == 2) ? (it & 1) : 0;
+      const int use = (NACC == 2) ? (it >> 1) : it;
+      if (ok) ok = warp_wait(&acc_full[acc], use & 1, abort_flag, p.status, DEV_TIMEOUT_ACCUM);
       tc_fence_after();
+      const uint32_t d_tmem = tmem + (uint32_t)(acc * L::kAccStride);
       for (int c0 = 0; c0 < BN; c0 += 16) {
         uint32_t r[16];
         if (ok) {
-          tmem_ld16(tmem + lane_base + c0, r);
+          tmem_ld16(d_tmem + lane_base + c0, r);
           tmem_ld_wait();
         }
         if constexpr (W13) {
-          // q 0,1: gate features 64m + 32q + lane; q 2,3: the matching up features
-          if (q >= 2 && ok) {
+          // q 0,1 hold gate features 64m + 32q + lane, q 2,3 the matching up features. Each warp
+          // pair swaps half of the chunk through shared memory: gate warps finish columns 0..7,
+          // up warps columns 8..15.
+          float* xg = xchg;                  // [8][64] gate values of columns 8..15
+          float* xu = xchg + 8 * 64;         // [8][64] up values of columns 0..7
+          const int fq = q & 1;
+          if (ok) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) xchg[c * 64 + 32 * (q - 2) + lane] = __uint_as_float(r[c]);
+            for (int c = 0; c < 8; ++c) {
+              if (q < 2) xg[c * 64 + 32 * fq + lane] = __uint_as_float(r[8 + c]);
+              else xu[c * 64 + 32 * fq + lane] = __uint_as_float(r[c]);
+            }
           }
           named_bar_sync(1, 128);
-          if (q < 2 && ok) {
-            const int feat = 64 * m + 32 * q + lane;
+          if (ok) {
+            const int feat = 64 * m + 32 * fq + lane;
+            const int cbase = (q < 2) ? 0 : 8;
 #pragma unroll 4
-            for (int c = 0; c < 16; ++c) {
-              const int col = c0 + c;
-              const float g = __uint_as_float(r[c]);
-              const float u = xchg[c * 64 + 32 * q + lane];
+            for (int c = 0; c < 8; ++c) {
+              const int col = c0 + cbase + c;
+              const float g = (q < 2) ? __uint_as_float(r[c]) : xg[c * 64 + 32 * fq + lane];
+              const float u = (q < 2) ? xu[c * 64 + 32 * fq + lane] : __uint_as_float(r[8 + c]);
               const float a = silu_mul(g, u);
               float am = fabsf(a);
 #pragma unroll
               for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
-              const int se = mx8_scale_exp(am);
+              const int se = e4m3_scale_exp(am);
               const float sc = __uint_as_float((uint32_t)(127 - se) << 23);
-              const uint32_t code = e4m3_pair(a * sc, 0.f) & 0xFF;
+              const uint32_t code = e4m3x2(a * sc, 0.f) & 0xFF;
               if (col < nrows) {
                 const size_t prow = (size_t)(row0 + col);
                 p.hq[prow * p.I + feat] = (uint8_t)code;
@@ -381,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0 && ok) mbar_arrive(acc_empty);
+      if (lane == 0 && ok) mbar_arrive(&acc_empty[acc]);
     }
   }
 
@@ -393,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
     }
   }
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 2) tmem_dealloc(tmem, L::kTmemCols);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -430,6 +491,20 @@ static int make_weight_tmap(CUtensorMap* m, const uint8_t* codes, long long tile
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Activation codes viewed as [rows, row_bytes] bytes, 128-byte swizzled boxes of box_rows rows.
+static int make_act_tmap(CUtensorMap* m, const uint8_t* base, int row_bytes, long long rows, int box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return MOE_ERR_CUDA;
+  cuuint64_t gdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), gdim, gstride, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 static int pick_bn(const moe_shape* s) {
   const double avg = (double)s->T * s->k / s->E;
   if (avg <= 16) return 16;
@@ -439,7 +514,8 @@ static int pick_bn(const moe_shape* s) {
 }
 
 template <int BN, bool W13>
-static int launch_gemm_bn(const CUtensorMap& tm, const GemmParams& gp, long long max_items, cudaStream_t st) {
+static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const GemmParams& gp, long long max_items,
+                          cudaStream_t st) {
   using L = Smem<BN>;
   auto kern = grouped_gemm_kernel<BN, W13>;
   const int smem = L::total(gp.E);
@@ -449,22 +525,30 @@ static int launch_gemm_bn(const CUtensorMap& tm, const GemmParams& gp, long long
       return MOE_ERR_CUDA;
     attr = L::total(kMaxE);
   }
-  const long long grid = std::min<long long>(max_items, 2LL * num_sms());
+  const long long grid = std::min<long long>(max_items, (long long)L::kCtasPerSm * num_sms());
   if (grid <= 0) return MOE_OK;
-  kern<<<(int)grid, kThreads, smem, st>>>(tm, gp);
+  kern<<<(int)grid, kThreads, smem, st>>>(tm, tmb, gp);
   return launch_status();
 }
 
 template <bool W13>
 static int launch_gemm(const moe_shape* s, const CUtensorMap& tm, const GemmParams& gp, cudaStream_t st) {
+  // activation operand as a TMA tensor for the wide token tile: W13 reads xq [T, H] one row per
+  // gather slot; W2 reads hq [T*k, I] in boxes of 128 plan rows
+  CUtensorMap tmb = tm;
   const long long slots = (long long)s->T * s->k;
   const int bn = pick_bn(s);
   const long long max_items = (long long)gp.MT * ((slots + bn - 1) / bn + std::min<long long>(s->E, slots));
+  if (bn == 128) {
+    const long long rows = W13 ? (long long)s->T : slots;
+    const int rc = make_act_tmap(&tmb, gp.bq, gp.b_row_bytes, rows, W13 ? 1 : 128);
+    if (rc) return rc;
+  }
   switch (bn) {
-    case 16: return launch_gemm_bn<16, W13>(tm, gp, max_items, st);
-    case 32: return launch_gemm_bn<32, W13>(tm, gp, max_items, st);
-    case 64: return launch_gemm_bn<64, W13>(tm, gp, max_items, st);
-    default: return launch_gemm_bn<128, W13>(tm, gp, max_items, st);
+    case 16: return launch_gemm_bn<16, W13>(tm, tmb, gp, max_items, st);
+    case 32: return launch_gemm_bn<32, W13>(tm, tmb, gp, max_items, st);
+    case 64: return launch_gemm_bn<64, W13>(tm, tmb, gp, max_items, st);
+    default: return launch_gemm_bn<128, W13>(tm, tmb, gp, max_items, st);
   }
 }
 

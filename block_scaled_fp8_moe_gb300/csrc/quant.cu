@@ -7,42 +7,9 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "mx.cuh"
 
 namespace moe {
-
-// Smallest s with amax <= qmax * 2^s, qmax = 1.qm * 2^qe (qm as a 23-bit mantissa field).
-// Exact integer work on the bits of amax, clamped to the UE8M0 range; amax = 0 -> -127.
-__device__ __forceinline__ int mx_scale_exp(float amax, int qe, uint32_t qm) {
-  uint32_t b = __float_as_uint(amax);
-  if (b == 0) return -127;
-  int e = (int)((b >> 23) & 0xFF);
-  uint32_t man = b & 0x7FFFFF;
-  if (e == 0) {                       // subnormal amax: normalise
-    int sh = __clz(man) - 8;
-    man = (man << sh) & 0x7FFFFF;
-    e = 1 - sh;
-  }
-  int s = (e - 127) - qe + (man > qm ? 1 : 0);
-  return max(-127, min(126, s));      // 127 is unreachable for finite fp32 amax and both formats
-}
-
-// 2^-s for s in [-127, 126] (always a normal fp32)
-__device__ __forceinline__ float pow2_neg(int s) { return __uint_as_float((uint32_t)(127 - s) << 23); }
-
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// E2M1 round-to-nearest-even of v (|v| <= 6 under the scale rule), from the value grid
-// {0, .5, 1, 1.5, 2, 3, 4, 6}: each comparison counts one grid step passed; at an exact midpoint
-// the step is taken only when it lands on the even code.
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-  float a = fabsf(v);
-  uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
-  return c | (signbit(v) ? 8u : 0u);
-}
 
 // 8 bf16 elements per thread, 4 threads per 32-block.
 __global__ void quant_mxfp8_kernel(const uint4* __restrict__ x, uint2* __restrict__ q, uint8_t* __restrict__ s,
@@ -66,7 +33,7 @@ __global__ void quant_mxfp8_kernel(const uint4* __restrict__ x, uint2* __restric
     for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    const int se = mx_scale_exp(m, 8, 0x600000u);
+    const int se = e4m3_scale_exp(m);
     const float sc = pow2_neg(se);
     uint32_t lo = e4m3x2(f[0] * sc, f[1] * sc) | (e4m3x2(f[2] * sc, f[3] * sc) << 16);
     uint32_t hi = e4m3x2(f[4] * sc, f[5] * sc) | (e4m3x2(f[6] * sc, f[7] * sc) << 16);
@@ -93,7 +60,7 @@ __global__ void quant_mxfp4_kernel(const float4* __restrict__ w, uint32_t* __res
     for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    const int se = mx_scale_exp(m, 2, 0x400000u);
+    const int se = e2m1_scale_exp(m);
     const float sc = pow2_neg(se);
     uint32_t packed = 0;
 #pragma unroll

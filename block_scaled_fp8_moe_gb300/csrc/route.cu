@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "mx.cuh"
 
 namespace moe {
 
@@ -102,19 +103,122 @@ __global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __res
 }
 
 // ---------------------------------------------------------------------------------------------
+// Logits, small T (decode), x staged in shared memory. A CTA owns kDecEpc experts; each thread
+// item (expert, chunk) streams its 128 bytes of Wr once (8 loads in flight) and runs the
+// sequential fma chain of that chunk for every token from shared memory; the chunk partials are
+// then folded left to right per (expert, token). The same order as router_small_kernel and the
+// tiled kernel. Optionally each CTA also MXFP8-quantises a share of the rows it already holds.
+// ---------------------------------------------------------------------------------------------
+constexpr int kDecEpc = 4;          // experts per CTA
+constexpr size_t kDecodeSmemMax = 160 * 1024;
+constexpr int kDecPad = 66;         // bf16 per staged 64-element chunk (2 pad -> conflict-free)
+
+__host__ __device__ inline size_t router_decode_smem(int T, int H) {
+  const int NC = H / kRouterChunk;
+  return (size_t)T * NC * kDecPad * 2 + (size_t)kDecEpc * T * NC * 4;
+}
+
+__global__ void __launch_bounds__(256) router_decode_kernel(const uint16_t* __restrict__ x,
+                                                            const uint16_t* __restrict__ wr,
+                                                            const float* __restrict__ bias, int T, int H, int E,
+                                                            float* __restrict__ score, float* __restrict__ key,
+                                                            uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
+  extern __shared__ __align__(16) uint8_t dsm_dec[];
+  const int NC = H / kRouterChunk;
+  uint16_t* xsm = reinterpret_cast<uint16_t*>(dsm_dec);                                // [T][NC][kDecPad]
+  float* part = reinterpret_cast<float*>(dsm_dec + (size_t)T * NC * kDecPad * 2);     // [kDecEpc][T][NC]
+  const int e0 = blockIdx.x * kDecEpc;
+  // stage x (16-byte global loads, 4-byte shared stores into the padded chunk layout)
+  for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) {
+    const int t = i / (H / 8), h = (i % (H / 8)) * 8;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + h));
+    uint32_t* d = reinterpret_cast<uint32_t*>(xsm + ((size_t)t * NC + h / kRouterChunk) * kDecPad + (h % kRouterChunk));
+    d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+  }
+  __syncthreads();
+  for (int it = threadIdx.x; it < kDecEpc * NC; it += blockDim.x) {
+    const int el = it / NC, c = it % NC;
+    const int e = e0 + el;
+    if (e >= E) continue;
+    const uint4* wp = reinterpret_cast<const uint4*>(wr + (size_t)e * H + (size_t)c * kRouterChunk);
+    uint4 wv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wv[i] = __ldg(wp + i);
+    for (int t = 0; t < T; ++t) {
+      const uint32_t* xp = reinterpret_cast<const uint32_t*>(xsm + ((size_t)t * NC + c) * kDecPad);
+      float p = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t xw = xp[i * 4 + q];
+          p = __fmaf_rn(bf_lo(xw), bf_lo(ww[q]), p);
+          p = __fmaf_rn(bf_hi(xw), bf_hi(ww[q]), p);
+        }
+      }
+      part[((size_t)el * T + t) * NC + c] = p;
+    }
+  }
+  // MXFP8 quantisation of a share of the staged rows (one 32-block per thread item)
+  if (xq) {
+    const int nblk = T * H / 32;
+    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += gridDim.x * blockDim.x) {
+      const int t = b / (H / 32), h = (b % (H / 32)) * 32;
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(xsm + ((size_t)t * NC + h / kRouterChunk) * kDecPad +
+                                                              (h % kRouterChunk));
+      float f[32];
+      float m = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        f[2 * i] = bf_lo(src[i]);
+        f[2 * i + 1] = bf_hi(src[i]);
+        m = fmaxf(m, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+      }
+      const int se = e4m3_scale_exp(m);
+      const float sc = pow2_neg(se);
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        o[i] = e4m3x2(f[4 * i] * sc, f[4 * i + 1] * sc) | (e4m3x2(f[4 * i + 2] * sc, f[4 * i + 3] * sc) << 16);
+      uint4* dq = reinterpret_cast<uint4*>(xq + (size_t)t * H + h);
+      dq[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dq[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      xs[(size_t)t * (H / 32) + h / 32] = (uint8_t)(se + 127);
+    }
+  }
+  __syncthreads();
+  for (int it = threadIdx.x; it < kDecEpc * T; it += blockDim.x) {
+    const int el = it / T, t = it % T;
+    const int e = e0 + el;
+    if (e >= E) continue;
+    const float* pp = part + ((size_t)el * T + t) * NC;
+    float acc = 0.f;
+    for (int c = 0; c < NC; ++c) acc = __fadd_rn(acc, pp[c]);
+    const float sc = sigmoid_cw(acc);
+    score[(size_t)t * E + e] = sc;
+    key[(size_t)t * E + e] = __fadd_rn(sc, bias[e]);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
 // Logits, large T: 64 tokens x 64 experts per CTA, 4 x 4 outputs per thread, one 64-wide h chunk
-// per shared-memory stage. Each output keeps its chunk partial (sequential fma from +0 over the
-// chunk) and adds it to the running sum after the chunk: the same order as the small kernel.
+// per shared-memory stage, staged transposed ([h][token], [h][expert]) so that each h step is two
+// 16-byte shared loads and 16 fma. Each output keeps its chunk partial (sequential fma from +0
+// over the chunk) and adds it to its running sum after the chunk: the same order as the small-T
+// kernels.
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) router_tiled_kernel(const uint16_t* __restrict__ x,
                                                            const uint16_t* __restrict__ wr,
                                                            const float* __restrict__ bias, int T, int H, int E,
                                                            float* __restrict__ score, float* __restrict__ key) {
-  __shared__ float xs[64][65];
-  __shared__ float ws[64][65];
+  __shared__ __align__(16) float xs[kRouterChunk][64];
+  __shared__ __align__(16) float ws[kRouterChunk][64];
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
   const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
+  // staging: thread -> (row = tid % 64, 16 consecutive h); a warp stores 32 rows of one h
+  const int srow = tid & 63, sh = (tid >> 6) * 16;
   float acc[4][4], part[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -122,21 +226,26 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const uint16_t* __res
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   for (int h0 = 0; h0 < H; h0 += kRouterChunk) {
     __syncthreads();
-    // 64 rows x 64 bf16 = 512 uint4 per matrix; 2 per thread per matrix
+    {
+      uint4 xa = make_uint4(0, 0, 0, 0), xb = xa, wa = xa, wb = xa;
+      if (t0 + srow < T) {
+        const uint4* xp = reinterpret_cast<const uint4*>(x + (size_t)(t0 + srow) * H + h0 + sh);
+        xa = __ldg(xp);
+        xb = __ldg(xp + 1);
+      }
+      if (e0 + srow < E) {
+        const uint4* wp = reinterpret_cast<const uint4*>(wr + (size_t)(e0 + srow) * H + h0 + sh);
+        wa = __ldg(wp);
+        wb = __ldg(wp + 1);
+      }
+      const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      const uint32_t ww[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-      const int idx = tid + rep * 256;
-      const int row = idx >> 3, seg = idx & 7;
-      uint4 xv = make_uint4(0, 0, 0, 0), wv = make_uint4(0, 0, 0, 0);
-      if (t0 + row < T) xv = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + row) * H + h0) + seg);
-      if (e0 + row < E) wv = __ldg(reinterpret_cast<const uint4*>(wr + (size_t)(e0 + row) * H + h0) + seg);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        xs[row][seg * 8 + 2 * q] = bf_lo(xw[q]);
-        xs[row][seg * 8 + 2 * q + 1] = bf_hi(xw[q]);
-        ws[row][seg * 8 + 2 * q] = bf_lo(ww[q]);
-        ws[row][seg * 8 + 2 * q + 1] = bf_hi(ww[q]);
+      for (int q = 0; q < 8; ++q) {
+        xs[sh + 2 * q][srow] = bf_lo(xw[q]);
+        xs[sh + 2 * q + 1][srow] = bf_hi(xw[q]);
+        ws[sh + 2 * q][srow] = bf_lo(ww[q]);
+        ws[sh + 2 * q + 1][srow] = bf_hi(ww[q]);
       }
     }
     __syncthreads();
@@ -146,15 +255,13 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const uint16_t* __res
       for (int j = 0; j < 4; ++j) part[i][j] = 0.f;
 #pragma unroll 8
     for (int h = 0; h < kRouterChunk; ++h) {
-      float xv[4], wv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) xv[i] = xs[ty + 16 * i][h];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) wv[j] = ws[tx + 16 * j][h];
+      const float4 xv = *reinterpret_cast<const float4*>(&xs[h][4 * ty]);
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[h][4 * tx]);
+      const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) part[i][j] = __fmaf_rn(xv[i], wv[j], part[i][j]);
+        for (int j = 0; j < 4; ++j) part[i][j] = __fmaf_rn(xa[i], wa[j], part[i][j]);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -163,11 +270,11 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const uint16_t* __res
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty + 16 * i;
+    const int t = t0 + 4 * ty + i;
     if (t >= T) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx + 16 * j;
+      const int e = e0 + 4 * tx + j;
       if (e >= E) continue;
       const float sc = sigmoid_cw(acc[i][j]);
       score[(size_t)t * E + e] = sc;
@@ -230,11 +337,12 @@ __global__ void __launch_bounds__(512) topk_plan_kernel(const float* __restrict_
 
   for (int tl = warp; tl < nt; tl += kTopkWarps) {
     const int t = tb0 + tl;
-    float kv[32];
+    float kv[32], sv[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int e = lane + 32 * i;
       kv[i] = (e < E) ? key[(size_t)t * E + e] : 0.f;
+      sv[i] = (e < E) ? score[(size_t)t * E + e] : 0.f;
     }
     uint32_t taken = 0;
     float sel_sum = 0.f;
@@ -254,8 +362,12 @@ __global__ void __launch_bounds__(512) topk_plan_kernel(const float* __restrict_
         int oe = __shfl_xor_sync(0xffffffffu, be, off);
         if (oe != 0x7fffffff && (be == 0x7fffffff || better(ok, oe, bk, be))) { bk = ok; be = oe; }
       }
+      float own = 0.f;                            // the winner's score, read by its owner lane
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i == (be >> 5)) own = sv[i];
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      const float s = score[(size_t)t * E + be];
+      const float s = __shfl_sync(0xffffffffu, own, be & 31);
       sel_sum = __fadd_rn(sel_sum, s);           // rank order, identical on every lane
       if (lane == j) { my_e = be; my_s = s; }
       sidx[tl * k + j] = (int16_t)be;
@@ -365,7 +477,8 @@ __global__ void plan_scatter_kernel(const int32_t* __restrict__ topk_idx, const 
 
 int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, const uint8_t* dead,
                  int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
-                 int32_t* row_of_slot, void* ws, cudaStream_t st) {
+                 int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done) {
+  if (quant_done) *quant_done = false;
   const Workspace L = workspace_layout(s);
   const int T = s->T, E = s->E, k = s->k, H = s->H;
   if (T == 0) {
@@ -375,7 +488,20 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
   }
   float* score = ws_ptr<float>(ws, L.score);
   float* key = ws_ptr<float>(ws, L.key);
-  if (T <= kSmallT) {
+  const size_t dec_smem = router_decode_smem(T, H);
+  if (T <= kSmallT && dec_smem <= kDecodeSmemMax) {
+    static bool dec_attr = false;
+    if (!dec_attr) {
+      if (cudaFuncSetAttribute(router_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kDecodeSmemMax) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      dec_attr = true;
+    }
+    const bool fuse = xq && xs;
+    router_decode_kernel<<<ceil_div(E, kDecEpc), 256, dec_smem, st>>>(x, wr, bias, T, H, E, score, key,
+                                                                      fuse ? xq : nullptr, fuse ? xs : nullptr);
+    if (quant_done) *quant_done = fuse;
+  } else if (T <= kSmallT) {
     router_small_kernel<<<ceil_div(E, 8), 256, 0, st>>>(x, wr, bias, T, H, E, score, key);
   } else {
     dim3 grid(ceil_div(T, 64), ceil_div(E, 64));
@@ -471,7 +597,7 @@ extern "C" int moe_route_topk(const moe_shape* s, const uint16_t* x, const uint1
   int rc = ws_check(s, ws, ws_bytes);
   if (rc) return rc;
   return launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, expert_counts, expert_offsets, slot_of_row,
-                      row_of_slot, ws, static_cast<cudaStream_t>(stream));
+                      row_of_slot, ws, static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr);
 }
 
 // ---------------------------------------------------------------------------------------------

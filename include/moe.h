@@ -177,6 +177,12 @@ MOE_API int moe_forward(const moe_shape* shape, const uint16_t* x, const uint16_
                 const uint8_t* w2_s, uint16_t* out, const moe_intermediates* inter, void* ws,
                 size_t ws_bytes, void* stream);
 
+/* Test hook for the bounded waits: launches one thread that waits on a barrier nothing arrives at,
+ * for limit_ns (<= 2 s). The wait expires, writes its code into the status word at the start of
+ * `ws` and the kernel returns; moe_check_device_status then reports MOE_ERR_TIMEOUT. No fault, no
+ * hang, the context stays usable. Not part of the layer. */
+MOE_API int moe_selftest_timeout(void* ws, uint64_t limit_ns, void* stream);
+
 /* Allocation-free variant of moe_route_topk, for callers that cannot allocate device memory:
  * engines that reserved all of HBM for their own pool at start-up, or code running inside a host
  * framework's callback where allocation is not allowed. It takes no workspace; its scratch lives in

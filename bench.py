@@ -43,6 +43,9 @@ def parse():
     ap.add_argument("--cpu-tokens", type=int, default=1)
     ap.add_argument("--tokens", type=int, default=0, help="override T of the workload (profiling aid)")
     ap.add_argument("--experts", type=int, default=0, help="override E of the workload (profiling aid)")
+    ap.add_argument("--record-traffic", default="", metavar="RAW_CSV",
+                    help="store DRAM bytes per launch of the grouped GEMMs from `ncu -i REP --page raw --csv` "
+                         "output into profiles/traffic.json for --config (stamped with the GEMM source hash)")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -61,6 +64,55 @@ def reduce_max(value: float, device) -> float:
 def tokens_per_s(world: int, rows_per_rank: int, steps: int, max_ms: float) -> float:
     """Whole-job throughput: every rank processes its own batch of rows each step."""
     return world * rows_per_rank * steps / (max_ms / 1e3)
+
+
+GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "mx.cuh", "common.cuh")
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def gemm_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "block_scaled_fp8_moe_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def record_traffic(raw_csv: str, workload: str) -> dict:
+    """Average dram__bytes_read.sum + dram__bytes_write.sum per launch of each grouped GEMM."""
+    import csv
+    rows = list(csv.reader(open(raw_csv)))
+    hdr = rows[0]
+    unit = dict(zip(hdr, rows[1]))
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    acc: dict = {}
+    for r in rows[2:]:
+        d = dict(zip(hdr, r))
+        name = d.get("Kernel Name", "")
+        if "grouped_gemm_kernel" not in name:
+            continue
+        key = "w13" if name.rstrip().endswith("1>(CUtensorMap_st, CUtensorMap_st, GemmParams)") else "w2"
+        b = sum(float(d[m]) * scale[unit[m]] for m in ("dram__bytes_read.sum", "dram__bytes_write.sum"))
+        acc.setdefault(key, []).append(b)
+    entry = {k: sum(v) / len(v) for k, v in acc.items()}
+    entry["source_hash"] = gemm_source_hash()
+    data = json.load(open(TRAFFIC_JSON)) if os.path.exists(TRAFFIC_JSON) else {}
+    data[workload] = entry
+    with open(TRAFFIC_JSON, "w") as fh:
+        json.dump(data, fh, indent=1, sort_keys=True)
+    return entry
+
+
+def measured_traffic(workload: str, keys) -> float | None:
+    """Bytes per launch from profiles/traffic.json, or None if absent or taken on other sources."""
+    try:
+        entry = json.load(open(TRAFFIC_JSON))[workload]
+    except Exception:
+        return None
+    if entry.get("source_hash") != gemm_source_hash() or any(k not in entry for k in keys):
+        return None
+    return float(sum(entry[k] for k in keys))
 
 
 def workload_name(cfg):
@@ -323,7 +375,7 @@ def gpu_arm(args):
         achieved = alg_bytes / (w13_ms * 1e-3) / 1e9
         roofline = {"kernel": "w13_swiglu_grouped (grouped_gemm_kernel<W13>)", "bound": "hbm",
                     "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
-                    "frac": round(achieved / hbm_gbs, 4), "traffic": None,
+                    "frac": round(achieved / hbm_gbs, 4), "traffic": measured_traffic(cfg.name, ("w13",)),
                     "peak_source": f"{peak_src} HBM copy bandwidth",
                     "alg_bytes_per_launch": alg_bytes, "touched_experts": touched,
                     "launch_ms": round(w13_ms, 5)}
@@ -332,7 +384,8 @@ def gpu_arm(args):
         achieved = flops / ((w13_ms + w2_ms) * 1e-3) / 1e12
         peak = FP8_OVER_BF16 * bf16_tflops
         roofline = {"kernel": "w13 + w2 grouped GEMMs", "bound": "tensor", "achieved": round(achieved, 1),
-                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "traffic": measured_traffic(cfg.name, ("w13", "w2")),
                     "peak_source": f"{peak_src} bf16 x {FP8_OVER_BF16} (nominal fp8/bf16 ratio)",
                     "alg_flops_per_step": flops, "launch_ms": round(w13_ms + w2_ms, 5)}
 
@@ -410,6 +463,9 @@ def reference_arm(args):
 
 def main():
     args = parse()
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, args.config)))
+        return
     if args.oracle_child:
         print(json.dumps(oracle_sample_timing(args.config, args.cpu_tokens, args.steps, args.warmup)))
         return

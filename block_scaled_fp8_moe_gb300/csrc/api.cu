@@ -42,7 +42,7 @@ extern "C" int moe_w13_swiglu_grouped(const moe_shape* s, const uint8_t* xq, con
   const Workspace L = workspace_layout(s);
   return launch_w13(s, xq, xs, w13, w13_s, expert_offsets, slot_of_row, hq, hs,
                     (s->flags & 1) ? swiglu_debug : nullptr, ws_ptr<uint32_t>(ws, L.status),
-                    static_cast<cudaStream_t>(stream));
+                    ws_ptr<uint8_t>(ws, L.xqp), ws_ptr<uint8_t>(ws, L.xsp), static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int moe_w2_combine_grouped(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2,
@@ -108,7 +108,8 @@ extern "C" int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t
     rc = launch_quant_mxfp8(s->T, s->H, x, xq, xs, st);
     if (rc) return rc;
   }
-  rc = launch_w13(s, xq, xs, w13, w13_s, offsets, slot_of_row, hq, hs, im.swiglu, status, st);
+  rc = launch_w13(s, xq, xs, w13, w13_s, offsets, slot_of_row, hq, hs, im.swiglu, status, ws_ptr<uint8_t>(ws, L.xqp),
+                  ws_ptr<uint8_t>(ws, L.xsp), st);
   if (rc) return rc;
   rc = launch_w2(s, hq, hs, w2, w2_s, topk_w, offsets, slot_of_row, y, status, st);
   if (rc) return rc;

@@ -38,6 +38,7 @@ struct Workspace {
   size_t status, score, key, cnt, base, rank;                  // router scratch
   size_t topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot;
   size_t xq, xs, hq, hs, y;                                    // forward intermediates
+  size_t xqp, xsp;                                             // plan-order copy of xq / xs
   size_t total;
 };
 
@@ -64,6 +65,8 @@ inline Workspace workspace_layout(const moe_shape* s) {
   w.hq = take(T * k * I);
   w.hs = take(T * k * (size_t)hs_pitch((int)I));
   w.y = take(T * k * H * 4);
+  w.xqp = take(T * k * H);
+  w.xsp = take(T * k * H / 32);
   w.total = off;
   return w;
 }
@@ -102,7 +105,7 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
                  int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done);
 int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
                const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
-               uint32_t* status, cudaStream_t st);
+               uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, cudaStream_t st);
 int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2s,
               const float* topk_w, const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
               cudaStream_t st);

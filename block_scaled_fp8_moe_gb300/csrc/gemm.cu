@@ -24,6 +24,7 @@
 // Work items (expert, weight panel, token tile) are walked with the token tile fastest, so CTAs
 // running at the same time share one weight panel through L2.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -32,14 +33,11 @@
 
 namespace moe {
 
+#ifndef MOE_KT_WIDE
+#define MOE_KT_WIDE 1               // K-chunks per stage for token tiles > 32
+#endif
 constexpr int kThreads = 256;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
-#ifndef MOE_STAGES_SMALL
-#define MOE_STAGES_SMALL 5          // pipeline stages for token tiles <= 16
-#endif
-#ifndef MOE_CTAS_SMALL
-#define MOE_CTAS_SMALL 2            // resident CTAs per SM for token tiles <= 16
-#endif
 
 struct GemmParams {
   // B side (activations)
@@ -67,11 +65,17 @@ struct GemmParams {
 
 template <int BN>
 struct Smem {
-  static constexpr int kStageA = 16384;
-  static constexpr int kStageB = BN * 128;
-  static constexpr int kStageBytes = kStageA + kStageB + 1024;   // + 512 B A scales + 512 B B scales
-  static constexpr int kStages = (BN <= 16) ? MOE_STAGES_SMALL : (BN <= 64 ? 4 : 6);
-  static constexpr int kCtasPerSm = (BN <= 16) ? MOE_CTAS_SMALL : (BN <= 64 ? 2 : 1);
+  // A pipeline stage holds KT consecutive K-chunks (weight tiles) of 128: small token tiles are
+  // weight-streaming bound and each stage hand-off costs a fixed few hundred ns per CTA, so they
+  // move 16 KB of packed weights per TMA request.
+  static constexpr int KT = (BN <= 32) ? 2 : MOE_KT_WIDE;
+  static constexpr int kTileA = 16384;                           // one unpacked 128 x 128 FP4 tile
+  static constexpr int kTileB = BN * 128;                        // BN rows x 128 FP8
+  static constexpr int kStageA = KT * kTileA;
+  static constexpr int kStageB = KT * kTileB;
+  static constexpr int kStageBytes = kStageA + kStageB + KT * 1024;   // + KT x (512 B A + 512 B B scales)
+  static constexpr int kStages = (BN <= 32) ? 2 : (BN <= 64 ? 3 : 6 / MOE_KT_WIDE);
+  static constexpr int kCtasPerSm = (BN <= 64) ? 2 : 1;
   // TMEM: two accumulator slots of kAccStride columns, then the ring of scale blocks
   static constexpr int kAccStride = (BN <= 64) ? 64 : 128;
   static constexpr int kSfCol = 2 * kAccStride;
@@ -80,7 +84,7 @@ struct Smem {
   // four-row gathers for W13's token rows) instead of cp.async
   static constexpr bool kTmaB = (BN >= 128);
   static constexpr int kTiles = kStages * kStageBytes;
-  static constexpr int kXchg = 64 * 16 * 4;                     // W13 epilogue exchange
+  static constexpr int kXchg = 2 * 64 * 16 * 4;                 // W13 epilogue exchange (gate + up)
   static constexpr int kMisc = 1024;                            // barriers, flags
   static constexpr int kRows = 128 * 8;                         // gather row table
   static constexpr int kFixed = 1024 + kTiles + kXchg + kMisc + kRows;
@@ -209,57 +213,56 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
         int e, m, nt, row0, nrows;
         decode(w, e, m, nt, row0, nrows);
         const int tile0 = (e * p.MT + m) * KC;
-        for (int kc = 0; kc < KC; ++kc) {
+        for (int kc0 = 0; kc0 < KC; kc0 += L::KT) {
           if (!mbar_wait(&empty[stage], phase ^ 1, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_EMPTY)) {
             ok = false;
             break;
           }
+          const int nv = min(L::KT, KC - kc0);            // chunks of this stage inside the panel
           uint8_t* sA = tiles + stage * L::kStageBytes;
           uint8_t* sSFA = sA + L::kStageA + L::kStageB;
-          mbar_arrive_expect_tx(&full[stage], kTileCodeBytes + kTileScaleBytes + (kTmaB ? L::kStageB : 0));
-          tma_load_2d(sA, &tmap_a, 0, (tile0 + kc) * 128, &full[stage]);
-          bulk_load(sSFA, p.a_scales + (size_t)(tile0 + kc) * kTileScaleBytes, kTileScaleBytes, &full[stage]);
+          // the box always moves KT tiles (past the panel: the next panel's tiles or TMA fill);
+          // the scale copy stops at the panel's end
+          mbar_arrive_expect_tx(&full[stage], L::KT * kTileCodeBytes + nv * kTileScaleBytes +
+                                                  (kTmaB ? L::kStageB : 0));
+          tma_load_2d(sA, &tmap_a, 0, (tile0 + kc0) * 128, &full[stage]);
+          bulk_load(sSFA, p.a_scales + (size_t)(tile0 + kc0) * kTileScaleBytes, nv * kTileScaleBytes, &full[stage]);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
     }
   } else if (kTmaB && warp == 1) {
     // ===================== TMA producer: activations (wide token tiles) =====================
-    // W13: lane i gathers plan rows 4i..4i+3 (their token rows of xq) with one four-row TMA gather;
-    // W2: lane 0 loads the tile's contiguous plan rows of hq with one 2D TMA box. Either way the
-    // rows past the tile's end are some other valid row (or TMA's zero fill); their columns are
-    // never stored. Every lane also copies the scale bytes of its rows lane + 32 i.
+    // The token operand of a wide tile is always in plan order (W2: hq; W13: a copy of xq gathered
+    // into plan order before the GEMM), so lane 0 loads the tile's contiguous plan rows with one
+    // 2D TMA box; rows past the tile's end belong to the next expert (or are TMA zero fill) and
+    // their columns are never stored. Every lane also copies the scale bytes of rows lane + 32 i.
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total; w += gridDim.x) {
       int e, m, nt, row0, nrows;
       decode(w, e, m, nt, row0, nrows);
-      int grow[4];
-      long long srow[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = 4 * lane + i;
-        grow[i] = W13 ? p.slot_of_row[row0 + min(c, nrows - 1)] / p.k : 0;
-        const int cs = lane + 32 * i;
-        srow[i] = cs < nrows ? (W13 ? (long long)(p.slot_of_row[row0 + cs] / p.k) : (long long)(row0 + cs)) : -1;
-      }
-      for (int kc = 0; kc < p.KC; ++kc) {
+      for (int kc0 = 0; kc0 < p.KC; kc0 += L::KT) {
         if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
         if (ok) {
-          uint8_t* sB = tiles + stage * L::kStageBytes + L::kStageA;
-          uint8_t* sSFB = sB + L::kStageB + 512;
-          if constexpr (W13) {
-            tma_gather4(sB + 4 * lane * 128, &tmap_b, kc * 128, grow[0], grow[1], grow[2], grow[3], &full[stage]);
-          } else {
-            if (lane == 0) tma_load_2d(sB, &tmap_b, kc * 128, row0, &full[stage]);
-          }
+          const int nv = min(L::KT, p.KC - kc0);
+          uint8_t* sB0 = tiles + stage * L::kStageBytes + L::kStageA;
+          uint8_t* sSFB0 = sB0 + L::kStageB + L::KT * 512;
+          // every stage moves KT boxes (the transaction count the weight producer announced);
+          // boxes past the end of K read TMA's zero fill and are never multiplied
+          if (lane == 0)
+            for (int j = 0; j < L::KT; ++j)
+              tma_load_2d(sB0 + j * L::kTileB, &tmap_b, (kc0 + j) * 128, row0, &full[stage]);
+          for (int j = 0; j < nv; ++j) {
+            const int kc = kc0 + j;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = lane + 32 * i;
-            const bool valid = srow[i] >= 0;
-            const uint8_t* src = valid ? p.bs + srow[i] * p.b_scale_pitch + kc * 4 : p.bs;
-            cp_async_4(sSFB + (c & 31) * 16 + (c >> 5) * 4, src, valid ? 4u : 0u);
+            for (int i = 0; i < 4; ++i) {
+              const int c = lane + 32 * i;
+              const bool valid = c < nrows;
+              const uint8_t* src = valid ? p.bs + (size_t)(row0 + c) * p.b_scale_pitch + kc * 4 : p.bs;
+              cp_async_4(sSFB0 + j * 512 + (c & 31) * 16 + (c >> 5) * 4, src, valid ? 4u : 0u);
+            }
           }
           cp_async_arrive_noinc(&full[stage]);
         }
@@ -288,24 +291,30 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
         s_rows[c] = r;
       }
       named_bar_sync(2, 64);
-      for (int kc = 0; kc < p.KC; ++kc) {
+      for (int kc0 = 0; kc0 < p.KC; kc0 += L::KT) {
         if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
         if (ok) {
-          uint8_t* sB = tiles + stage * L::kStageBytes + L::kStageA;
-          uint8_t* sSFB = sB + L::kStageB + 512;
-          for (int i = pb; i < BN * 8; i += 64) {
-            const int c = i >> 3, j = i & 7;
-            const long long r = s_rows[c];
-            const int kbyte = kc * 128 + j * 16;
-            const bool valid = (r >= 0) && (kbyte < p.b_row_bytes);
-            const uint8_t* src = valid ? p.bq + r * p.b_row_bytes + kbyte : p.bq;
-            cp_async_16(sB + c * 128 + ((j ^ (c & 7)) << 4), src, valid ? 16u : 0u);
-          }
-          for (int c = pb; c < BN; c += 64) {
-            const long long r = s_rows[c];
-            const bool valid = r >= 0;
-            const uint8_t* src = valid ? p.bs + r * p.b_scale_pitch + kc * 4 : p.bs;
-            cp_async_4(sSFB + (c & 31) * 16 + (c >> 5) * 4, src, valid ? 4u : 0u);
+          const int nv = min(L::KT, p.KC - kc0);
+          uint8_t* sB0 = tiles + stage * L::kStageBytes + L::kStageA;
+          uint8_t* sSFB0 = sB0 + L::kStageB + L::KT * 512;
+          for (int j2 = 0; j2 < nv; ++j2) {
+            const int kc = kc0 + j2;
+            uint8_t* sB = sB0 + j2 * L::kTileB;
+            uint8_t* sSFB = sSFB0 + j2 * 512;
+            for (int i = pb; i < BN * 8; i += 64) {
+              const int c = i >> 3, j = i & 7;
+              const long long r = s_rows[c];
+              const int kbyte = kc * 128 + j * 16;
+              const bool valid = (r >= 0) && (kbyte < p.b_row_bytes);
+              const uint8_t* src = valid ? p.bq + r * p.b_row_bytes + kbyte : p.bq;
+              cp_async_16(sB + c * 128 + ((j ^ (c & 7)) << 4), src, valid ? 16u : 0u);
+            }
+            for (int c = pb; c < BN; c += 64) {
+              const long long r = s_rows[c];
+              const bool valid = r >= 0;
+              const uint8_t* src = valid ? p.bs + r * p.b_scale_pitch + kc * 4 : p.bs;
+              cp_async_4(sSFB + (c & 31) * 16 + (c >> 5) * 4, src, valid ? 4u : 0u);
+            }
           }
           cp_async_arrive_noinc(&full[stage]);
         }
@@ -331,27 +340,32 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(acc * L::kAccStride);
-        for (int kc = 0; kc < p.KC; ++kc) {
+        for (int kc0 = 0; kc0 < p.KC; kc0 += L::KT) {
           if (!mbar_wait(&full[stage], phase, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_FULL)) {
             ok = false;
             break;
           }
           fence_async_smem();
           tc_fence_after();
-          uint8_t* sA = tiles + stage * L::kStageBytes;
-          uint8_t* sB = sA + L::kStageA;
-          uint8_t* sSFA = sB + L::kStageB;
-          uint8_t* sSFB = sSFA + 512;
-          const uint32_t tsfa = tmem + L::kSfCol + stage * 8;
-          const uint32_t tsfb = tsfa + 4;
-          tc_cp_32x128b_warpx4(tsfa, smem_desc(smem_u32(sSFA), 16, 128, 0));
-          tc_cp_32x128b_warpx4(tsfb, smem_desc(smem_u32(sSFB), 16, 128, 0));
-          const int nk = min(4, (p.K - kc * 128) / 32);
-          for (int kb = 0; kb < nk; ++kb) {
-            const uint64_t ad = smem_desc(smem_u32(sA) + kb * 32, 16, 1024, 2);
-            const uint64_t bd = smem_desc(smem_u32(sB) + kb * 32, 16, 1024, 2);
-            const uint32_t id = idesc_base | ((uint32_t)kb << 4) | ((uint32_t)kb << 29);
-            mma_mxf8f6f4(d_tmem, ad, bd, id, tsfa, tsfb, (kc > 0 || kb > 0) ? 1u : 0u);
+          const int nv = min(L::KT, p.KC - kc0);
+          uint8_t* sA0 = tiles + stage * L::kStageBytes;
+          uint8_t* sB0 = sA0 + L::kStageA;
+          uint8_t* sSFA0 = sB0 + L::kStageB;
+          uint8_t* sSFB0 = sSFA0 + L::KT * 512;
+          for (int j = 0; j < nv; ++j) {
+            const int kc = kc0 + j;
+            const uint32_t tsfa = tmem + L::kSfCol + (stage * L::KT + j) * 8;
+            const uint32_t tsfb = tsfa + 4;
+            tc_cp_32x128b_warpx4(tsfa, smem_desc(smem_u32(sSFA0 + j * 512), 16, 128, 0));
+            tc_cp_32x128b_warpx4(tsfb, smem_desc(smem_u32(sSFB0 + j * 512), 16, 128, 0));
+            const uint32_t a0 = smem_u32(sA0 + j * L::kTileA), b0 = smem_u32(sB0 + j * L::kTileB);
+            const int nk = min(4, (p.K - kc * 128) / 32);
+            for (int kb = 0; kb < nk; ++kb) {
+              const uint64_t ad = smem_desc(a0 + kb * 32, 16, 1024, 2);
+              const uint64_t bd = smem_desc(b0 + kb * 32, 16, 1024, 2);
+              const uint32_t id = idesc_base | ((uint32_t)kb << 4) | ((uint32_t)kb << 29);
+              mma_mxf8f6f4(d_tmem, ad, bd, id, tsfa, tsfb, (kc > 0 || kb > 0) ? 1u : 0u);
+            }
           }
           tc_commit(&empty[stage]);
           if (++stage == S) { stage = 0; phase ^= 1; }
@@ -377,6 +391,19 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       decode(w, e, m, nt, row0, nrows);
       const int acc = (NACC == 2) ? (it & 1) : 0;
       const int use = (NACC == 2) ? (it >> 1) : it;
+      // W2: the slot and routing weight of every column of this tile, one coalesced load per lane
+      // (issued before the accumulator wait so its latency hides behind it)
+      int w2_slot[(BN + 31) / 32];
+      float w2_wgt[(BN + 31) / 32];
+      if constexpr (!W13) {
+#pragma unroll
+        for (int i = 0; i < (BN + 31) / 32; ++i) {
+          const int col = lane + 32 * i;
+          w2_slot[i] = col < nrows ? p.slot_of_row[row0 + col] : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < (BN + 31) / 32; ++i) w2_wgt[i] = (lane + 32 * i) < nrows ? p.topk_w[w2_slot[i]] : 0.f;
+      }
       if (ok) ok = warp_wait(&acc_full[acc], use & 1, abort_flag, p.status, DEV_TIMEOUT_ACCUM);
       tc_fence_after();
       const uint32_t d_tmem = tmem + (uint32_t)(acc * L::kAccStride);
@@ -387,40 +414,50 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
           tmem_ld_wait();
         }
         if constexpr (W13) {
-          // q 0,1 hold gate features 64m + 32q + lane, q 2,3 the matching up features. Each warp
-          // pair swaps half of the chunk through shared memory: gate warps finish columns 0..7,
-          // up warps columns 8..15.
-          float* xg = xchg;                  // [8][64] gate values of columns 8..15
-          float* xu = xchg + 8 * 64;         // [8][64] up values of columns 0..7
-          const int fq = q & 1;
+          // q 0,1 hold gate features 64m + 32q + lane, q 2,3 the matching up features. The chunk
+          // goes to shared memory as [column][feature]; then thread t owns column t / 8 and the
+          // eight features 8 (t % 8) .. +7: SwiGLU, a four-thread amax per 32-block, and one
+          // 8-byte store of codes.
+          float* gs = xchg;                  // [16][64] gate
+          float* us = xchg + 16 * 64;        // [16][64] up
           if (ok) {
+            float* dst = (q < 2) ? gs : us;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              if (q < 2) xg[c * 64 + 32 * fq + lane] = __uint_as_float(r[8 + c]);
-              else xu[c * 64 + 32 * fq + lane] = __uint_as_float(r[c]);
-            }
+            for (int c = 0; c < 16; ++c) dst[c * 64 + 32 * (q & 1) + lane] = __uint_as_float(r[c]);
           }
           named_bar_sync(1, 128);
           if (ok) {
-            const int feat = 64 * m + 32 * fq + lane;
-            const int cbase = (q < 2) ? 0 : 8;
-#pragma unroll 4
-            for (int c = 0; c < 8; ++c) {
-              const int col = c0 + cbase + c;
-              const float g = (q < 2) ? __uint_as_float(r[c]) : xg[c * 64 + 32 * fq + lane];
-              const float u = (q < 2) ? xu[c * 64 + 32 * fq + lane] : __uint_as_float(r[8 + c]);
-              const float a = silu_mul(g, u);
-              float am = fabsf(a);
+            const int t = threadIdx.x - 128;
+            const int cc = t >> 3, f0 = (t & 7) * 8;
+            const int col = c0 + cc;
+            const float4 g0 = *reinterpret_cast<const float4*>(gs + cc * 64 + f0);
+            const float4 g1 = *reinterpret_cast<const float4*>(gs + cc * 64 + f0 + 4);
+            const float4 u0 = *reinterpret_cast<const float4*>(us + cc * 64 + f0);
+            const float4 u1 = *reinterpret_cast<const float4*>(us + cc * 64 + f0 + 4);
+            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            float a[8];
+            float am = 0.f;
 #pragma unroll
-              for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
-              const int se = e4m3_scale_exp(am);
-              const float sc = __uint_as_float((uint32_t)(127 - se) << 23);
-              const uint32_t code = e4m3x2(a * sc, 0.f) & 0xFF;
-              if (col < nrows) {
-                const size_t prow = (size_t)(row0 + col);
-                p.hq[prow * p.I + feat] = (uint8_t)code;
-                if (lane == 0) p.hs[prow * p.hs_pitch + (feat >> 5)] = (uint8_t)(se + 127);
-                if (p.dbg) p.dbg[prow * p.I + feat] = a;
+            for (int i = 0; i < 8; ++i) {
+              a[i] = silu_mul(gv[i], uv[i]);
+              am = fmaxf(am, fabsf(a[i]));
+            }
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+            const int se = e4m3_scale_exp(am);
+            const float sc = __uint_as_float((uint32_t)(127 - se) << 23);
+            const uint32_t lo = e4m3x2(a[0] * sc, a[1] * sc) | (e4m3x2(a[2] * sc, a[3] * sc) << 16);
+            const uint32_t hi = e4m3x2(a[4] * sc, a[5] * sc) | (e4m3x2(a[6] * sc, a[7] * sc) << 16);
+            if (col < nrows) {
+              const size_t prow = (size_t)(row0 + col);
+              const int feat = 64 * m + f0;
+              *reinterpret_cast<uint2*>(p.hq + prow * p.I + feat) = make_uint2(lo, hi);
+              if ((t & 3) == 0) p.hs[prow * p.hs_pitch + (feat >> 5)] = (uint8_t)(se + 127);
+              if (p.dbg) {
+                float4* d = reinterpret_cast<float4*>(p.dbg + prow * p.I + feat);
+                d[0] = make_float4(a[0], a[1], a[2], a[3]);
+                d[1] = make_float4(a[4], a[5], a[6], a[7]);
               }
             }
           }
@@ -428,14 +465,13 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
         } else {
           if (ok) {
             const int feat = 128 * m + 32 * q + lane;
-#pragma unroll 4
+#pragma unroll
             for (int c = 0; c < 16; ++c) {
               const int col = c0 + c;
-              if (col < nrows) {
-                const int slot = p.slot_of_row[row0 + col];
-                const float wgt = p.topk_w[slot];
-                p.y[(size_t)slot * p.H + feat] = __fmul_rn(wgt, __uint_as_float(r[c]));
-              }
+              // slot and routing weight of column col, loaded once per tile by lane col % 32
+              const int slot = __shfl_sync(0xffffffffu, w2_slot[col >> 5], col & 31);
+              const float wgt = __shfl_sync(0xffffffffu, w2_wgt[col >> 5], col & 31);
+              if (col < nrows) p.y[(size_t)slot * p.H + feat] = __fmul_rn(wgt, __uint_as_float(r[c]));
             }
           }
         }
@@ -477,13 +513,14 @@ static EncodeTiledFn get_encode() {
   return fn;
 }
 
-// Packed weight codes viewed as [tiles * 128 rows, 128 FP4 elements], 64 bytes per row.
-static int make_weight_tmap(CUtensorMap* m, const uint8_t* codes, long long tiles) {
+// Packed weight codes viewed as [tiles * 128 rows, 128 FP4 elements], 64 bytes per row; one box
+// covers `box_tiles` consecutive tiles.
+static int make_weight_tmap(CUtensorMap* m, const uint8_t* codes, long long tiles, int box_tiles) {
   EncodeTiledFn enc = get_encode();
   if (!enc) return MOE_ERR_CUDA;
   cuuint64_t gdim[2] = {128, (cuuint64_t)tiles * 128};
   cuuint64_t gstride[1] = {64};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {128, (cuuint32_t)(128 * box_tiles)};
   cuuint32_t estride[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t*>(codes), gdim, gstride, box,
                    estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -532,16 +569,19 @@ static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const G
 }
 
 template <bool W13>
-static int launch_gemm(const moe_shape* s, const CUtensorMap& tm, const GemmParams& gp, cudaStream_t st) {
-  // activation operand as a TMA tensor for the wide token tile: W13 reads xq [T, H] one row per
-  // gather slot; W2 reads hq [T*k, I] in boxes of 128 plan rows
-  CUtensorMap tmb = tm;
+static int launch_gemm(const moe_shape* s, const uint8_t* codes, const GemmParams& gp, cudaStream_t st) {
   const long long slots = (long long)s->T * s->k;
   const int bn = pick_bn(s);
+  CUtensorMap tm;
+  const int box_tiles = (bn <= 32) ? Smem<16>::KT : (bn <= 64 ? Smem<64>::KT : Smem<128>::KT);
+  int rc0 = make_weight_tmap(&tm, codes, (long long)s->E * gp.MT * gp.KC, box_tiles);
+  if (rc0) return rc0;
+  // activation operand of the wide token tile as a TMA tensor: [T*k plan rows, K] bytes, boxes of
+  // 128 plan rows (W13: the plan-order copy of xq; W2: hq)
+  CUtensorMap tmb = tm;
   const long long max_items = (long long)gp.MT * ((slots + bn - 1) / bn + std::min<long long>(s->E, slots));
   if (bn == 128) {
-    const long long rows = W13 ? (long long)s->T : slots;
-    const int rc = make_act_tmap(&tmb, gp.bq, gp.b_row_bytes, rows, W13 ? 1 : 128);
+    const int rc = make_act_tmap(&tmb, gp.bq, gp.b_row_bytes, slots, 128);
     if (rc) return rc;
   }
   switch (bn) {
@@ -552,13 +592,47 @@ static int launch_gemm(const moe_shape* s, const CUtensorMap& tm, const GemmPara
   }
 }
 
+// Copies the quantised activation rows (codes and scale bytes) into plan order: plan row p gets
+// token slot_of_row[p] / k. Only the first offsets[E] rows are live; the rest are left untouched.
+__global__ void gather_plan_rows_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs, int H,
+                                        const int32_t* __restrict__ slot_of_row, const int32_t* __restrict__ offsets,
+                                        int E, int k, int max_rows, uint8_t* __restrict__ xqp,
+                                        uint8_t* __restrict__ xsp) {
+  const int S = min(offsets[E], max_rows);
+  const int q16 = H / 16, s4 = H / 128;          // 16-byte code chunks and 4-byte scale words per row
+  const int per_row = q16 + s4;
+  const long long n = (long long)S * per_row;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int prow = (int)(i / per_row), j = (int)(i % per_row);
+    const int t = slot_of_row[prow] / k;
+    if (j < q16) {
+      reinterpret_cast<uint4*>(xqp + (size_t)prow * H)[j] = __ldg(reinterpret_cast<const uint4*>(xq + (size_t)t * H) + j);
+    } else {
+      const int w = j - q16;
+      reinterpret_cast<uint32_t*>(xsp + (size_t)prow * (H / 32))[w] =
+          __ldg(reinterpret_cast<const uint32_t*>(xs + (size_t)t * (H / 32)) + w);
+    }
+  }
+}
+
 int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
                const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
-               uint32_t* status, cudaStream_t st) {
+               uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, cudaStream_t st) {
   if (s->T == 0) return MOE_OK;
   GemmParams gp{};
   gp.bq = xq;
   gp.bs = xs;
+  if (pick_bn(s) == 128) {
+    // wide tiles read the token operand in plan order with TMA boxes: gather it once
+    const long long n = (long long)s->T * s->k * (s->H / 16 + s->H / 128);
+    const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);
+    gather_plan_rows_kernel<<<blocks, 256, 0, st>>>(xq, xs, s->H, slot_of_row, offsets, s->E, s->k, s->T * s->k,
+                                                    xq_plan, xs_plan);
+    const int rc = launch_status();
+    if (rc) return rc;
+    gp.bq = xq_plan;
+    gp.bs = xs_plan;
+  }
   gp.b_row_bytes = s->H;
   gp.b_scale_pitch = s->H / 32;
   gp.a_scales = w13s;
@@ -576,10 +650,7 @@ int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const u
   gp.hs_pitch = hs_pitch(s->I);
   gp.dbg = dbg;
   gp.status = status;
-  CUtensorMap tm;
-  int rc = make_weight_tmap(&tm, w13, (long long)s->E * gp.MT * gp.KC);
-  if (rc) return rc;
-  return launch_gemm<true>(s, tm, gp, st);
+  return launch_gemm<true>(s, w13, gp, st);
 }
 
 int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2s,
@@ -604,10 +675,7 @@ int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const ui
   gp.topk_w = topk_w;
   gp.y = y;
   gp.status = status;
-  CUtensorMap tm;
-  int rc = make_weight_tmap(&tm, w2, (long long)s->E * gp.MT * gp.KC);
-  if (rc) return rc;
-  return launch_gemm<false>(s, tm, gp, st);
+  return launch_gemm<false>(s, w2, gp, st);
 }
 
 }  // namespace moe

@@ -551,13 +551,8 @@ __global__ void combine_kernel(const float* __restrict__ y, const int32_t* __res
         const float4* yp = reinterpret_cast<const float4*>(y + ((size_t)t * k + j) * H) + 2 * h8;
         const float4 a = __ldg(yp), b = __ldg(yp + 1);
         const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        if (j == 0) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] = v[q];
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], v[q]);
-        }
+        for (int q = 0; q < 8; ++q) acc[q] = (j == 0) ? v[q] : __fadd_rn(acc[q], v[q]);
       }
     }
     uint32_t o[4];

@@ -17,6 +17,7 @@ CASES = [
     ("c300", 300, 384, 32, 3, 128),     # BN 32, multi-block plan
     ("c130", 130, 256, 8, 2, 576),      # BN 64, W2 K = 576 (partial last chunk)
     ("c600", 600, 256, 8, 2, 256),      # BN 128
+    ("c5w576", 5, 256, 8, 2, 576),      # BN 16: two K-chunks per stage, W2 K = 576 -> odd chunk count
 ]
 
 

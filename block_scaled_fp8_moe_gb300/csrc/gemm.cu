@@ -34,7 +34,7 @@
 namespace moe {
 
 #ifndef MOE_KT_WIDE
-#define MOE_KT_WIDE 1               // K-chunks per stage for token tiles > 32
+#define MOE_KT_WIDE 2               // K-chunks per stage for token tiles > 32
 #endif
 constexpr int kThreads = 256;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
@@ -68,7 +68,7 @@ struct Smem {
   // A pipeline stage holds KT consecutive K-chunks (weight tiles) of 128: small token tiles are
   // weight-streaming bound and each stage hand-off costs a fixed few hundred ns per CTA, so they
   // move 16 KB of packed weights per TMA request.
-  static constexpr int KT = (BN <= 32) ? 2 : MOE_KT_WIDE;
+  static constexpr int KT = (BN <= 32) ? 2 : (BN <= 64 ? 1 : MOE_KT_WIDE);
   static constexpr int kTileA = 16384;                           // one unpacked 128 x 128 FP4 tile
   static constexpr int kTileB = BN * 128;                        // BN rows x 128 FP8
   static constexpr int kStageA = KT * kTileA;

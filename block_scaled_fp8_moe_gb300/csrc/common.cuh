@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -18,7 +20,7 @@ constexpr int kTileRows = 128;         // weight rows per packed tile
 constexpr int kTileCodeBytes = kTileRows * kTileK / 2;   // 8192
 constexpr int kTileScaleBytes = 512;
 
-inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 inline bool shape_ok(const moe_shape* s) {
@@ -39,6 +41,7 @@ struct Workspace {
   size_t topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot;
   size_t xq, xs, hq, hs, y;                                    // forward intermediates
   size_t xqp, xsp;                                             // plan-order copy of xq / xs
+  size_t xnorm, wnorm, cand, ncand;                            // router screen
   size_t total;
 };
 
@@ -67,6 +70,10 @@ inline Workspace workspace_layout(const moe_shape* s) {
   w.y = take(T * k * H * 4);
   w.xqp = take(T * k * H);
   w.xsp = take(T * k * H / 32);
+  w.xnorm = take(T * 4);
+  w.wnorm = take(E * 4);
+  w.cand = take(T * 64 * 4);
+  w.ncand = take(T * 4);
   w.total = off;
   return w;
 }
@@ -96,6 +103,27 @@ inline int num_sms() {
   return n;
 }
 
+// Launch with the programmatic-stream-serialization attribute: the kernel may begin while the
+// previous kernel on `st` finishes (it calls pdl_wait() before reading anything produced upstream).
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
 // Internal launchers (defined in the .cu files), all asynchronous on `st`.
 int launch_quant_mxfp8(int rows, int cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st);
 // When xq/xs are given and the small-batch router runs, it also writes the MXFP8 quantisation of x
@@ -110,5 +138,10 @@ int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const ui
               const float* topk_w, const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
               cudaStream_t st);
 int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, uint16_t* out, cudaStream_t st);
+// Large-T router: certified tensor-core screen + exact recompute of the surviving experts; writes
+// the same score/key rows as the exact router for every expert that can be selected.
+bool router_screen_supported(const moe_shape* s);
+int launch_router_screen(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, void* ws,
+                         float* score, float* key, cudaStream_t st);
 
 }  // namespace moe

@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
 
-  // ---- prologue: plan tables, barriers, TMEM ----
-  for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets[i];
+  // ---- prologue: barriers and TMEM (overlaps the previous kernel), then the plan tables ----
+  pdl_trigger();
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < S; ++s) {
@@ -160,6 +160,12 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
     tmem_alloc(tmem_slot, L::kTmemCols);
     tmem_relinquish();
   }
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmap_a);
+    if (kTmaB) prefetch_tmap(&tmap_b);
+  }
+  pdl_wait();                                    // everything below may read upstream results
+  for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets[i];
   __syncthreads();
   if (warp == 0) {
     // tile starts: warp-parallel prefix sum of ceil(count_e / BN), times MT
@@ -179,10 +185,6 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       run += (s_off[e + 1] - s_off[e] + BN - 1) / BN;
     }
     if (lane == 31) s_cum[E] = incl * p.MT;
-    if (threadIdx.x == 0) {
-      prefetch_tmap(&tmap_a);
-      if (kTmaB) prefetch_tmap(&tmap_b);
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -564,8 +566,7 @@ static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const G
   }
   const long long grid = std::min<long long>(max_items, (long long)L::kCtasPerSm * num_sms());
   if (grid <= 0) return MOE_OK;
-  kern<<<(int)grid, kThreads, smem, st>>>(tm, tmb, gp);
-  return launch_status();
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), (size_t)smem, st, tm, tmb, gp);
 }
 
 template <bool W13>
@@ -598,6 +599,8 @@ __global__ void gather_plan_rows_kernel(const uint8_t* __restrict__ xq, const ui
                                         const int32_t* __restrict__ slot_of_row, const int32_t* __restrict__ offsets,
                                         int E, int k, int max_rows, uint8_t* __restrict__ xqp,
                                         uint8_t* __restrict__ xsp) {
+  pdl_trigger();
+  pdl_wait();
   const int S = min(offsets[E], max_rows);
   const int q16 = H / 16, s4 = H / 128;          // 16-byte code chunks and 4-byte scale words per row
   const int per_row = q16 + s4;
@@ -626,9 +629,8 @@ int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const u
     // wide tiles read the token operand in plan order with TMA boxes: gather it once
     const long long n = (long long)s->T * s->k * (s->H / 16 + s->H / 128);
     const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);
-    gather_plan_rows_kernel<<<blocks, 256, 0, st>>>(xq, xs, s->H, slot_of_row, offsets, s->E, s->k, s->T * s->k,
-                                                    xq_plan, xs_plan);
-    const int rc = launch_status();
+    const int rc = launch_pdl(gather_plan_rows_kernel, dim3(blocks), dim3(256), 0, st, xq, xs, s->H, slot_of_row,
+                              offsets, s->E, s->k, s->T * s->k, xq_plan, xs_plan);
     if (rc) return rc;
     gp.bq = xq_plan;
     gp.bs = xs_plan;

@@ -8,12 +8,15 @@
 
 #include "common.cuh"
 #include "mx.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 
 // 8 bf16 elements per thread, 4 threads per 32-block.
 __global__ void quant_mxfp8_kernel(const uint4* __restrict__ x, uint2* __restrict__ q, uint8_t* __restrict__ s,
                                    long long n_groups) {
+  pdl_trigger();
+  pdl_wait();
   // The loop bound is uniform across the warp (the shuffles below need every lane).
   const unsigned lane = threadIdx.x & 31;
   for (long long g0 = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31u); g0 < n_groups;
@@ -132,9 +135,8 @@ int launch_quant_mxfp8(int rows, int cols, const uint16_t* x, uint8_t* q, uint8_
   int threads = 256;
   long long need = (groups + threads - 1) / threads;
   int blocks = (int)std::min<long long>(need, (long long)num_sms() * 8);
-  quant_mxfp8_kernel<<<blocks, threads, 0, st>>>(reinterpret_cast<const uint4*>(x), reinterpret_cast<uint2*>(q), s,
-                                                 groups);
-  return launch_status();
+  return launch_pdl(quant_mxfp8_kernel, dim3(blocks), dim3(threads), 0, st, reinterpret_cast<const uint4*>(x),
+                    reinterpret_cast<uint2*>(q), s, groups);
 }
 
 }  // namespace moe

@@ -10,42 +10,10 @@
 
 #include "common.cuh"
 #include "mx.cuh"
+#include "ptx.cuh"
+#include "router_math.cuh"
 
 namespace moe {
-
-// ---------------------------------------------------------------------------------------------
-// Library-independent exp / sigmoid from IEEE fp32 +, -, *, / (each correctly rounded; the
-// _rn intrinsics keep the compiler from contracting them). exp(t), t in [-80, 80]:
-// n = rint(t / ln2); r = (t - n ln2_hi) - n ln2_lo (Cody & Waite); degree-7 Taylor polynomial
-// of exp(r) in Horner form; times 2^n (exact). ln2_hi keeps 16 significant bits so n * ln2_hi
-// is exact. Coefficients are 1/k! rounded to fp32.
-// ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ float exp_cw(float t) {
-  const float kLog2e = 1.4426950408889634f;
-  const float kLn2Hi = 0.693145751953125f;              // 45426 / 2^16
-  const float kLn2Lo = 1.4286067653302226e-06f;         // ln2 - kLn2Hi, rounded to fp32
-  float n = rintf(__fmul_rn(t, kLog2e));
-  float r = __fsub_rn(t, __fmul_rn(n, kLn2Hi));
-  r = __fsub_rn(r, __fmul_rn(n, kLn2Lo));
-  float p = 1.9841269841269841e-04f;                    // 1/7!
-  p = __fadd_rn(__fmul_rn(p, r), 1.3888888888888889e-03f);   // 1/6!
-  p = __fadd_rn(__fmul_rn(p, r), 8.3333333333333332e-03f);   // 1/5!
-  p = __fadd_rn(__fmul_rn(p, r), 4.1666666666666664e-02f);   // 1/4!
-  p = __fadd_rn(__fmul_rn(p, r), 1.6666666666666666e-01f);   // 1/3!
-  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-  const float two_n = __int_as_float(((int)n + 127) << 23);
-  return __fmul_rn(p, two_n);
-}
-
-__device__ __forceinline__ float sigmoid_cw(float z) {
-  float t = fminf(fmaxf(-z, -80.0f), 80.0f);
-  return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_cw(t)));
-}
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ---------------------------------------------------------------------------------------------
 // Logits, small T (decode): one warp per expert. Lane l owns the chunks c = l, l + 32, ...;
@@ -58,6 +26,8 @@ __global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __res
                                                            const uint16_t* __restrict__ wr,
                                                            const float* __restrict__ bias, int T, int H, int E,
                                                            float* __restrict__ score, float* __restrict__ key) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float part[8][kSmallT][33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + warp;
@@ -123,6 +93,8 @@ __global__ void __launch_bounds__(256) router_decode_kernel(const uint16_t* __re
                                                             const float* __restrict__ bias, int T, int H, int E,
                                                             float* __restrict__ score, float* __restrict__ key,
                                                             uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ __align__(16) uint8_t dsm_dec[];
   const int NC = H / kRouterChunk;
   uint16_t* xsm = reinterpret_cast<uint16_t*>(dsm_dec);                                // [T][NC][kDecPad]
@@ -212,6 +184,8 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const uint16_t* __res
                                                            const uint16_t* __restrict__ wr,
                                                            const float* __restrict__ bias, int T, int H, int E,
                                                            float* __restrict__ score, float* __restrict__ key) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ __align__(16) float xs[kRouterChunk][64];
   __shared__ __align__(16) float ws[kRouterChunk][64];
   const int tid = threadIdx.x;
@@ -325,6 +299,8 @@ __global__ void __launch_bounds__(512) topk_plan_kernel(const float* __restrict_
                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                         int32_t* __restrict__ slot_of_row,
                                                         int32_t* __restrict__ row_of_slot) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint32_t dsm[];
   uint32_t* mask = dsm;                                         // [E][8]
   int16_t* sidx = reinterpret_cast<int16_t*>(dsm + E * 8);      // [kPlanBlock][k]
@@ -438,6 +414,8 @@ __global__ void __launch_bounds__(512) topk_plan_kernel(const float* __restrict_
 __global__ void __launch_bounds__(512) plan_scan_kernel(const int32_t* __restrict__ cnt, int nb, int E,
                                                         int32_t* __restrict__ base, int32_t* __restrict__ counts,
                                                         int32_t* __restrict__ offsets) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int tot[kMaxE];
   __shared__ int total_s;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -462,6 +440,8 @@ __global__ void __launch_bounds__(512) plan_scan_kernel(const int32_t* __restric
 __global__ void plan_scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ rank,
                                     const int32_t* __restrict__ base, int T, int E, int k,
                                     int32_t* __restrict__ slot_of_row, int32_t* __restrict__ row_of_slot) {
+  pdl_trigger();
+  pdl_wait();
   const long long n = (long long)T * k;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const int r = rank[i];
@@ -489,6 +469,7 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
   float* score = ws_ptr<float>(ws, L.score);
   float* key = ws_ptr<float>(ws, L.key);
   const size_t dec_smem = router_decode_smem(T, H);
+  int rc0 = MOE_OK;
   if (T <= kSmallT && dec_smem <= kDecodeSmemMax) {
     static bool dec_attr = false;
     if (!dec_attr) {
@@ -498,16 +479,20 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
       dec_attr = true;
     }
     const bool fuse = xq && xs;
-    router_decode_kernel<<<ceil_div(E, kDecEpc), 256, dec_smem, st>>>(x, wr, bias, T, H, E, score, key,
-                                                                      fuse ? xq : nullptr, fuse ? xs : nullptr);
+    uint8_t* fq = fuse ? xq : nullptr;
+    uint8_t* fs = fuse ? xs : nullptr;
+    rc0 = launch_pdl(router_decode_kernel, dim3(ceil_div(E, kDecEpc)), dim3(256), dec_smem, st, x, wr, bias, T, H, E,
+                     score, key, fq, fs);
     if (quant_done) *quant_done = fuse;
   } else if (T <= kSmallT) {
-    router_small_kernel<<<ceil_div(E, 8), 256, 0, st>>>(x, wr, bias, T, H, E, score, key);
+    rc0 = launch_pdl(router_small_kernel, dim3(ceil_div(E, 8)), dim3(256), 0, st, x, wr, bias, T, H, E, score, key);
+  } else if (router_screen_supported(s)) {
+    rc0 = launch_router_screen(s, x, wr, bias, ws, score, key, st);
   } else {
-    dim3 grid(ceil_div(T, 64), ceil_div(E, 64));
-    router_tiled_kernel<<<grid, 256, 0, st>>>(x, wr, bias, T, H, E, score, key);
+    rc0 = launch_pdl(router_tiled_kernel, dim3(ceil_div(T, 64), ceil_div(E, 64)), dim3(256), 0, st, x, wr, bias, T,
+                     H, E, score, key);
   }
-  int rc = launch_status();
+  int rc = rc0;
   if (rc) return rc;
   const int nb = ceil_div(T, kPlanBlock);
   const size_t smem = (size_t)E * 8 * 4 + (size_t)kPlanBlock * k * 2;
@@ -519,17 +504,15 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
   int32_t* cnt = ws_ptr<int32_t>(ws, L.cnt);
   int32_t* base = ws_ptr<int32_t>(ws, L.base);
   int32_t* rank = ws_ptr<int32_t>(ws, L.rank);
-  topk_plan_kernel<<<nb, 512, smem, st>>>(score, key, dead, T, E, k, topk_idx, topk_w, cnt, rank, counts, offsets,
-                                          slot_of_row, row_of_slot);
-  rc = launch_status();
+  rc = launch_pdl(topk_plan_kernel, dim3(nb), dim3(512), smem, st, score, key, dead, T, E, k, topk_idx, topk_w, cnt,
+                  rank, counts, offsets, slot_of_row, row_of_slot);
   if (rc || nb == 1) return rc;
-  plan_scan_kernel<<<1, 512, 0, st>>>(cnt, nb, E, base, counts, offsets);
-  rc = launch_status();
+  rc = launch_pdl(plan_scan_kernel, dim3(1), dim3(512), 0, st, cnt, nb, E, base, counts, offsets);
   if (rc) return rc;
   const long long n = (long long)T * k;
   const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 4);
-  plan_scatter_kernel<<<blocks, 256, 0, st>>>(topk_idx, rank, base, T, E, k, slot_of_row, row_of_slot);
-  return launch_status();
+  return launch_pdl(plan_scatter_kernel, dim3(blocks), dim3(256), 0, st, topk_idx, rank, base, T, E, k, slot_of_row,
+                    row_of_slot);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -538,6 +521,8 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
 // ---------------------------------------------------------------------------------------------
 __global__ void combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_of_slot, int T, int H,
                                int k, uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int H8 = H / 8;
   const long long n = (long long)T * H8;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
@@ -570,8 +555,7 @@ int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slo
   const long long n = (long long)s->T * (s->H / 8);
   if (n == 0) return MOE_OK;
   const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);
-  combine_kernel<<<blocks, 256, 0, st>>>(y, row_of_slot, s->T, s->H, s->k, out);
-  return launch_status();
+  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, st, y, row_of_slot, s->T, s->H, s->k, out);
 }
 
 }  // namespace moe

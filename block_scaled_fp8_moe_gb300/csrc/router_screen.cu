@@ -1,0 +1,386 @@
+// Certified tensor-core screen for the router at large T, followed by an exact recompute of the
+// few experts that can still be in a row's top-k. The selected experts, their weights and the
+// plan are bit-identical to the fixed-order fp32 router (the screen only prunes experts that
+// provably cannot be selected).
+//
+// "New Deepseek 4.1 flash recipe", post 6 "How it works" item 3 (TileKernels MoE top-k gate) and
+// "Why TileLang" (fixed-order reductions); TP4 serving profile README, settings table, "Target LM
+// head" row: read a cheap screen with a proven error bound, then compute exactly only what can
+// still win.
+//
+// 1. router_norms_kernel: ||x_t||_2 and ||Wr_e||_2 (fp32, rounded up by a relative 2^-10).
+// 2. router_screen_kernel: L~ = x Wr^T on tcgen05 (bf16 x bf16, fp32 accumulate; 128 rows x all
+//    E experts per CTA, TMA-fed, accumulator in TMEM). bf16 products are exact, so the only error
+//    is accumulation: for any summation order |L~ - L| <= gamma ||x|| ||Wr_e||, gamma = 6 H 2^-24
+//    (covers the tensor core's and the fixed-order fp32 path's roundings; Cauchy-Schwarz bounds
+//    sum |x_h w_h|). The sigmoid is 1/4-Lipschitz, so every exact key lies in
+//    [key~ - d_e, key~ + d_e], d_e = gamma ||x|| ||Wr_e|| / 4 + 2e-6 (the same sigmoid code on both
+//    sides: its rounding and the bias addition are inside the 2e-6). With tau = the k-th largest
+//    lower bound, an expert with upper bound < tau is below the k-th exact key: it cannot be
+//    selected. Every other expert is a candidate.
+// 3. router_exact_kernel: one warp per row recomputes the candidates' logits in the fixed chunked
+//    order, then writes that row's keys (-inf for pruned experts) and scores for the top-k kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "router_math.cuh"
+
+namespace moe {
+
+constexpr int kScrRows = 128;        // rows (tokens) per CTA = MMA M
+constexpr int kScrK = 64;            // bf16 elements of K per stage (128-byte rows)
+constexpr int kScrStages = 4;
+constexpr int kScrMaxE = 256;
+constexpr int kCandMax = 64;
+constexpr int kExactWarps = 8;
+constexpr uint64_t kScrWaitNs = 1000000000ull;
+
+bool router_screen_supported(const moe_shape* s) {
+  return s->E <= kScrMaxE && s->H % kScrK == 0 && s->H <= 4096 && s->k <= s->E;
+}
+
+__global__ void router_norms_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, int T, int H,
+                                    int E, float* __restrict__ xnorm, float* __restrict__ wnorm) {
+  pdl_trigger();
+  pdl_wait();
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int r = warp; r < T + E; r += nwarps) {
+    const uint16_t* row = r < T ? x + (size_t)r * H : wr + (size_t)(r - T) * H;
+    float ss = 0.f;
+    for (int h = lane * 8; h < H; h += 256) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + h));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float a = bf_lo(w[q]), b = bf_hi(w[q]);
+        ss = fmaf(a, a, ss);
+        ss = fmaf(b, b, ss);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    // fp32 sum of squares is within H * 2^-24 (relative) of the exact value; 2^-10 covers it
+    const float n = sqrtf(ss) * (1.0f + 0.0009765625f);
+    if (lane == 0) {
+      if (r < T) xnorm[r] = n;
+      else wnorm[r - T] = n;
+    }
+  }
+}
+
+struct ScreenParams {
+  const float* bias;
+  const float* xnorm;
+  const float* wnorm;
+  int T, H, E, EP, k;
+  float gamma4;          // gamma / 4
+  int32_t* cand;         // [T, kCandMax]
+  int32_t* ncand;        // [T]; -1 = too many candidates, recompute every expert
+  uint32_t* status;
+};
+
+__global__ void __launch_bounds__(256, 1) router_screen_kernel(const __grid_constant__ CUtensorMap tmx,
+                                                                const __grid_constant__ CUtensorMap tmw,
+                                                                const ScreenParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int stageA = kScrRows * kScrK * 2;           // 16 KB
+  const int stageB = p.EP * kScrK * 2;               // EP x 128 B
+  const int stage_bytes = stageA + stageB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + kScrStages * stage_bytes);
+  uint64_t* empty = full + kScrStages;
+  uint64_t* accb = empty + kScrStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * kScrRows;
+  const int NS = p.H / kScrK;
+
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < kScrStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accb, 1);
+    mbar_fence_init();
+    prefetch_tmap(&tmx);
+    prefetch_tmap(&tmw);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  pdl_wait();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int s = 0; s < NS; ++s) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, kScrWaitNs, abort_flag, p.status, DEV_TIMEOUT_EMPTY)) break;
+        uint8_t* sA = base + stage * stage_bytes;
+        mbar_arrive_expect_tx(&full[stage], stage_bytes);
+        tma_load_2d(sA, &tmx, s * kScrK, t0, &full[stage]);
+        tma_load_2d(sA + stageA, &tmw, s * kScrK, 0, &full[stage]);
+        if (++stage == kScrStages) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint32_t idesc = idesc_bf16_f32(kScrRows, p.EP);
+      for (int s = 0; s < NS; ++s) {
+        if (!mbar_wait(&full[stage], phase, kScrWaitNs, abort_flag, p.status, DEV_TIMEOUT_FULL)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(base + stage * stage_bytes), b0 = a0 + stageA;
+#pragma unroll
+        for (int kb = 0; kb < kScrK / 16; ++kb)
+          mma_bf16(tmem, smem_desc(a0 + kb * 32, 16, 1024, 2), smem_desc(b0 + kb * 32, 16, 1024, 2), idesc,
+                   (s > 0 || kb > 0) ? 1u : 0u);
+        tc_commit(&empty[stage]);
+        if (++stage == kScrStages) { stage = 0; phase ^= 1; }
+      }
+      if (ok) tc_commit(accb);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // one thread per row: TMEM lane = row within the CTA
+    const int tl = threadIdx.x - 128;
+    const int tok = t0 + tl;
+    const uint32_t lane_base = (uint32_t)(32 * (warp - 4)) << 16;
+    uint32_t okw = 1;
+    if (lane == 0) okw = mbar_wait(accb, 0, kScrWaitNs, abort_flag, p.status, DEV_TIMEOUT_ACCUM) ? 1u : 0u;
+    const bool ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
+    tc_fence_after();
+    // the stage buffers are free now: lower bounds lo[e][row], 128 KB
+    float* lo = reinterpret_cast<float*>(base);
+    const float xn = (tok < p.T) ? p.xnorm[tok] : 0.f;
+    if (ok) {
+      for (int c0 = 0; c0 < p.EP; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_base + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int e = c0 + c;
+          if (e < p.E) {
+            const float key = __fadd_rn(sigmoid_cw(__uint_as_float(r[c])), p.bias[e]);
+            const float d = p.gamma4 * xn * p.wnorm[e] + 2e-6f;
+            lo[e * kScrRows + tl] = key - d;
+          }
+        }
+      }
+    }
+    // tau = k-th largest lower bound (selection by repeated maximum, taken entries set to -inf)
+    float tau = -INFINITY;
+    if (ok) {
+      for (int j = 0; j < p.k; ++j) {
+        float best = -INFINITY;
+        int be = 0;
+        for (int e = 0; e < p.E; ++e) {
+          const float v = lo[e * kScrRows + tl];
+          if (v > best) { best = v; be = e; }
+        }
+        tau = best;
+        lo[be * kScrRows + tl] = -INFINITY;
+      }
+    }
+    int n = 0;
+    if (ok) {
+      for (int c0 = 0; c0 < p.EP; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_base + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int e = c0 + c;
+          if (e < p.E && tok < p.T) {
+            const float key = __fadd_rn(sigmoid_cw(__uint_as_float(r[c])), p.bias[e]);
+            const float d = p.gamma4 * xn * p.wnorm[e] + 2e-6f;
+            if (key + d >= tau) {
+              if (n < kCandMax) p.cand[(size_t)tok * kCandMax + n] = e;
+              ++n;
+            }
+          }
+        }
+      }
+    }
+    if (tok < p.T) p.ncand[tok] = (!ok || n > kCandMax) ? -1 : n;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// One warp per row: exact fixed-order logits of the candidates (every expert if the list
+// overflowed), sigmoid, key; the row's keys are written in full (-inf where pruned).
+__global__ void __launch_bounds__(kExactWarps * 32) router_exact_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, const float* __restrict__ bias,
+    const int32_t* __restrict__ cand, const int32_t* __restrict__ ncand, int T, int H, int E,
+    float* __restrict__ score, float* __restrict__ key) {
+  extern __shared__ __align__(16) uint8_t dsm_ex[];
+  pdl_trigger();
+  pdl_wait();
+  const int NC = H / kRouterChunk;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // per warp: the row in padded chunks (66 bf16 per chunk), partials [32][NC + 1], results [32]x2
+  const size_t xw_bytes = align_up((size_t)NC * 66 * 2, 16);
+  const size_t per_warp = xw_bytes + (size_t)32 * (NC + 1) * 4 + 64 * 4 + 32 * 4;
+  uint8_t* wbase = dsm_ex + warp * per_warp;
+  uint16_t* xsm = reinterpret_cast<uint16_t*>(wbase);
+  float* part = reinterpret_cast<float*>(wbase + xw_bytes);
+  float* rs = part + 32 * (NC + 1);          // [32] scores of the batch
+  float* rk = rs + 32;                        // [32] keys
+  int* re = reinterpret_cast<int*>(rk + 32);  // [32] experts
+  for (int t = blockIdx.x * kExactWarps + warp; t < T; t += gridDim.x * kExactWarps) {
+    const int nc = ncand[t];
+    const int ncount = nc < 0 ? E : nc;
+    // stage the row
+    for (int i = lane; i < H / 8; i += 32) {
+      const int h = i * 8;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + h));
+      uint32_t* d = reinterpret_cast<uint32_t*>(xsm + (h / kRouterChunk) * 66 + (h % kRouterChunk));
+      d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+    }
+    // the full key row first (pruned experts never win), then the candidates' exact values
+    for (int e = lane; e < E; e += 32) {
+      key[(size_t)t * E + e] = -INFINITY;
+      score[(size_t)t * E + e] = 0.f;
+    }
+    __syncwarp();
+    for (int b0 = 0; b0 < ncount; b0 += 32) {
+      const int nb = min(32, ncount - b0);
+      for (int ci = 0; ci < nb; ++ci) {
+        const int e = nc < 0 ? b0 + ci : cand[(size_t)t * kCandMax + b0 + ci];
+        for (int c = lane; c < NC; c += 32) {
+          const uint4* wp = reinterpret_cast<const uint4*>(wr + (size_t)e * H + (size_t)c * kRouterChunk);
+          const uint32_t* xp = reinterpret_cast<const uint32_t*>(xsm + c * 66);
+          float pacc = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 wv = __ldg(wp + i);
+            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t xw = xp[i * 4 + q];
+              pacc = __fmaf_rn(bf_lo(xw), bf_lo(ww[q]), pacc);
+              pacc = __fmaf_rn(bf_hi(xw), bf_hi(ww[q]), pacc);
+            }
+          }
+          part[ci * (NC + 1) + c] = pacc;
+        }
+        if (lane == 0) re[ci] = e;
+      }
+      __syncwarp();
+      if (lane < nb) {
+        float acc = 0.f;
+        for (int c = 0; c < NC; ++c) acc = __fadd_rn(acc, part[lane * (NC + 1) + c]);
+        const int e = re[lane];
+        const float sc = sigmoid_cw(acc);
+        rs[lane] = sc;
+        rk[lane] = __fadd_rn(sc, bias[e]);
+      }
+      __syncwarp();
+      if (lane < nb) {
+        const int e = re[lane];
+        score[(size_t)t * E + e] = rs[lane];
+        key[(size_t)t * E + e] = rk[lane];
+      }
+      __syncwarp();
+    }
+  }
+}
+
+typedef CUresult (*EncodeTiledFnR)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static int make_bf16_tmap(CUtensorMap* m, const uint16_t* base, int cols, int rows, int box_rows) {
+  static EncodeTiledFnR enc = nullptr;
+  if (!enc) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return MOE_ERR_CUDA;
+    enc = reinterpret_cast<EncodeTiledFnR>(ptr);
+  }
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kScrK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), gdim, gstride, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_router_screen(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, void* ws,
+                         float* score, float* key, cudaStream_t st) {
+  const Workspace L = workspace_layout(s);
+  const int T = s->T, H = s->H, E = s->E;
+  float* xnorm = ws_ptr<float>(ws, L.xnorm);
+  float* wnorm = ws_ptr<float>(ws, L.wnorm);
+  int32_t* cand = ws_ptr<int32_t>(ws, L.cand);
+  int32_t* ncand = ws_ptr<int32_t>(ws, L.ncand);
+  const int nb = (int)std::min<long long>(((long long)(T + E) * 32 + 255) / 256, (long long)num_sms() * 8);
+  int rc = launch_pdl(router_norms_kernel, dim3(nb), dim3(256), 0, st, x, wr, T, H, E, xnorm, wnorm);
+  if (rc) return rc;
+  ScreenParams sp{};
+  sp.bias = bias;
+  sp.xnorm = xnorm;
+  sp.wnorm = wnorm;
+  sp.T = T;
+  sp.H = H;
+  sp.E = E;
+  sp.EP = (E + 15) / 16 * 16;
+  sp.k = s->k;
+  sp.gamma4 = (float)(6.0 * H / 16777216.0 / 4.0);
+  sp.cand = cand;
+  sp.ncand = ncand;
+  sp.status = ws_ptr<uint32_t>(ws, L.status);
+  CUtensorMap tmx, tmw;
+  rc = make_bf16_tmap(&tmx, x, H, T, kScrRows);
+  if (rc) return rc;
+  rc = make_bf16_tmap(&tmw, wr, H, E, sp.EP);
+  if (rc) return rc;
+  const int smem = 1024 + kScrStages * (kScrRows * kScrK * 2 + sp.EP * kScrK * 2) + 256;
+  static int attr = 0;
+  if (attr < smem) {
+    if (cudaFuncSetAttribute(router_screen_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr = smem;
+  }
+  rc = launch_pdl(router_screen_kernel, dim3(ceil_div(T, kScrRows)), dim3(256), (size_t)smem, st, tmx, tmw, sp);
+  if (rc) return rc;
+  const int NC = H / kRouterChunk;
+  const size_t per_warp = align_up((size_t)NC * 66 * 2, 16) + (size_t)32 * (NC + 1) * 4 + 64 * 4 + 32 * 4;
+  const size_t esmem = per_warp * kExactWarps;
+  static size_t eattr = 0;
+  if (eattr < esmem) {
+    if (cudaFuncSetAttribute(router_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)esmem) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    eattr = esmem;
+  }
+  const int eg = (int)std::min<long long>((T + kExactWarps - 1) / kExactWarps, (long long)num_sms() * 4);
+  return launch_pdl(router_exact_kernel, dim3(eg), dim3(kExactWarps * 32), esmem, st, x, wr, bias, cand, ncand, T, H,
+                    E, score, key);
+}
+
+}  // namespace moe

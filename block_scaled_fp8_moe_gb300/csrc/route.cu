@@ -267,9 +267,6 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const uint16_t* __res
 // ---------------------------------------------------------------------------------------------
 constexpr int kTopkWarps = 16;
 
-__device__ __forceinline__ bool better(float ka, int ea, float kb, int eb) {
-  return ka > kb || (ka == kb && ea < eb);
-}
 
 __device__ void block_exclusive_scan(int* vals, int n, int* total) {
   // vals in shared memory, n <= 1024; blockDim.x == 512
@@ -292,6 +289,83 @@ __device__ void block_exclusive_scan(int* vals, int n, int* total) {
   __syncthreads();
 }
 
+// One token's top-k on one warp. Lane l holds experts l, l + 32, ... (NI of them) and its own
+// best untaken (key desc, expert asc); each round is a warp arg-max over the lanes' bests (two
+// warp reductions), after which only the winning lane rescans its NI values. Selected weights: sigma_j / sum, the sum
+// accumulated in rank order (identical on every lane). Lane j < k ends with the j-th choice.
+template <int NI>
+__device__ __forceinline__ void warp_topk(const float* __restrict__ krow, const float* __restrict__ srow, int E, int k,
+                                          int lane, int16_t* sidx, int* my_e, float* my_s, float* sum_out) {
+  float kv[NI], sv[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int e = lane + 32 * i;
+    kv[i] = (e < E) ? krow[e] : 0.f;
+    sv[i] = (e < E) ? srow[e] : 0.f;
+  }
+  uint32_t taken = 0;
+  auto local_best = [&](float& bk, int& be) {
+    bk = 0.f;
+    be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (be == 0x7fffffff || kv[i] > bk)) { bk = kv[i]; be = e; }
+    }
+  };
+  float lk;
+  int le;
+  local_best(lk, le);
+  float sel_sum = 0.f;
+  for (int j = 0; j < k; ++j) {
+    // warp arg-max: the largest key (order-preserving unsigned image; keys are never -0 or NaN),
+    // then the lowest expert among the lanes holding it; a lane with nothing left offers 0
+    uint32_t u = 0;
+    if (le != 0x7fffffff) {
+      const uint32_t bits = __float_as_uint(lk);
+      u = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+    }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, u);
+    const int be = __reduce_min_sync(0xffffffffu, (u == m && le != 0x7fffffff) ? le : 0x7fffffff);
+    float own = 0.f;                            // the winner's score, read by its owner lane
+    if ((be & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < NI; ++i)
+        if (i == (be >> 5)) own = sv[i];
+      taken |= 1u << (be >> 5);
+      local_best(lk, le);
+    }
+    const float sc = __shfl_sync(0xffffffffu, own, be & 31);
+    sel_sum = __fadd_rn(sel_sum, sc);
+    if (lane == j) { *my_e = be; *my_s = sc; }
+    if (sidx && lane == 0) sidx[j] = (int16_t)be;
+  }
+  *sum_out = sel_sum;
+}
+
+// Top-k alone, one warp per token over the whole grid (the multi-block plan reads its result).
+template <int NI>
+__global__ void __launch_bounds__(256) topk_select_kernel(const float* __restrict__ score,
+                                                          const float* __restrict__ key, int T, int E, int k,
+                                                          int32_t* __restrict__ topk_idx,
+                                                          float* __restrict__ topk_w) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+    int my_e = -1;
+    float my_s = 0.f, sum = 0.f;
+    warp_topk<NI>(key + (size_t)t * E, score + (size_t)t * E, E, k, lane, nullptr, &my_e, &my_s, &sum);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = my_e;
+      topk_w[(size_t)t * k + lane] = __fdiv_rn(my_s, sum);
+    }
+  }
+}
+
+// SELECT: this CTA routes its tokens (16 warps, one token at a time each); otherwise the choices
+// are read back from topk_idx (written by topk_select_kernel).
+template <int NI, bool SELECT>
 __global__ void __launch_bounds__(512) topk_plan_kernel(const float* __restrict__ score, const float* __restrict__ key,
                                                         const uint8_t* __restrict__ dead, int T, int E, int k,
                                                         int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
@@ -311,47 +385,19 @@ __global__ void __launch_bounds__(512) topk_plan_kernel(const float* __restrict_
   const int nt = min(kPlanBlock, T - tb0);
   for (int i = threadIdx.x; i < E * 8; i += blockDim.x) mask[i] = 0;
 
-  for (int tl = warp; tl < nt; tl += kTopkWarps) {
-    const int t = tb0 + tl;
-    float kv[32], sv[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      kv[i] = (e < E) ? key[(size_t)t * E + e] : 0.f;
-      sv[i] = (e < E) ? score[(size_t)t * E + e] : 0.f;
-    }
-    uint32_t taken = 0;
-    float sel_sum = 0.f;
-    int my_e = -1;
-    float my_s = 0.f;
-    for (int j = 0; j < k; ++j) {
-      float bk = 0.f;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (be == 0x7fffffff || kv[i] > bk)) { bk = kv[i]; be = e; }
+  if (SELECT) {
+    for (int tl = warp; tl < nt; tl += kTopkWarps) {
+      const int t = tb0 + tl;
+      int my_e = -1;
+      float my_s = 0.f, sum = 0.f;
+      warp_topk<NI>(key + (size_t)t * E, score + (size_t)t * E, E, k, lane, sidx + tl * k, &my_e, &my_s, &sum);
+      if (lane < k) {
+        topk_idx[(size_t)t * k + lane] = my_e;
+        topk_w[(size_t)t * k + lane] = __fdiv_rn(my_s, sum);
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-        int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (oe != 0x7fffffff && (be == 0x7fffffff || better(ok, oe, bk, be))) { bk = ok; be = oe; }
-      }
-      float own = 0.f;                            // the winner's score, read by its owner lane
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i == (be >> 5)) own = sv[i];
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      const float s = __shfl_sync(0xffffffffu, own, be & 31);
-      sel_sum = __fadd_rn(sel_sum, s);           // rank order, identical on every lane
-      if (lane == j) { my_e = be; my_s = s; }
-      sidx[tl * k + j] = (int16_t)be;
     }
-    if (lane < k) {
-      topk_idx[(size_t)t * k + lane] = my_e;
-      topk_w[(size_t)t * k + lane] = __fdiv_rn(my_s, sel_sum);
-    }
+  } else {
+    for (int i = threadIdx.x; i < nt * k; i += blockDim.x) sidx[i] = (int16_t)topk_idx[(size_t)tb0 * k + i];
   }
   __syncthreads();
   // per-expert token bitmasks of this block (bit order = token order)
@@ -455,6 +501,86 @@ __global__ void plan_scatter_kernel(const int32_t* __restrict__ topk_idx, const 
   }
 }
 
+template <int NI>
+static int launch_topk_plan_ni(int nb, int E, size_t smem, cudaStream_t st, const float* score, const float* key,
+                               const uint8_t* dead, int T, int k, int32_t* topk_idx, float* topk_w, int32_t* cnt,
+                               int32_t* rank, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
+                               int32_t* row_of_slot) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(topk_plan_kernel<NI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(topk_plan_kernel<NI, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
+            cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  if (nb == 1)
+    return launch_pdl(topk_plan_kernel<NI, true>, dim3(1), dim3(512), smem, st, score, key, dead, T, E, k, topk_idx,
+                      topk_w, cnt, rank, counts, offsets, slot_of_row, row_of_slot);
+  // many blocks: selection spread over the whole GPU, then the per-block plan
+  const int sel_blocks = (int)std::min<long long>(((long long)T + 7) / 8, (long long)num_sms() * 8);
+  int rc = launch_pdl(topk_select_kernel<NI>, dim3(sel_blocks), dim3(256), 0, st, score, key, T, E, k, topk_idx,
+                      topk_w);
+  if (rc) return rc;
+  return launch_pdl(topk_plan_kernel<NI, false>, dim3(nb), dim3(512), smem, st, score, key, dead, T, E, k, topk_idx,
+                    topk_w, cnt, rank, counts, offsets, slot_of_row, row_of_slot);
+}
+
+// NI = experts per lane, the smallest power of two with 32 * NI >= E.
+static int launch_topk_plan(int nb, int E, size_t smem, cudaStream_t st, const float* score, const float* key,
+                            const uint8_t* dead, int T, int k, int32_t* topk_idx, float* topk_w, int32_t* cnt,
+                            int32_t* rank, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
+                            int32_t* row_of_slot) {
+#define MOE_TOPK_CASE(N)                                                                                        \
+  if (E <= 32 * N)                                                                                              \
+    return launch_topk_plan_ni<N>(nb, E, smem, st, score, key, dead, T, k, topk_idx, topk_w, cnt, rank, counts, \
+                                  offsets, slot_of_row, row_of_slot);
+  MOE_TOPK_CASE(1)
+  MOE_TOPK_CASE(2)
+  MOE_TOPK_CASE(4)
+  MOE_TOPK_CASE(8)
+  MOE_TOPK_CASE(16)
+  MOE_TOPK_CASE(32)
+#undef MOE_TOPK_CASE
+  return MOE_ERR_UNSUPPORTED_SHAPE;
+}
+
+// One plan block, plain launch (no programmatic serialisation): used by the allocation-free router.
+template <int NI>
+static int launch_topk_single_plain_ni(size_t smem, cudaStream_t st, const float* score, const float* key,
+                                       const uint8_t* dead, int T, int E, int k, int32_t* topk_idx, float* topk_w,
+                                       int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
+                                       int32_t* row_of_slot) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(topk_plan_kernel<NI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  topk_plan_kernel<NI, true><<<1, 512, smem, st>>>(score, key, dead, T, E, k, topk_idx, topk_w, nullptr, nullptr,
+                                                   counts, offsets, slot_of_row, row_of_slot);
+  return launch_status();
+}
+
+static int launch_topk_single_plain(int E, size_t smem, cudaStream_t st, const float* score, const float* key,
+                                    const uint8_t* dead, int T, int k, int32_t* topk_idx, float* topk_w,
+                                    int32_t* counts, int32_t* offsets, int32_t* slot_of_row, int32_t* row_of_slot) {
+#define MOE_TOPK_CASE(N)                                                                                          \
+  if (E <= 32 * N)                                                                                                \
+    return launch_topk_single_plain_ni<N>(smem, st, score, key, dead, T, E, k, topk_idx, topk_w, counts, offsets, \
+                                          slot_of_row, row_of_slot);
+  MOE_TOPK_CASE(1)
+  MOE_TOPK_CASE(2)
+  MOE_TOPK_CASE(4)
+  MOE_TOPK_CASE(8)
+  MOE_TOPK_CASE(16)
+  MOE_TOPK_CASE(32)
+#undef MOE_TOPK_CASE
+  return MOE_ERR_UNSUPPORTED_SHAPE;
+}
+
 int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, const uint8_t* dead,
                  int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
                  int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done) {
@@ -496,16 +622,11 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
   if (rc) return rc;
   const int nb = ceil_div(T, kPlanBlock);
   const size_t smem = (size_t)E * 8 * 4 + (size_t)kPlanBlock * k * 2;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(topk_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-    attr_set = true;
-  }
   int32_t* cnt = ws_ptr<int32_t>(ws, L.cnt);
   int32_t* base = ws_ptr<int32_t>(ws, L.base);
   int32_t* rank = ws_ptr<int32_t>(ws, L.rank);
-  rc = launch_pdl(topk_plan_kernel, dim3(nb), dim3(512), smem, st, score, key, dead, T, E, k, topk_idx, topk_w, cnt,
-                  rank, counts, offsets, slot_of_row, row_of_slot);
+  rc = launch_topk_plan(nb, E, smem, st, score, key, dead, T, k, topk_idx, topk_w, cnt, rank, counts, offsets,
+                        slot_of_row, row_of_slot);
   if (rc || nb == 1) return rc;
   rc = launch_pdl(plan_scan_kernel, dim3(1), dim3(512), 0, st, cnt, nb, E, base, counts, offsets);
   if (rc) return rc;
@@ -623,7 +744,6 @@ extern "C" int moe_route_topk_noalloc(const moe_shape* s, const uint16_t* x, con
   // not a device address, so ask the runtime for it.
   static std::mutex mu;
   static float* scratch_of_device[64] = {};
-  static bool smem_attr_set = false;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   float* scratch = nullptr;
@@ -633,12 +753,6 @@ extern "C" int moe_route_topk_noalloc(const moe_shape* s, const uint16_t* x, con
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
       scratch_of_device[dev] = static_cast<float*>(p);
-    }
-    if (!smem_attr_set) {
-      if (cudaFuncSetAttribute(topk_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
-          cudaSuccess)
-        return MOE_ERR_CUDA;
-      smem_attr_set = true;
     }
     scratch = scratch_of_device[dev];
   }
@@ -655,7 +769,8 @@ extern "C" int moe_route_topk_noalloc(const moe_shape* s, const uint16_t* x, con
   // one plan block (T <= kPlanBlock): the kernel scans and scatters itself and never touches the
   // multi-block count/rank arrays
   const size_t smem = (size_t)E * 8 * 4 + (size_t)kPlanBlock * k * 2;
-  topk_plan_kernel<<<1, 512, smem, st>>>(score, key, dead, T, E, k, topk_idx, topk_w, nullptr, nullptr,
-                                         expert_counts, expert_offsets, slot_of_row, row_of_slot);
+  rc = launch_topk_single_plain(E, smem, st, score, key, dead, T, k, topk_idx, topk_w, expert_counts,
+                               expert_offsets, slot_of_row, row_of_slot);
+  if (rc) return rc;
   return launch_status();
 }

@@ -34,7 +34,6 @@ constexpr int kScrK = 64;            // bf16 elements of K per stage (128-byte r
 constexpr int kScrStages = 4;
 constexpr int kScrMaxE = 256;
 constexpr int kCandMax = 64;
-constexpr int kExactWarps = 8;
 constexpr uint64_t kScrWaitNs = 1000000000ull;
 
 bool router_screen_supported(const moe_shape* s) {
@@ -226,83 +225,166 @@ __global__ void __launch_bounds__(256, 1) router_screen_kernel(const __grid_cons
   if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
-// One warp per row: exact fixed-order logits of the candidates (every expert if the list
-// overflowed), sigmoid, key; the row's keys are written in full (-inf where pruned).
-__global__ void __launch_bounds__(kExactWarps * 32) router_exact_kernel(
+// Exact recompute, one warp per CTA. The warp walks its rows t = blockIdx.x, + gridDim.x, ... as
+// a stream of items: the row of x, then the Wr row of each candidate (every expert if the list
+// overflowed). Items flow through a kExactStages-slot FIFO in shared memory filled by cp.async
+// with coalesced 16-B copies; each 64-element chunk lands at a 144-B pitch so the lanes' reads of
+// chunks lane and lane + 32 fall in distinct banks. The row of x moves to registers when reached;
+// a candidate item gives each lane the fixed-order partials of its two chunks, and once per
+// kExactBatch candidates (or at the row's end) lane b folds candidate b's partials in chunk order,
+// applies the sigmoid and writes score and key. A row's keys are first written in full as -inf
+// (scores 0), so pruned experts are never selected. The row metadata (count, candidate list) is
+// loaded one row ahead of the producer so no copy waits on it.
+constexpr int kExactBatch = 8;
+constexpr int kExactStages = 4;
+constexpr int kExactPitch = 144;     // bytes per staged 64-element chunk
+constexpr int kExactVec = 16;        // 16-B vectors per lane for one 4096-element row
+
+struct ExactItem {
+  int t, j, e, cnt;                  // row, item index (-1 = x), expert, candidates in the row
+};
+
+static size_t exact_smem_bytes(int H) {
+  const int NC = H / kRouterChunk;
+  return (size_t)kExactStages * NC * kExactPitch + (size_t)kExactBatch * (NC + 1) * 4 + kExactBatch * 4 +
+         kExactStages * sizeof(ExactItem);
+}
+
+__global__ void __launch_bounds__(32, 16) router_exact_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, const float* __restrict__ bias,
     const int32_t* __restrict__ cand, const int32_t* __restrict__ ncand, int T, int H, int E,
     float* __restrict__ score, float* __restrict__ key) {
-  extern __shared__ __align__(16) uint8_t dsm_ex[];
+  extern __shared__ __align__(16) uint8_t esm[];
+  const int NC = H / kRouterChunk;
+  const int nv = NC * 8;
+  const int slot_bytes = NC * kExactPitch;
+  float* part = reinterpret_cast<float*>(esm + kExactStages * slot_bytes);   // [kExactBatch][NC + 1]
+  int* re = reinterpret_cast<int*>(part + kExactBatch * (NC + 1));
+  ExactItem* desc = reinterpret_cast<ExactItem*>(re + kExactBatch);
+  const int lane = threadIdx.x;
   pdl_trigger();
   pdl_wait();
-  const int NC = H / kRouterChunk;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // per warp: the row in padded chunks (66 bf16 per chunk), partials [32][NC + 1], results [32]x2
-  const size_t xw_bytes = align_up((size_t)NC * 66 * 2, 16);
-  const size_t per_warp = xw_bytes + (size_t)32 * (NC + 1) * 4 + 64 * 4 + 32 * 4;
-  uint8_t* wbase = dsm_ex + warp * per_warp;
-  uint16_t* xsm = reinterpret_cast<uint16_t*>(wbase);
-  float* part = reinterpret_cast<float*>(wbase + xw_bytes);
-  float* rs = part + 32 * (NC + 1);          // [32] scores of the batch
-  float* rk = rs + 32;                        // [32] keys
-  int* re = reinterpret_cast<int*>(rk + 32);  // [32] experts
-  for (int t = blockIdx.x * kExactWarps + warp; t < T; t += gridDim.x * kExactWarps) {
-    const int nc = ncand[t];
-    const int ncount = nc < 0 ? E : nc;
-    // stage the row
-    for (int i = lane; i < H / 8; i += 32) {
-      const int h = i * 8;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + h));
-      uint32_t* d = reinterpret_cast<uint32_t*>(xsm + (h / kRouterChunk) * 66 + (h % kRouterChunk));
-      d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+
+  // ---- producer cursor: row p_t, item p_j; meta of this row and (prefetched) of the next ----
+  const int stride = gridDim.x;
+  int p_t = blockIdx.x, p_j = -1;
+  int p_nc = 0, p_cl0 = 0, p_cl1 = 0;
+  int n_nc = 0, n_cl0 = 0, n_cl1 = 0;
+  auto load_meta = [&](int t, int& nc, int& cl0, int& cl1) {
+    if (t < T) {
+      nc = ncand[t];
+      cl0 = cand[(size_t)t * kCandMax + lane];
+      cl1 = cand[(size_t)t * kCandMax + 32 + lane];
     }
-    // the full key row first (pruned experts never win), then the candidates' exact values
-    for (int e = lane; e < E; e += 32) {
-      key[(size_t)t * E + e] = -INFINITY;
-      score[(size_t)t * E + e] = 0.f;
+  };
+  load_meta(p_t, p_nc, p_cl0, p_cl1);
+  load_meta(p_t + stride, n_nc, n_cl0, n_cl1);
+  int ps = 0;
+  auto produce = [&]() {
+    ExactItem it{T, 0, 0, 0};
+    if (p_t < T) {
+      const int cnt = p_nc < 0 ? E : p_nc;
+      const uint16_t* src;
+      int e = 0;
+      if (p_j < 0) {
+        src = x + (size_t)p_t * H;
+      } else {
+        const int v = __shfl_sync(0xffffffffu, p_j < 32 ? p_cl0 : p_cl1, p_j & 31);
+        e = p_nc < 0 ? p_j : v;
+        src = wr + (size_t)e * H;
+      }
+      uint8_t* dst = esm + ps * slot_bytes;
+      const uint4* g = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+      for (int r = 0; r < kExactVec; ++r) {
+        const int i = lane + 32 * r;
+        if (i < nv) cp_async_16(dst + (i >> 3) * kExactPitch + (i & 7) * 16, g + i, 16);
+      }
+      it = ExactItem{p_t, p_j, e, cnt};
+      if (++p_j == cnt) {
+        p_t += stride;
+        p_j = -1;
+        p_nc = n_nc;
+        p_cl0 = n_cl0;
+        p_cl1 = n_cl1;
+        load_meta(p_t + stride, n_nc, n_cl0, n_cl1);
+      }
+    }
+    if (lane == 0) desc[ps] = it;
+    cp_async_commit();
+    if (++ps == kExactStages) ps = 0;
+  };
+
+  for (int i = 0; i < kExactStages - 1; ++i) produce();
+  uint32_t xr[2][32];                // the row's chunks lane and lane + 32 (bf16 pairs)
+  int cs = 0, b = 0;
+  for (;;) {
+    produce();
+    cp_async_wait_group<kExactStages - 1>();
+    __syncwarp();
+    const ExactItem it = desc[cs];
+    if (it.t >= T) break;
+    const uint8_t* slot = esm + cs * slot_bytes;
+    if (it.j < 0) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = c < NC ? *reinterpret_cast<const uint4*>(slot + c * kExactPitch + i * 16)
+                                 : make_uint4(0, 0, 0, 0);
+          xr[h][4 * i] = v.x;
+          xr[h][4 * i + 1] = v.y;
+          xr[h][4 * i + 2] = v.z;
+          xr[h][4 * i + 3] = v.w;
+        }
+      }
+      for (int e = lane; e < E; e += 32) {
+        key[(size_t)it.t * E + e] = -INFINITY;
+        score[(size_t)it.t * E + e] = 0.f;
+      }
+      b = 0;
+    } else {
+      // two independent 64-FMA chains (chunks lane and lane + 32), each in element order
+      const uint8_t* w0 = slot + lane * kExactPitch;
+      const uint8_t* w1 = slot + (lane + 32) * kExactPitch;
+      const bool two = lane + 32 < NC;
+      float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 a = lane < NC ? *reinterpret_cast<const uint4*>(w0 + i * 16) : make_uint4(0, 0, 0, 0);
+        const uint4 c = two ? *reinterpret_cast<const uint4*>(w1 + i * 16) : make_uint4(0, 0, 0, 0);
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
+        const uint32_t wc[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          p0 = __fmaf_rn(bf_lo(xr[0][4 * i + q]), bf_lo(wa[q]), p0);
+          p1 = __fmaf_rn(bf_lo(xr[1][4 * i + q]), bf_lo(wc[q]), p1);
+          p0 = __fmaf_rn(bf_hi(xr[0][4 * i + q]), bf_hi(wa[q]), p0);
+          p1 = __fmaf_rn(bf_hi(xr[1][4 * i + q]), bf_hi(wc[q]), p1);
+        }
+      }
+      if (lane < NC) part[b * (NC + 1) + lane] = p0;
+      if (two) part[b * (NC + 1) + lane + 32] = p1;
+      if (lane == 0) re[b] = it.e;
+      ++b;
+      if (b == kExactBatch || it.j + 1 == it.cnt) {
+        __syncwarp();
+        if (lane < b) {
+          float acc = 0.f;
+          for (int c = 0; c < NC; ++c) acc = __fadd_rn(acc, part[lane * (NC + 1) + c]);
+          const int e = re[lane];
+          const float sc = sigmoid_cw(acc);
+          score[(size_t)it.t * E + e] = sc;
+          key[(size_t)it.t * E + e] = __fadd_rn(sc, bias[e]);
+        }
+        b = 0;
+      }
     }
     __syncwarp();
-    for (int b0 = 0; b0 < ncount; b0 += 32) {
-      const int nb = min(32, ncount - b0);
-      for (int ci = 0; ci < nb; ++ci) {
-        const int e = nc < 0 ? b0 + ci : cand[(size_t)t * kCandMax + b0 + ci];
-        for (int c = lane; c < NC; c += 32) {
-          const uint4* wp = reinterpret_cast<const uint4*>(wr + (size_t)e * H + (size_t)c * kRouterChunk);
-          const uint32_t* xp = reinterpret_cast<const uint32_t*>(xsm + c * 66);
-          float pacc = 0.f;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 wv = __ldg(wp + i);
-            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t xw = xp[i * 4 + q];
-              pacc = __fmaf_rn(bf_lo(xw), bf_lo(ww[q]), pacc);
-              pacc = __fmaf_rn(bf_hi(xw), bf_hi(ww[q]), pacc);
-            }
-          }
-          part[ci * (NC + 1) + c] = pacc;
-        }
-        if (lane == 0) re[ci] = e;
-      }
-      __syncwarp();
-      if (lane < nb) {
-        float acc = 0.f;
-        for (int c = 0; c < NC; ++c) acc = __fadd_rn(acc, part[lane * (NC + 1) + c]);
-        const int e = re[lane];
-        const float sc = sigmoid_cw(acc);
-        rs[lane] = sc;
-        rk[lane] = __fadd_rn(sc, bias[e]);
-      }
-      __syncwarp();
-      if (lane < nb) {
-        const int e = re[lane];
-        score[(size_t)t * E + e] = rs[lane];
-        key[(size_t)t * E + e] = rk[lane];
-      }
-      __syncwarp();
-    }
+    if (++cs == kExactStages) cs = 0;
   }
+  cp_async_wait_all();
 }
 
 typedef CUresult (*EncodeTiledFnR)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -368,19 +450,21 @@ int launch_router_screen(const moe_shape* s, const uint16_t* x, const uint16_t* 
   }
   rc = launch_pdl(router_screen_kernel, dim3(ceil_div(T, kScrRows)), dim3(256), (size_t)smem, st, tmx, tmw, sp);
   if (rc) return rc;
-  const int NC = H / kRouterChunk;
-  const size_t per_warp = align_up((size_t)NC * 66 * 2, 16) + (size_t)32 * (NC + 1) * 4 + 64 * 4 + 32 * 4;
-  const size_t esmem = per_warp * kExactWarps;
+  const size_t esmem = exact_smem_bytes(H);
   static size_t eattr = 0;
+  static int eper_sm = 0;
   if (eattr < esmem) {
     if (cudaFuncSetAttribute(router_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)esmem) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     eattr = esmem;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&eper_sm, router_exact_kernel, 32, esmem) != cudaSuccess ||
+        eper_sm < 1)
+      eper_sm = 1;
   }
-  const int eg = (int)std::min<long long>((T + kExactWarps - 1) / kExactWarps, (long long)num_sms() * 4);
-  return launch_pdl(router_exact_kernel, dim3(eg), dim3(kExactWarps * 32), esmem, st, x, wr, bias, cand, ncand, T, H,
-                    E, score, key);
+  const int eg = (int)std::min<long long>(T, (long long)num_sms() * eper_sm);
+  return launch_pdl(router_exact_kernel, dim3(eg), dim3(32), esmem, st, x, wr, bias, cand, ncand, T, H, E, score,
+                    key);
 }
 
 }  // namespace moe

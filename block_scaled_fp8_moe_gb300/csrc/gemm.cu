@@ -34,7 +34,10 @@
 namespace moe {
 
 #ifndef MOE_KT_WIDE
-#define MOE_KT_WIDE 2               // K-chunks per stage for token tiles > 32
+#define MOE_KT_WIDE 2               // K-chunks per stage for 128-row token tiles
+#endif
+#ifndef MOE_WIDE_BN
+#define MOE_WIDE_BN 224             // widest token tile (MMA N) of the prefill path
 #endif
 constexpr int kThreads = 256;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
@@ -68,20 +71,25 @@ struct Smem {
   // A pipeline stage holds KT consecutive K-chunks (weight tiles) of 128: small token tiles are
   // weight-streaming bound and each stage hand-off costs a fixed few hundred ns per CTA, so they
   // move 16 KB of packed weights per TMA request.
-  static constexpr int KT = (BN <= 32) ? 2 : (BN <= 64 ? 1 : MOE_KT_WIDE);
+  static constexpr int KT = (BN <= 32) ? 2 : (BN <= 64 ? 1 : (BN == 128 ? MOE_KT_WIDE : 1));
   static constexpr int kTileA = 16384;                           // one unpacked 128 x 128 FP4 tile
   static constexpr int kTileB = BN * 128;                        // BN rows x 128 FP8
   static constexpr int kStageA = KT * kTileA;
   static constexpr int kStageB = KT * kTileB;
-  static constexpr int kStageBytes = kStageA + kStageB + KT * 1024;   // + KT x (512 B A + 512 B B scales)
-  static constexpr int kStages = (BN <= 32) ? 2 : (BN <= 64 ? 3 : 6 / MOE_KT_WIDE);
+  static constexpr int kSfbChunk = 512 * ((BN + 127) / 128);     // B scale atoms of one K-chunk
+  static constexpr int kSfChunk = 512 + kSfbChunk;
+  static constexpr int kStageBytes = (int)((kStageA + kStageB + KT * kSfChunk + 1023) / 1024 * 1024);
+  static constexpr int kStages = (BN <= 32) ? 2 : (BN <= 64 ? 3 : (BN == 128 ? 6 / MOE_KT_WIDE : 4));
   static constexpr int kCtasPerSm = (BN <= 64) ? 2 : 1;
-  // TMEM: two accumulator slots of kAccStride columns, then the ring of scale blocks
-  static constexpr int kAccStride = (BN <= 64) ? 64 : 128;
+  // TMEM: two accumulator slots of kAccStride columns, then the ring of scale blocks (one slot of
+  // kSfSlot columns per K-chunk in flight: 4 for A, 4 per 128 token rows for B)
+  static constexpr int kAccStride = (BN <= 64) ? 64 : BN;
   static constexpr int kSfCol = 2 * kAccStride;
+  static constexpr int kSfSlot = 4 + 4 * ((BN + 127) / 128);
   static constexpr int kTmemCols = (BN <= 64) ? 256 : 512;
-  // wide token tiles read the activation operand with TMA (a 2D box for W2's contiguous plan rows,
-  // four-row gathers for W13's token rows) instead of cp.async
+  static_assert(kSfCol + kStages * KT * kSfSlot <= kTmemCols, "TMEM columns");
+  // wide token tiles read the activation operand with TMA (one 2D box of plan-order rows per
+  // K-chunk) instead of cp.async gathers, and size each expert's tiles to its row count
   static constexpr bool kTmaB = (BN >= 128);
   static constexpr int kTiles = kStages * kStageBytes;
   static constexpr int kXchg = 2 * 64 * 16 * 4;                 // W13 epilogue exchange (gate + up)
@@ -115,7 +123,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 }
 
 template <int BN, bool W13>
-__global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+__global__ void __launch_bounds__(kThreads, (BN <= 64) ? 2 : 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                     const __grid_constant__ CUtensorMap tmap_b,
                                                                     const GemmParams p) {
   using L = Smem<BN>;
@@ -192,16 +200,19 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
   const uint32_t tmem = *tmem_slot;
   const int total = s_cum[E];
 
-  // decode work item w -> (e, m, nt)
-  auto decode = [&](int w, int& e, int& m, int& nt, int& row0, int& nrows) {
+  // decode work item w -> (e, m, nt); tw = the expert's tile width (columns per token tile): BN
+  // for narrow tiles, else its rows spread evenly over ceil(count / BN) tiles, rounded up to 16
+  auto decode = [&](int w, int& e, int& m, int& nt, int& row0, int& nrows, int& tw) {
     e = find_expert(s_cum, E, w);
     const int cnt = s_off[e + 1] - s_off[e];
     const int ntiles = (cnt + BN - 1) / BN;
+    tw = BN;
+    if (kTmaB) tw = min(BN, ((cnt + ntiles - 1) / ntiles + 15) / 16 * 16);
     const int local = w - s_cum[e];
     m = local / ntiles;
     nt = local - m * ntiles;
-    row0 = s_off[e] + nt * BN;
-    nrows = min(BN, cnt - nt * BN);
+    row0 = s_off[e] + nt * tw;
+    nrows = min(tw, cnt - nt * tw);
   };
 
   if (warp == 0) {
@@ -212,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       bool ok = true;
       const int KC = p.KC;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-        int e, m, nt, row0, nrows;
-        decode(w, e, m, nt, row0, nrows);
+        int e, m, nt, row0, nrows, tw;
+        decode(w, e, m, nt, row0, nrows, tw);
         const int tile0 = (e * p.MT + m) * KC;
         for (int kc0 = 0; kc0 < KC; kc0 += L::KT) {
           if (!mbar_wait(&empty[stage], phase ^ 1, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_EMPTY)) {
@@ -243,27 +254,28 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
     uint32_t phase = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total; w += gridDim.x) {
-      int e, m, nt, row0, nrows;
-      decode(w, e, m, nt, row0, nrows);
+      int e, m, nt, row0, nrows, tw;
+      decode(w, e, m, nt, row0, nrows, tw);
       for (int kc0 = 0; kc0 < p.KC; kc0 += L::KT) {
         if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
         if (ok) {
           const int nv = min(L::KT, p.KC - kc0);
           uint8_t* sB0 = tiles + stage * L::kStageBytes + L::kStageA;
           uint8_t* sSFB0 = sB0 + L::kStageB + L::KT * 512;
-          // every stage moves KT boxes (the transaction count the weight producer announced);
-          // boxes past the end of K read TMA's zero fill and are never multiplied
+          // every stage moves KT boxes of BN rows (the transaction count the weight producer
+          // announced); rows past the tile and boxes past the end of K are never multiplied
           if (lane == 0)
             for (int j = 0; j < L::KT; ++j)
               tma_load_2d(sB0 + j * L::kTileB, &tmap_b, (kc0 + j) * 128, row0, &full[stage]);
           for (int j = 0; j < nv; ++j) {
             const int kc = kc0 + j;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < (BN + 31) / 32; ++i) {
               const int c = lane + 32 * i;
               const bool valid = c < nrows;
               const uint8_t* src = valid ? p.bs + (size_t)(row0 + c) * p.b_scale_pitch + kc * 4 : p.bs;
-              cp_async_4(sSFB0 + j * 512 + (c & 31) * 16 + (c >> 5) * 4, src, valid ? 4u : 0u);
+              cp_async_4(sSFB0 + j * L::kSfbChunk + (c >> 7) * 512 + (c & 31) * 16 + ((c >> 5) & 3) * 4, src,
+                         valid ? 4u : 0u);
             }
           }
           cp_async_arrive_noinc(&full[stage]);
@@ -281,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
     uint32_t phase = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total; w += gridDim.x) {
-      int e, m, nt, row0, nrows;
-      decode(w, e, m, nt, row0, nrows);
+      int e, m, nt, row0, nrows, tw;
+      decode(w, e, m, nt, row0, nrows, tw);
       named_bar_sync(2, 64);                          // previous item's table no longer in use
       for (int c = pb; c < BN; c += 64) {
         long long r = -1;
@@ -302,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
           for (int j2 = 0; j2 < nv; ++j2) {
             const int kc = kc0 + j2;
             uint8_t* sB = sB0 + j2 * L::kTileB;
-            uint8_t* sSFB = sSFB0 + j2 * 512;
+            uint8_t* sSFB = sSFB0 + j2 * L::kSfbChunk;
             for (int i = pb; i < BN * 8; i += 64) {
               const int c = i >> 3, j = i & 7;
               const long long r = s_rows[c];
@@ -331,8 +343,10 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      const uint32_t idesc_base = idesc_mxf8f6f4(5 /*E2M1*/, 0 /*E4M3*/, 128, BN, 0, 0);
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it) {
+        int e, m, nt, row0, nrows, tw;
+        decode(w, e, m, nt, row0, nrows, tw);
+        const uint32_t idesc_base = idesc_mxf8f6f4(5 /*E2M1*/, 0 /*E4M3*/, 128, tw, 0, 0);
         const int acc = (NACC == 2) ? (it & 1) : 0;
         const int use = (NACC == 2) ? (it >> 1) : it;       // how many times this slot was used before
         if (use > 0 &&
@@ -356,10 +370,12 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
           uint8_t* sSFB0 = sSFA0 + L::KT * 512;
           for (int j = 0; j < nv; ++j) {
             const int kc = kc0 + j;
-            const uint32_t tsfa = tmem + L::kSfCol + (stage * L::KT + j) * 8;
+            const uint32_t tsfa = tmem + L::kSfCol + (stage * L::KT + j) * L::kSfSlot;
             const uint32_t tsfb = tsfa + 4;
             tc_cp_32x128b_warpx4(tsfa, smem_desc(smem_u32(sSFA0 + j * 512), 16, 128, 0));
-            tc_cp_32x128b_warpx4(tsfb, smem_desc(smem_u32(sSFB0 + j * 512), 16, 128, 0));
+            // B scales: one 512-byte atom per 128 token rows, atom q at TMEM column tsfb + 4 q
+            for (int q = 0; q * 128 < tw; ++q)
+              tc_cp_32x128b_warpx4(tsfb + 4 * q, smem_desc(smem_u32(sSFB0 + j * L::kSfbChunk + q * 512), 16, 128, 0));
             const uint32_t a0 = smem_u32(sA0 + j * L::kTileA), b0 = smem_u32(sB0 + j * L::kTileB);
             const int nk = min(4, (p.K - kc * 128) / 32);
             for (int kb = 0; kb < nk; ++kb) {
@@ -389,8 +405,8 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
     int it = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total; w += gridDim.x, ++it) {
-      int e, m, nt, row0, nrows;
-      decode(w, e, m, nt, row0, nrows);
+      int e, m, nt, row0, nrows, tw;
+      decode(w, e, m, nt, row0, nrows, tw);
       const int acc = (NACC == 2) ? (it & 1) : 0;
       const int use = (NACC == 2) ? (it >> 1) : it;
       // W2: the slot and routing weight of every column of this tile, one coalesced load per lane
@@ -409,71 +425,92 @@ __global__ void __launch_bounds__(kThreads, 2) grouped_gemm_kernel(const __grid_
       if (ok) ok = warp_wait(&acc_full[acc], use & 1, abort_flag, p.status, DEV_TIMEOUT_ACCUM);
       tc_fence_after();
       const uint32_t d_tmem = tmem + (uint32_t)(acc * L::kAccStride);
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t r[16];
+      // TMEM is read kGrp 16-column chunks per round trip (one wait for several loads)
+      constexpr int kGrp = W13 ? 2 : 4;
+      for (int cg = 0; cg < tw; cg += 16 * kGrp) {
+        uint32_t rg[kGrp][16];
         if (ok) {
-          tmem_ld16(d_tmem + lane_base + c0, r);
+#pragma unroll
+          for (int h = 0; h < kGrp; ++h)
+            if (cg + 16 * h < tw) tmem_ld16(d_tmem + lane_base + cg + 16 * h, rg[h]);
           tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < kGrp; ++h) reg_fence16(rg[h]);
         }
-        if constexpr (W13) {
-          // q 0,1 hold gate features 64m + 32q + lane, q 2,3 the matching up features. The chunk
-          // goes to shared memory as [column][feature]; then thread t owns column t / 8 and the
-          // eight features 8 (t % 8) .. +7: SwiGLU, a four-thread amax per 32-block, and one
-          // 8-byte store of codes.
-          float* gs = xchg;                  // [16][64] gate
-          float* us = xchg + 16 * 64;        // [16][64] up
-          if (ok) {
-            float* dst = (q < 2) ? gs : us;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) dst[c * 64 + 32 * (q & 1) + lane] = __uint_as_float(r[c]);
-          }
-          named_bar_sync(1, 128);
-          if (ok) {
-            const int t = threadIdx.x - 128;
-            const int cc = t >> 3, f0 = (t & 7) * 8;
-            const int col = c0 + cc;
-            const float4 g0 = *reinterpret_cast<const float4*>(gs + cc * 64 + f0);
-            const float4 g1 = *reinterpret_cast<const float4*>(gs + cc * 64 + f0 + 4);
-            const float4 u0 = *reinterpret_cast<const float4*>(us + cc * 64 + f0);
-            const float4 u1 = *reinterpret_cast<const float4*>(us + cc * 64 + f0 + 4);
-            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-            const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-            float a[8];
-            float am = 0.f;
+        for (int h = 0; h < kGrp; ++h) {
+          const int c0 = cg + 16 * h;
+          if (c0 >= tw) break;
+          const uint32_t(&r)[16] = rg[h];
+          if constexpr (W13) {
+            // q 0,1 hold gate features 64m + 32q + lane, q 2,3 the matching up features. The chunk
+            // goes to shared memory as [column][feature]; then thread t owns column t / 8 and the
+            // eight features 8 (t % 8) .. +7: SwiGLU, a four-thread amax per 32-block, and one
+            // 8-byte store of codes.
+            float* gs = xchg;                  // [16][64] gate
+            float* us = xchg + 16 * 64;        // [16][64] up
+            if (ok) {
+              float* dst = (q < 2) ? gs : us;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              a[i] = silu_mul(gv[i], uv[i]);
-              am = fmaxf(am, fabsf(a[i]));
+              for (int c = 0; c < 16; ++c) dst[c * 64 + 32 * (q & 1) + lane] = __uint_as_float(r[c]);
             }
-            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-            const int se = e4m3_scale_exp(am);
-            const float sc = __uint_as_float((uint32_t)(127 - se) << 23);
-            const uint32_t lo = e4m3x2(a[0] * sc, a[1] * sc) | (e4m3x2(a[2] * sc, a[3] * sc) << 16);
-            const uint32_t hi = e4m3x2(a[4] * sc, a[5] * sc) | (e4m3x2(a[6] * sc, a[7] * sc) << 16);
-            if (col < nrows) {
-              const size_t prow = (size_t)(row0 + col);
-              const int feat = 64 * m + f0;
-              *reinterpret_cast<uint2*>(p.hq + prow * p.I + feat) = make_uint2(lo, hi);
-              if ((t & 3) == 0) p.hs[prow * p.hs_pitch + (feat >> 5)] = (uint8_t)(se + 127);
-              if (p.dbg) {
-                float4* d = reinterpret_cast<float4*>(p.dbg + prow * p.I + feat);
-                d[0] = make_float4(a[0], a[1], a[2], a[3]);
-                d[1] = make_float4(a[4], a[5], a[6], a[7]);
+            named_bar_sync(1, 128);
+            if (ok) {
+              const int t = threadIdx.x - 128;
+              const int cc = t >> 3, f0 = (t & 7) * 8;
+              const int col = c0 + cc;
+              const float4 g0 = *reinterpret_cast<const float4*>(gs + cc * 64 + f0);
+              const float4 g1 = *reinterpret_cast<const float4*>(gs + cc * 64 + f0 + 4);
+              const float4 u0 = *reinterpret_cast<const float4*>(us + cc * 64 + f0);
+              const float4 u1 = *reinterpret_cast<const float4*>(us + cc * 64 + f0 + 4);
+              const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+              const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+              float a[8];
+              float am = 0.f;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                a[i] = silu_mul(gv[i], uv[i]);
+                am = fmaxf(am, fabsf(a[i]));
+              }
+              am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+              am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+              const int se = e4m3_scale_exp(am);
+              const float sc = __uint_as_float((uint32_t)(127 - se) << 23);
+              const uint32_t lo = e4m3x2(a[0] * sc, a[1] * sc) | (e4m3x2(a[2] * sc, a[3] * sc) << 16);
+              const uint32_t hi = e4m3x2(a[4] * sc, a[5] * sc) | (e4m3x2(a[6] * sc, a[7] * sc) << 16);
+              if (col < nrows) {
+                const size_t prow = (size_t)(row0 + col);
+                const int feat = 64 * m + f0;
+                *reinterpret_cast<uint2*>(p.hq + prow * p.I + feat) = make_uint2(lo, hi);
+                if ((t & 3) == 0) p.hs[prow * p.hs_pitch + (feat >> 5)] = (uint8_t)(se + 127);
+                if (p.dbg) {
+                  float4* d = reinterpret_cast<float4*>(p.dbg + prow * p.I + feat);
+                  d[0] = make_float4(a[0], a[1], a[2], a[3]);
+                  d[1] = make_float4(a[4], a[5], a[6], a[7]);
+                }
               }
             }
-          }
-          named_bar_sync(1, 128);
-        } else {
-          if (ok) {
-            const int feat = 128 * m + 32 * q + lane;
+            named_bar_sync(1, 128);
+          } else {
+            if (ok) {
+              const int feat = 128 * m + 32 * q + lane;
+              // this chunk's 16 columns lie in one 32-column group (c0 is a multiple of 16)
+              int g_slot = 0;
+              float g_wgt = 0.f;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int col = c0 + c;
-              // slot and routing weight of column col, loaded once per tile by lane col % 32
-              const int slot = __shfl_sync(0xffffffffu, w2_slot[col >> 5], col & 31);
-              const float wgt = __shfl_sync(0xffffffffu, w2_wgt[col >> 5], col & 31);
-              if (col < nrows) p.y[(size_t)slot * p.H + feat] = __fmul_rn(wgt, __uint_as_float(r[c]));
+              for (int i = 0; i < (BN + 31) / 32; ++i)
+                if (i == (c0 >> 5)) {
+                  g_slot = w2_slot[i];
+                  g_wgt = w2_wgt[i];
+                }
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const int col = c0 + c;
+                // slot and routing weight of column col, loaded once per tile by lane col % 32
+                const int slot = __shfl_sync(0xffffffffu, g_slot, col & 31);
+                const float wgt = __shfl_sync(0xffffffffu, g_wgt, col & 31);
+                if (col < nrows) p.y[(size_t)slot * p.H + feat] = __fmul_rn(wgt, __uint_as_float(r[c]));
+              }
             }
           }
         }
@@ -544,12 +581,15 @@ static int make_act_tmap(CUtensorMap* m, const uint8_t* base, int row_bytes, lon
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Token-tile width from the mean rows per expert. Wide tiles (MMA N up to MOE_WIDE_BN) are sized
+// per expert inside the kernel: an N = 128 block-scaled MMA with its scale copies occupies the
+// tensor core about as long as an N = 256 one, so fewer, wider tiles raise the math rate.
 static int pick_bn(const moe_shape* s) {
   const double avg = (double)s->T * s->k / s->E;
   if (avg <= 16) return 16;
   if (avg <= 32) return 32;
   if (avg <= 64) return 64;
-  return 128;
+  return MOE_WIDE_BN;
 }
 
 template <int BN, bool W13>
@@ -572,24 +612,28 @@ static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const G
 template <bool W13>
 static int launch_gemm(const moe_shape* s, const uint8_t* codes, const GemmParams& gp, cudaStream_t st) {
   const long long slots = (long long)s->T * s->k;
-  const int bn = pick_bn(s);
+  int bn = pick_bn(s);
+  // a down projection with a short K (fewer than 8 chunks) is bound by its epilogue's per-slot
+  // stores, not by the MMA rate: it keeps 128-row token tiles
+  if (!W13 && bn > 128 && gp.KC < 8) bn = 128;
   CUtensorMap tm;
-  const int box_tiles = (bn <= 32) ? Smem<16>::KT : (bn <= 64 ? Smem<64>::KT : Smem<128>::KT);
+  const int box_tiles = (bn <= 32) ? Smem<16>::KT : (bn <= 64 ? Smem<64>::KT : (bn == 128 ? Smem<128>::KT : Smem<MOE_WIDE_BN>::KT));
   int rc0 = make_weight_tmap(&tm, codes, (long long)s->E * gp.MT * gp.KC, box_tiles);
   if (rc0) return rc0;
   // activation operand of the wide token tile as a TMA tensor: [T*k plan rows, K] bytes, boxes of
-  // 128 plan rows (W13: the plan-order copy of xq; W2: hq)
+  // bn plan rows (W13: the plan-order copy of xq; W2: hq)
   CUtensorMap tmb = tm;
   const long long max_items = (long long)gp.MT * ((slots + bn - 1) / bn + std::min<long long>(s->E, slots));
-  if (bn == 128) {
-    const int rc = make_act_tmap(&tmb, gp.bq, gp.b_row_bytes, slots, 128);
+  if (bn >= 128) {
+    const int rc = make_act_tmap(&tmb, gp.bq, gp.b_row_bytes, slots, bn);
     if (rc) return rc;
   }
   switch (bn) {
     case 16: return launch_gemm_bn<16, W13>(tm, tmb, gp, max_items, st);
     case 32: return launch_gemm_bn<32, W13>(tm, tmb, gp, max_items, st);
     case 64: return launch_gemm_bn<64, W13>(tm, tmb, gp, max_items, st);
-    default: return launch_gemm_bn<128, W13>(tm, tmb, gp, max_items, st);
+    case 128: return launch_gemm_bn<128, W13>(tm, tmb, gp, max_items, st);
+    default: return launch_gemm_bn<MOE_WIDE_BN, W13>(tm, tmb, gp, max_items, st);
   }
 }
 
@@ -625,7 +669,7 @@ int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const u
   GemmParams gp{};
   gp.bq = xq;
   gp.bs = xs;
-  if (pick_bn(s) == 128) {
+  if (pick_bn(s) >= 128) {
     // wide tiles read the token operand in plan order with TMA boxes: gather it once
     const long long n = (long long)s->T * s->k * (s->H / 16 + s->H / 128);
     const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);

@@ -227,45 +227,71 @@ __global__ void __launch_bounds__(256, 1) router_screen_kernel(const __grid_cons
 
 // Exact recompute, one warp per CTA. The warp walks its rows t = blockIdx.x, + gridDim.x, ... as
 // a stream of items: the row of x, then the Wr row of each candidate (every expert if the list
-// overflowed). Items flow through a kExactStages-slot FIFO in shared memory filled by cp.async
-// with coalesced 16-B copies; each 64-element chunk lands at a 144-B pitch so the lanes' reads of
-// chunks lane and lane + 32 fall in distinct banks. The row of x moves to registers when reached;
-// a candidate item gives each lane the fixed-order partials of its two chunks, and once per
-// kExactBatch candidates (or at the row's end) lane b folds candidate b's partials in chunk order,
-// applies the sigmoid and writes score and key. A row's keys are first written in full as -inf
-// (scores 0), so pruned experts are never selected. The row metadata (count, candidate list) is
-// loaded one row ahead of the producer so no copy waits on it.
+// overflowed). Items flow through a kExactStages-slot FIFO in shared memory, one TMA box per item
+// (H/64 chunk rows of 128 bytes, 128-byte swizzle: the 16-byte unit j of chunk c sits at unit
+// j ^ (c % 8), so the lanes' reads of chunks lane and lane + 32 fall in distinct banks). The row of
+// x moves to registers when reached; a candidate item gives each lane the fixed-order partials of
+// its two chunks (fp32 fused multiply-add of bf16 operands: one rounding per step, the same as
+// widening first), and once per kExactBatch candidates (or at the row's end) lane b folds
+// candidate b's partials in chunk order, applies the sigmoid and writes score and key. A row's keys
+// are first written in full as -inf (scores 0), so pruned experts are never selected. The row
+// metadata (count, candidate list) is loaded one row ahead of the producer. Waits are bounded; on
+// expiry the kernel records DEV_TIMEOUT_FULL and stops.
 constexpr int kExactBatch = 8;
 constexpr int kExactStages = 4;
-constexpr int kExactPitch = 144;     // bytes per staged 64-element chunk
-constexpr int kExactVec = 16;        // 16-B vectors per lane for one 4096-element row
 
 struct ExactItem {
   int t, j, e, cnt;                  // row, item index (-1 = x), expert, candidates in the row
 };
 
+// Slots start on 1024-byte boundaries: the 128-byte swizzle pattern is a function of the shared
+// address, and the reads below assume it restarts at every slot.
+__host__ __device__ inline int exact_slot_bytes(int NC) { return (NC * 128 + 1023) / 1024 * 1024; }
+
 static size_t exact_smem_bytes(int H) {
   const int NC = H / kRouterChunk;
-  return (size_t)kExactStages * NC * kExactPitch + (size_t)kExactBatch * (NC + 1) * 4 + kExactBatch * 4 +
-         kExactStages * sizeof(ExactItem);
+  return 1024 + (size_t)kExactStages * exact_slot_bytes(NC) + (size_t)kExactBatch * (NC + 1) * 4 + kExactBatch * 4 +
+         kExactStages * (sizeof(ExactItem) + 8) + 16;
+}
+
+// acc <- fma(lo(x), lo(w), acc), then the same for the high halves (elements 2i, 2i + 1)
+__device__ __forceinline__ float fma2_bf16(uint32_t x, uint32_t w, float acc) {
+  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+      "mov.b32 {xl, xh}, %1;\n\t"
+      "mov.b32 {wl, wh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, xl, wl, %0;\n\t"
+      "fma.rn.f32.bf16 %0, xh, wh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(x), "r"(w));
+  return acc;
 }
 
 __global__ void __launch_bounds__(32, 16) router_exact_kernel(
-    const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, const float* __restrict__ bias,
+    const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw, const float* __restrict__ bias,
     const int32_t* __restrict__ cand, const int32_t* __restrict__ ncand, int T, int H, int E,
-    float* __restrict__ score, float* __restrict__ key) {
-  extern __shared__ __align__(16) uint8_t esm[];
+    float* __restrict__ score, float* __restrict__ key, uint32_t* __restrict__ status) {
+  extern __shared__ uint8_t esm_raw[];
+  uint8_t* esm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(esm_raw) + 1023) & ~uintptr_t(1023));
   const int NC = H / kRouterChunk;
-  const int nv = NC * 8;
-  const int slot_bytes = NC * kExactPitch;
+  const int slot_bytes = exact_slot_bytes(NC);
   float* part = reinterpret_cast<float*>(esm + kExactStages * slot_bytes);   // [kExactBatch][NC + 1]
   int* re = reinterpret_cast<int*>(part + kExactBatch * (NC + 1));
   ExactItem* desc = reinterpret_cast<ExactItem*>(re + kExactBatch);
+  uint64_t* full = reinterpret_cast<uint64_t*>(desc + kExactStages);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(full + kExactStages);
   const int lane = threadIdx.x;
+  if (lane == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < kExactStages; ++i) mbar_init(&full[i], 1);
+    mbar_fence_init();
+    prefetch_tmap(&tmx);
+    prefetch_tmap(&tmw);
+  }
+  __syncwarp();
   pdl_trigger();
   pdl_wait();
 
-  // ---- producer cursor: row p_t, item p_j; meta of this row and (prefetched) of the next ----
+  // ---- producer cursor (lane 0 issues): row p_t, item p_j; meta of this row and the next ----
   const int stride = gridDim.x;
   int p_t = blockIdx.x, p_j = -1;
   int p_nc = 0, p_cl0 = 0, p_cl1 = 0;
@@ -284,21 +310,16 @@ __global__ void __launch_bounds__(32, 16) router_exact_kernel(
     ExactItem it{T, 0, 0, 0};
     if (p_t < T) {
       const int cnt = p_nc < 0 ? E : p_nc;
-      const uint16_t* src;
       int e = 0;
-      if (p_j < 0) {
-        src = x + (size_t)p_t * H;
-      } else {
+      if (p_j >= 0) {
         const int v = __shfl_sync(0xffffffffu, p_j < 32 ? p_cl0 : p_cl1, p_j & 31);
         e = p_nc < 0 ? p_j : v;
-        src = wr + (size_t)e * H;
       }
-      uint8_t* dst = esm + ps * slot_bytes;
-      const uint4* g = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-      for (int r = 0; r < kExactVec; ++r) {
-        const int i = lane + 32 * r;
-        if (i < nv) cp_async_16(dst + (i >> 3) * kExactPitch + (i & 7) * 16, g + i, 16);
+      if (lane == 0) {
+        fence_async_smem();          // this slot's generic reads precede the copy that refills it
+        mbar_arrive_expect_tx(&full[ps], (uint32_t)(NC * 128));
+        if (p_j < 0) tma_load_2d(esm + ps * slot_bytes, &tmx, 0, p_t * NC, &full[ps]);
+        else tma_load_2d(esm + ps * slot_bytes, &tmw, 0, e * NC, &full[ps]);
       }
       it = ExactItem{p_t, p_j, e, cnt};
       if (++p_j == cnt) {
@@ -311,19 +332,22 @@ __global__ void __launch_bounds__(32, 16) router_exact_kernel(
       }
     }
     if (lane == 0) desc[ps] = it;
-    cp_async_commit();
     if (++ps == kExactStages) ps = 0;
   };
 
   for (int i = 0; i < kExactStages - 1; ++i) produce();
   uint32_t xr[2][32];                // the row's chunks lane and lane + 32 (bf16 pairs)
   int cs = 0, b = 0;
+  uint32_t phase = 0;
+  const int sw = (lane & 7) * 16;    // swizzle of chunks lane and lane + 32
   for (;;) {
     produce();
-    cp_async_wait_group<kExactStages - 1>();
     __syncwarp();
     const ExactItem it = desc[cs];
     if (it.t >= T) break;
+    uint32_t okw = 1;
+    if (lane == 0) okw = mbar_wait(&full[cs], phase, kScrWaitNs, abort_flag, status, DEV_TIMEOUT_FULL) ? 1u : 0u;
+    if (!__shfl_sync(0xffffffffu, okw, 0)) break;
     const uint8_t* slot = esm + cs * slot_bytes;
     if (it.j < 0) {
 #pragma unroll
@@ -331,7 +355,7 @@ __global__ void __launch_bounds__(32, 16) router_exact_kernel(
         const int c = lane + 32 * h;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint4 v = c < NC ? *reinterpret_cast<const uint4*>(slot + c * kExactPitch + i * 16)
+          const uint4 v = c < NC ? *reinterpret_cast<const uint4*>(slot + c * 128 + ((i * 16) ^ sw))
                                  : make_uint4(0, 0, 0, 0);
           xr[h][4 * i] = v.x;
           xr[h][4 * i + 1] = v.y;
@@ -345,26 +369,25 @@ __global__ void __launch_bounds__(32, 16) router_exact_kernel(
       }
       b = 0;
     } else {
-      // two independent 64-FMA chains (chunks lane and lane + 32), each in element order
-      const uint8_t* w0 = slot + lane * kExactPitch;
-      const uint8_t* w1 = slot + (lane + 32) * kExactPitch;
-      const bool two = lane + 32 < NC;
+      // two independent 64-step chains (chunks lane and lane + 32), each in element order
+      const uint8_t* w0 = slot + lane * 128;
+      const uint8_t* w1 = slot + (lane + 32) * 128;
+      const bool one = lane < NC, two = lane + 32 < NC;
       float p0 = 0.f, p1 = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint4 a = lane < NC ? *reinterpret_cast<const uint4*>(w0 + i * 16) : make_uint4(0, 0, 0, 0);
-        const uint4 c = two ? *reinterpret_cast<const uint4*>(w1 + i * 16) : make_uint4(0, 0, 0, 0);
-        const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
-        const uint32_t wc[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          p0 = __fmaf_rn(bf_lo(xr[0][4 * i + q]), bf_lo(wa[q]), p0);
-          p1 = __fmaf_rn(bf_lo(xr[1][4 * i + q]), bf_lo(wc[q]), p1);
-          p0 = __fmaf_rn(bf_hi(xr[0][4 * i + q]), bf_hi(wa[q]), p0);
-          p1 = __fmaf_rn(bf_hi(xr[1][4 * i + q]), bf_hi(wc[q]), p1);
-        }
+        const uint4 a = one ? *reinterpret_cast<const uint4*>(w0 + ((i * 16) ^ sw)) : make_uint4(0, 0, 0, 0);
+        const uint4 c = two ? *reinterpret_cast<const uint4*>(w1 + ((i * 16) ^ sw)) : make_uint4(0, 0, 0, 0);
+        p0 = fma2_bf16(xr[0][4 * i], a.x, p0);
+        p1 = fma2_bf16(xr[1][4 * i], c.x, p1);
+        p0 = fma2_bf16(xr[0][4 * i + 1], a.y, p0);
+        p1 = fma2_bf16(xr[1][4 * i + 1], c.y, p1);
+        p0 = fma2_bf16(xr[0][4 * i + 2], a.z, p0);
+        p1 = fma2_bf16(xr[1][4 * i + 2], c.z, p1);
+        p0 = fma2_bf16(xr[0][4 * i + 3], a.w, p0);
+        p1 = fma2_bf16(xr[1][4 * i + 3], c.w, p1);
       }
-      if (lane < NC) part[b * (NC + 1) + lane] = p0;
+      if (one) part[b * (NC + 1) + lane] = p0;
       if (two) part[b * (NC + 1) + lane + 32] = p1;
       if (lane == 0) re[b] = it.e;
       ++b;
@@ -382,9 +405,17 @@ __global__ void __launch_bounds__(32, 16) router_exact_kernel(
       }
     }
     __syncwarp();
-    if (++cs == kExactStages) cs = 0;
+    if (++cs == kExactStages) {
+      cs = 0;
+      phase ^= 1;
+    }
   }
-  cp_async_wait_all();
+  if (*abort_flag) {
+    // copies still in flight land before the CTA's shared memory goes away
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000) {
+    }
+  }
 }
 
 typedef CUresult (*EncodeTiledFnR)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -450,6 +481,12 @@ int launch_router_screen(const moe_shape* s, const uint16_t* x, const uint16_t* 
   }
   rc = launch_pdl(router_screen_kernel, dim3(ceil_div(T, kScrRows)), dim3(256), (size_t)smem, st, tmx, tmw, sp);
   if (rc) return rc;
+  CUtensorMap tex, tew;
+  const int NC = H / kRouterChunk;
+  rc = make_bf16_tmap(&tex, x, kRouterChunk, T * NC, NC);
+  if (rc) return rc;
+  rc = make_bf16_tmap(&tew, wr, kRouterChunk, E * NC, NC);
+  if (rc) return rc;
   const size_t esmem = exact_smem_bytes(H);
   static size_t eattr = 0;
   static int eper_sm = 0;
@@ -463,8 +500,8 @@ int launch_router_screen(const moe_shape* s, const uint16_t* x, const uint16_t* 
       eper_sm = 1;
   }
   const int eg = (int)std::min<long long>(T, (long long)num_sms() * eper_sm);
-  return launch_pdl(router_exact_kernel, dim3(eg), dim3(32), esmem, st, x, wr, bias, cand, ncand, T, H, E, score,
-                    key);
+  return launch_pdl(router_exact_kernel, dim3(eg), dim3(32), esmem, st, tex, tew, bias, cand, ncand, T, H, E, score,
+                    key, sp.status);
 }
 
 }  // namespace moe

@@ -38,11 +38,13 @@ extern "C" int moe_w13_swiglu_grouped(const moe_shape* s, const uint8_t* xq, con
   if (rc) return rc;
   if (s->T == 0) return MOE_OK;
   if (!xq || !xs || !w13 || !w13_s || !expert_offsets || !slot_of_row || !hq || !hs) return MOE_ERR_INVALID_ARG;
-  if (!aligned(xq, 16) || !aligned(xs, 4) || !aligned(w13, 32) || !aligned(w13_s, 16)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(xq, 16) || !aligned(xs, 4) || !aligned(w13, 32) || !aligned(w13_s, 16) || !aligned(hq, 16) ||
+      !aligned(swiglu_debug, 16))
+    return MOE_ERR_INVALID_ARG;
   const Workspace L = workspace_layout(s);
   return launch_w13(s, xq, xs, w13, w13_s, expert_offsets, slot_of_row, hq, hs,
                     (s->flags & 1) ? swiglu_debug : nullptr, ws_ptr<uint32_t>(ws, L.status),
-                    ws_ptr<uint8_t>(ws, L.xqp), ws_ptr<uint8_t>(ws, L.xsp), static_cast<cudaStream_t>(stream));
+                    ws_ptr<uint8_t>(ws, L.xqp), ws_ptr<uint8_t>(ws, L.xsp), false, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int moe_w2_combine_grouped(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2,
@@ -82,6 +84,9 @@ extern "C" int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t
   const Workspace L = workspace_layout(s);
   moe_intermediates im{};
   if (inter) im = *inter;
+  if (!aligned(im.xq, 16) || !aligned(im.xs, 4) || !aligned(im.hq, 16) || !aligned(im.hs, 4) ||
+      !aligned(im.swiglu, 16) || !aligned(im.topk_idx, 4) || !aligned(im.topk_w, 4))
+    return MOE_ERR_INVALID_ARG;
   auto pick = [&](auto* user, size_t off) {
     using Tp = std::remove_pointer_t<decltype(user)>;
     return user ? user : ws_ptr<Tp>(ws, off);
@@ -104,12 +109,21 @@ extern "C" int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t
   rc = launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, ws, st,
                     xq, xs, &quant_done);
   if (rc) return rc;
-  if (!quant_done) {
+  uint8_t* xqp = ws_ptr<uint8_t>(ws, L.xqp);
+  uint8_t* xsp = ws_ptr<uint8_t>(ws, L.xsp);
+  // wide-tile W13 reads the activations in plan order: quantise straight into it (token-order
+  // codes are written too only when the caller asked for them)
+  const bool plan_rows = !quant_done && w13_wants_plan_rows(s);
+  if (plan_rows) {
+    const bool token_order = im.xq || im.xs;
+    rc = launch_quant_mxfp8_plan(s->T, s->H, s->k, x, token_order ? xq : nullptr, token_order ? xs : nullptr,
+                                 row_of_slot, xqp, xsp, st);
+    if (rc) return rc;
+  } else if (!quant_done) {
     rc = launch_quant_mxfp8(s->T, s->H, x, xq, xs, st);
     if (rc) return rc;
   }
-  rc = launch_w13(s, xq, xs, w13, w13_s, offsets, slot_of_row, hq, hs, im.swiglu, status, ws_ptr<uint8_t>(ws, L.xqp),
-                  ws_ptr<uint8_t>(ws, L.xsp), st);
+  rc = launch_w13(s, xq, xs, w13, w13_s, offsets, slot_of_row, hq, hs, im.swiglu, status, xqp, xsp, plan_rows, st);
   if (rc) return rc;
   rc = launch_w2(s, hq, hs, w2, w2_s, topk_w, offsets, slot_of_row, y, status, st);
   if (rc) return rc;

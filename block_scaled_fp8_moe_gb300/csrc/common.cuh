@@ -126,6 +126,11 @@ inline int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
 
 // Internal launchers (defined in the .cu files), all asynchronous on `st`.
 int launch_quant_mxfp8(int rows, int cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st);
+// Quantises x and writes codes/scales to plan rows row_of_slot[t k + j] of qp/sp (q/s nullable).
+int launch_quant_mxfp8_plan(int rows, int cols, int k, const uint16_t* x, uint8_t* q, uint8_t* s,
+                            const int32_t* row_of_slot, uint8_t* qp, uint8_t* sp, cudaStream_t st);
+// True when W13 runs wide token tiles, whose activation operand is read in plan order.
+bool w13_wants_plan_rows(const moe_shape* s);
 // When xq/xs are given and the small-batch router runs, it also writes the MXFP8 quantisation of x
 // and sets *quant_done.
 int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, const uint8_t* dead,
@@ -133,7 +138,7 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
                  int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done);
 int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
                const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
-               uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, cudaStream_t st);
+               uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, bool plan_rows_ready, cudaStream_t st);
 int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2s,
               const float* topk_w, const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
               cudaStream_t st);

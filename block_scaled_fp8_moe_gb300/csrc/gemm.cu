@@ -11,16 +11,18 @@
 // order for every output element: the K loop is identical, never split, and a token's column
 // position does not change the arithmetic of its column.
 //
-// Roles (256 threads):
+// Roles (256 threads; 384 for wide token tiles):
 //   warp 0      TMA producer: packed weight tile (FP4, unpacked to 8-bit containers by the TMA)
 //               and its 512-byte scale block (bulk copy); one mbarrier transaction per stage.
-//   warps 1, 3  gather producers: cp.async of the BN activation rows (128 B each, 128B-swizzled
-//               in shared memory) and their scale bytes; arrive on the same stage mbarrier.
-//   warp 2      TMEM owner and MMA issuer: tcgen05.cp of both scale blocks to TMEM, four
-//               K=32 MMAs per stage, tcgen05.commit releases the stage only after the MMAs
-//               (and copies) that read it are complete.
-//   warps 4-7   epilogue: tcgen05.ld of the fp32 accumulator, SwiGLU + MXFP8 requant (W13) or
-//               routing-weight scaling into the per-slot buffer (W2).
+//   warps 1, 3  token-operand producers: cp.async gathers of the BN activation rows (128 B each,
+//               128B-swizzled in shared memory) and their scale bytes for narrow tiles; for wide
+//               tiles warp 1 loads one TMA box of plan-order rows per K-chunk. Both arrive on the
+//               same stage mbarrier.
+//   warp 2      TMEM owner and MMA issuer: tcgen05.cp of the scale blocks to TMEM, four K=32
+//               MMAs per K-chunk, tcgen05.commit releases the stage only after the MMAs (and
+//               copies) that read it are complete.
+//   warps 4-7   epilogue (and 8-11 for wide tiles): tcgen05.ld of the fp32 accumulator, SwiGLU +
+//               MXFP8 requant (W13) or routing-weight scaling into the per-slot buffer (W2).
 // Work items (expert, weight panel, token tile) are walked with the token tile fastest, so CTAs
 // running at the same time share one weight panel through L2.
 #include <cuda.h>
@@ -39,7 +41,13 @@ namespace moe {
 #ifndef MOE_WIDE_BN
 #define MOE_WIDE_BN 224             // widest token tile (MMA N) of the prefill path
 #endif
-constexpr int kThreads = 256;
+// 4 producer/MMA warps + 4 epilogue warps; wide token tiles take 8 epilogue warps (two per TMEM
+// lane quarter, splitting the tile's columns), since their epilogue, not the MMA, sets the pace.
+template <int BN>
+struct Threads {
+  static constexpr int kEpiWarps = (BN >= 128) ? 8 : 4;
+  static constexpr int kCount = 128 + 32 * kEpiWarps;
+};
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
 
 struct GemmParams {
@@ -92,7 +100,7 @@ struct Smem {
   // K-chunk) instead of cp.async gathers, and size each expert's tiles to its row count
   static constexpr bool kTmaB = (BN >= 128);
   static constexpr int kTiles = kStages * kStageBytes;
-  static constexpr int kXchg = 2 * 64 * 16 * 4;                 // W13 epilogue exchange (gate + up)
+  static constexpr int kXchg = 2 * 64 * 16 * 4 * (Threads<BN>::kEpiWarps / 4);   // W13 epilogue exchange
   static constexpr int kMisc = 1024;                            // barriers, flags
   static constexpr int kRows = 128 * 8;                         // gather row table
   static constexpr int kFixed = 1024 + kTiles + kXchg + kMisc + kRows;
@@ -123,7 +131,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 }
 
 template <int BN, bool W13>
-__global__ void __launch_bounds__(kThreads, (BN <= 64) ? 2 : 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+__global__ void __launch_bounds__(Threads<BN>::kCount, (BN <= 64) ? 2 : 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                     const __grid_constant__ CUtensorMap tmap_b,
                                                                     const GemmParams p) {
   using L = Smem<BN>;
@@ -159,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, (BN <= 64) ? 2 : 1) grouped_gemm_ker
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);
+      mbar_init(&acc_empty[a], Threads<BN>::kEpiWarps);
     }
     mbar_init(drain, 1);
     mbar_fence_init();
@@ -173,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, (BN <= 64) ? 2 : 1) grouped_gemm_ker
     if (kTmaB) prefetch_tmap(&tmap_b);
   }
   pdl_wait();                                    // everything below may read upstream results
-  for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets[i];
+  for (int i = threadIdx.x; i <= E; i += Threads<BN>::kCount) s_off[i] = p.offsets[i];
   __syncthreads();
   if (warp == 0) {
     // tile starts: warp-parallel prefix sum of ceil(count_e / BN), times MT
@@ -397,10 +405,14 @@ __global__ void __launch_bounds__(kThreads, (BN <= 64) ? 2 : 1) grouped_gemm_ker
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ===================== epilogue (warps 4..7 -> TMEM lanes 32 (warp - 4)) =====================
-    // As above, an expired wait turns the remaining iterations into no-ops that still meet at the
-    // named barriers.
-    const int q = warp - 4;
+    // ===================== epilogue (warp w -> TMEM lanes 32 (w % 4)) =====================
+    // With 8 epilogue warps, warps 4-7 take the even column groups of a tile and warps 8-11 the
+    // odd ones, each set with its own exchange buffer and named barrier. As above, an expired wait
+    // turns the remaining iterations into no-ops that still meet at the named barriers.
+    constexpr int kHalves = Threads<BN>::kEpiWarps / 4;
+    const int q = (warp - 4) & 3;
+    const int half = (warp - 4) >> 2;
+    const uint32_t bar_id = 1 + 2 * half;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     int it = 0;
     bool ok = true;
@@ -427,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, (BN <= 64) ? 2 : 1) grouped_gemm_ker
       const uint32_t d_tmem = tmem + (uint32_t)(acc * L::kAccStride);
       // TMEM is read kGrp 16-column chunks per round trip (one wait for several loads)
       constexpr int kGrp = W13 ? 2 : 4;
-      for (int cg = 0; cg < tw; cg += 16 * kGrp) {
+      for (int cg = 16 * kGrp * half; cg < tw; cg += 16 * kGrp * kHalves) {
         uint32_t rg[kGrp][16];
         if (ok) {
 #pragma unroll
@@ -447,16 +459,16 @@ __global__ void __launch_bounds__(kThreads, (BN <= 64) ? 2 : 1) grouped_gemm_ker
             // goes to shared memory as [column][feature]; then thread t owns column t / 8 and the
             // eight features 8 (t % 8) .. +7: SwiGLU, a four-thread amax per 32-block, and one
             // 8-byte store of codes.
-            float* gs = xchg;                  // [16][64] gate
-            float* us = xchg + 16 * 64;        // [16][64] up
+            float* gs = xchg + half * 2 * 16 * 64;   // [16][64] gate
+            float* us = gs + 16 * 64;                 // [16][64] up
             if (ok) {
               float* dst = (q < 2) ? gs : us;
 #pragma unroll
               for (int c = 0; c < 16; ++c) dst[c * 64 + 32 * (q & 1) + lane] = __uint_as_float(r[c]);
             }
-            named_bar_sync(1, 128);
+            named_bar_sync(bar_id, 128);
             if (ok) {
-              const int t = threadIdx.x - 128;
+              const int t = threadIdx.x - 128 - 128 * half;
               const int cc = t >> 3, f0 = (t & 7) * 8;
               const int col = c0 + cc;
               const float4 g0 = *reinterpret_cast<const float4*>(gs + cc * 64 + f0);
@@ -490,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, (BN <= 64) ? 2 : 1) grouped_gemm_ker
                 }
               }
             }
-            named_bar_sync(1, 128);
+            named_bar_sync(bar_id, 128);
           } else {
             if (ok) {
               const int feat = 128 * m + 32 * q + lane;
@@ -606,12 +618,14 @@ static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const G
   }
   const long long grid = std::min<long long>(max_items, (long long)L::kCtasPerSm * num_sms());
   if (grid <= 0) return MOE_OK;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), (size_t)smem, st, tm, tmb, gp);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(Threads<BN>::kCount), (size_t)smem, st, tm, tmb, gp);
 }
 
 template <bool W13>
 static int launch_gemm(const moe_shape* s, const uint8_t* codes, const GemmParams& gp, cudaStream_t st) {
   const long long slots = (long long)s->T * s->k;
+  // TMA row coordinates of the packed weights are 32-bit: 128 rows per tile
+  if ((long long)s->E * gp.MT * gp.KC * 128 >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
   int bn = pick_bn(s);
   // a down projection with a short K (fewer than 8 chunks) is bound by its epilogue's per-slot
   // stores, not by the MMA rate: it keeps 128-row token tiles
@@ -662,14 +676,19 @@ __global__ void gather_plan_rows_kernel(const uint8_t* __restrict__ xq, const ui
   }
 }
 
+bool w13_wants_plan_rows(const moe_shape* s) { return pick_bn(s) >= 128; }
+
 int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
                const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
-               uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, cudaStream_t st) {
+               uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, bool plan_rows_ready, cudaStream_t st) {
   if (s->T == 0) return MOE_OK;
   GemmParams gp{};
   gp.bq = xq;
   gp.bs = xs;
-  if (pick_bn(s) >= 128) {
+  if (pick_bn(s) >= 128 && plan_rows_ready) {
+    gp.bq = xq_plan;
+    gp.bs = xs_plan;
+  } else if (pick_bn(s) >= 128) {
     // wide tiles read the token operand in plan order with TMA boxes: gather it once
     const long long n = (long long)s->T * s->k * (s->H / 16 + s->H / 128);
     const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);

@@ -129,6 +129,65 @@ __global__ void pack_scales_kernel(const uint8_t* __restrict__ s, uint8_t* __res
   }
 }
 
+// The same quantisation, written straight into plan order: the codes and scales of token t go to
+// plan rows row_of_slot[t k + j] (j < k; -1 = no row), and also to q / s in token order when those
+// are given. Replaces quantise-then-gather for the wide-tile GEMM path.
+__global__ void quant_mxfp8_plan_kernel(const uint4* __restrict__ x, uint2* __restrict__ q, uint8_t* __restrict__ s,
+                                        const int32_t* __restrict__ row_of_slot, int k, int H, long long n_groups,
+                                        uint2* __restrict__ qp, uint8_t* __restrict__ sp) {
+  pdl_trigger();
+  pdl_wait();
+  const unsigned lane = threadIdx.x & 31;
+  const int g_row = H / 8;                      // 8-element groups per row
+  for (long long g0 = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31u); g0 < n_groups;
+       g0 += (long long)gridDim.x * blockDim.x) {
+    const long long g = g0 + lane;
+    const bool valid = g < n_groups;
+    uint4 v = valid ? __ldg(x + g) : make_uint4(0, 0, 0, 0);
+    float f[8];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    const int se = e4m3_scale_exp(m);
+    const float sc = pow2_neg(se);
+    const uint32_t lo = e4m3x2(f[0] * sc, f[1] * sc) | (e4m3x2(f[2] * sc, f[3] * sc) << 16);
+    const uint32_t hi = e4m3x2(f[4] * sc, f[5] * sc) | (e4m3x2(f[6] * sc, f[7] * sc) << 16);
+    if (valid) {
+      const long long t = g / g_row;
+      const int c = (int)(g - t * g_row);
+      if (q) {
+        q[g] = make_uint2(lo, hi);
+        if ((g & 3) == 0) s[g >> 2] = (uint8_t)(se + 127);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int prow = __ldg(row_of_slot + t * k + j);
+        if (prow < 0) continue;
+        qp[(long long)prow * g_row + c] = make_uint2(lo, hi);
+        if ((c & 3) == 0) sp[(long long)prow * (H / 32) + (c >> 2)] = (uint8_t)(se + 127);
+      }
+    }
+  }
+}
+
+int launch_quant_mxfp8_plan(int rows, int cols, int k, const uint16_t* x, uint8_t* q, uint8_t* s,
+                            const int32_t* row_of_slot, uint8_t* qp, uint8_t* sp, cudaStream_t st) {
+  long long groups = (long long)rows * cols / 8;
+  if (groups == 0) return MOE_OK;
+  int threads = 256;
+  long long need = (groups + threads - 1) / threads;
+  int blocks = (int)std::min<long long>(need, (long long)num_sms() * 8);
+  return launch_pdl(quant_mxfp8_plan_kernel, dim3(blocks), dim3(threads), 0, st, reinterpret_cast<const uint4*>(x),
+                    reinterpret_cast<uint2*>(q), s, row_of_slot, k, cols, groups, reinterpret_cast<uint2*>(qp), sp);
+}
+
 int launch_quant_mxfp8(int rows, int cols, const uint16_t* x, uint8_t* q, uint8_t* s, cudaStream_t st) {
   long long groups = (long long)rows * cols / 8;
   if (groups == 0) return MOE_OK;

@@ -81,19 +81,35 @@ struct ScreenParams {
   uint32_t* status;
 };
 
-__global__ void __launch_bounds__(256, 1) router_screen_kernel(const __grid_constant__ CUtensorMap tmx,
-                                                                const __grid_constant__ CUtensorMap tmw,
-                                                                const ScreenParams p) {
+// Epilogue layout: 16 warps, four per TMEM lane quarter; warp group g (0..3) of a quarter takes
+// the 16-column expert chunks g, g + 4, ... of the tile, so the 128 rows x E experts of bounds are
+// computed by 512 threads. Each thread keeps the k largest lower bounds of its experts; one thread
+// per row merges the four lists into tau (the k-th largest over all experts: the global top k is
+// inside the union of the groups' top k).
+constexpr int kScrEpiWarps = 16;
+constexpr int kScrThreads = 128 + 32 * kScrEpiWarps;
+
+static int screen_smem_bytes(int EP, int k) {
+  const int stages = kScrStages * (kScrRows * kScrK * 2 + EP * kScrK * 2);
+  const int scratch = EP * kScrRows * 4 + 4 * k * kScrRows * 4 + 2 * kScrRows * 4;
+  return 1024 + 1024 + (stages > scratch ? stages : scratch);
+}
+
+__global__ void __launch_bounds__(kScrThreads, 1) router_screen_kernel(const __grid_constant__ CUtensorMap tmx,
+                                                                        const __grid_constant__ CUtensorMap tmw,
+                                                                        const ScreenParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int stageA = kScrRows * kScrK * 2;           // 16 KB
-  const int stageB = p.EP * kScrK * 2;               // EP x 128 B
-  const int stage_bytes = stageA + stageB;
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + kScrStages * stage_bytes);
+  // first 1 KB: barriers and flags; then the stage ring, reused after the mainloop as scratch
+  uint64_t* full = reinterpret_cast<uint64_t*>(base);
   uint64_t* empty = full + kScrStages;
   uint64_t* accb = empty + kScrStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  uint8_t* ring = base + 1024;
+  const int stageA = kScrRows * kScrK * 2;           // 16 KB
+  const int stageB = p.EP * kScrK * 2;               // EP x 128 B
+  const int stage_bytes = stageA + stageB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * kScrRows;
   const int NS = p.H / kScrK;
@@ -126,7 +142,7 @@ __global__ void __launch_bounds__(256, 1) router_screen_kernel(const __grid_cons
       uint32_t phase = 0;
       for (int s = 0; s < NS; ++s) {
         if (!mbar_wait(&empty[stage], phase ^ 1, kScrWaitNs, abort_flag, p.status, DEV_TIMEOUT_EMPTY)) break;
-        uint8_t* sA = base + stage * stage_bytes;
+        uint8_t* sA = ring + stage * stage_bytes;
         mbar_arrive_expect_tx(&full[stage], stage_bytes);
         tma_load_2d(sA, &tmx, s * kScrK, t0, &full[stage]);
         tma_load_2d(sA + stageA, &tmw, s * kScrK, 0, &full[stage]);
@@ -145,7 +161,7 @@ __global__ void __launch_bounds__(256, 1) router_screen_kernel(const __grid_cons
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(base + stage * stage_bytes), b0 = a0 + stageA;
+        const uint32_t a0 = smem_u32(ring + stage * stage_bytes), b0 = a0 + stageA;
 #pragma unroll
         for (int kb = 0; kb < kScrK / 16; ++kb)
           mma_bf16(tmem, smem_desc(a0 + kb * 32, 16, 1024, 2), smem_desc(b0 + kb * 32, 16, 1024, 2), idesc,
@@ -157,25 +173,33 @@ __global__ void __launch_bounds__(256, 1) router_screen_kernel(const __grid_cons
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // one thread per row: TMEM lane = row within the CTA
-    const int tl = threadIdx.x - 128;
+    const int qd = warp & 3;                         // TMEM lane quarter
+    const int g = (warp - 4) >> 2;                   // expert-chunk group
+    const int tl = qd * 32 + lane;                   // row within the tile = TMEM lane
     const int tok = t0 + tl;
-    const uint32_t lane_base = (uint32_t)(32 * (warp - 4)) << 16;
+    const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
+    const int k = p.k;
     uint32_t okw = 1;
     if (lane == 0) okw = mbar_wait(accb, 0, kScrWaitNs, abort_flag, p.status, DEV_TIMEOUT_ACCUM) ? 1u : 0u;
     const bool ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
     tc_fence_after();
-    // the stage buffers are free now: lower bounds lo[e][row], 128 KB
-    float* lo = reinterpret_cast<float*>(base);
+    // scratch (the stage ring is free now): lo[EP][128], lists[4][k][128], tau[128], count[128]
+    float* lo = reinterpret_cast<float*>(ring);
+    float* lists = lo + p.EP * kScrRows;
+    float* tau_s = lists + 4 * k * kScrRows;
+    int* cnt_s = reinterpret_cast<int*>(tau_s + kScrRows);
     const float xn = (tok < p.T) ? p.xnorm[tok] : 0.f;
+    if (g == 0) cnt_s[tl] = 0;
+    const int nch = p.EP / 16;
     if (ok) {
-      for (int c0 = 0; c0 < p.EP; c0 += 16) {
+      for (int ch = g; ch < nch; ch += 4) {
         uint32_t r[16];
-        tmem_ld16(tmem + lane_base + c0, r);
+        tmem_ld16(tmem + lane_base + ch * 16, r);
         tmem_ld_wait();
+        reg_fence16(r);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const int e = c0 + c;
+          const int e = ch * 16 + c;
           if (e < p.E) {
             const float key = __fadd_rn(sigmoid_cw(__uint_as_float(r[c])), p.bias[e]);
             const float d = p.gamma4 * xn * p.wnorm[e] + 2e-6f;
@@ -183,42 +207,66 @@ __global__ void __launch_bounds__(256, 1) router_screen_kernel(const __grid_cons
           }
         }
       }
-    }
-    // tau = k-th largest lower bound (selection by repeated maximum, taken entries set to -inf)
-    float tau = -INFINITY;
-    if (ok) {
-      for (int j = 0; j < p.k; ++j) {
+      // this thread's k largest lower bounds (repeated maximum; taken entries set to -inf)
+      for (int j = 0; j < k; ++j) {
         float best = -INFINITY;
-        int be = 0;
-        for (int e = 0; e < p.E; ++e) {
-          const float v = lo[e * kScrRows + tl];
-          if (v > best) { best = v; be = e; }
-        }
-        tau = best;
-        lo[be * kScrRows + tl] = -INFINITY;
+        int be = -1;
+        for (int ch = g; ch < nch; ch += 4)
+          for (int c = 0; c < 16; ++c) {
+            const int e = ch * 16 + c;
+            if (e < p.E) {
+              const float v = lo[e * kScrRows + tl];
+              if (be < 0 || v > best) { best = v; be = e; }
+            }
+          }
+        lists[(g * k + j) * kScrRows + tl] = best;
+        if (be >= 0) lo[be * kScrRows + tl] = -INFINITY;
       }
     }
-    int n = 0;
+    named_bar_sync(1, 32 * kScrEpiWarps);
+    if (ok && g == 0) {
+      // tau = the k-th largest of the four lists
+      float tau = -INFINITY;
+      for (int j = 0; j < k; ++j) {
+        float best = -INFINITY;
+        int bi = 0;
+        for (int i = 0; i < 4 * k; ++i) {
+          const float v = lists[i * kScrRows + tl];
+          if (v > best) { best = v; bi = i; }
+        }
+        tau = best;
+        lists[bi * kScrRows + tl] = -INFINITY;
+      }
+      tau_s[tl] = tau;
+    }
+    named_bar_sync(1, 32 * kScrEpiWarps);
+    // (the TMEM loads are warp-collective: every lane runs them; rows past T only skip the writes)
     if (ok) {
-      for (int c0 = 0; c0 < p.EP; c0 += 16) {
+      const float tau = tau_s[tl];
+      for (int ch = g; ch < nch; ch += 4) {
         uint32_t r[16];
-        tmem_ld16(tmem + lane_base + c0, r);
+        tmem_ld16(tmem + lane_base + ch * 16, r);
         tmem_ld_wait();
+        reg_fence16(r);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const int e = c0 + c;
+          const int e = ch * 16 + c;
           if (e < p.E && tok < p.T) {
             const float key = __fadd_rn(sigmoid_cw(__uint_as_float(r[c])), p.bias[e]);
             const float d = p.gamma4 * xn * p.wnorm[e] + 2e-6f;
             if (key + d >= tau) {
+              const int n = atomicAdd(&cnt_s[tl], 1);
               if (n < kCandMax) p.cand[(size_t)tok * kCandMax + n] = e;
-              ++n;
             }
           }
         }
       }
     }
-    if (tok < p.T) p.ncand[tok] = (!ok || n > kCandMax) ? -1 : n;
+    named_bar_sync(1, 32 * kScrEpiWarps);
+    if (g == 0 && tok < p.T) {
+      const int n = cnt_s[tl];
+      p.ncand[tok] = (!ok || n > kCandMax) ? -1 : n;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -309,7 +357,7 @@ __global__ void __launch_bounds__(32, 16) router_exact_kernel(
   auto produce = [&]() {
     ExactItem it{T, 0, 0, 0};
     if (p_t < T) {
-      const int cnt = p_nc < 0 ? E : p_nc;
+      const int cnt = (p_nc < 0 || p_nc > kCandMax) ? E : p_nc;
       int e = 0;
       if (p_j >= 0) {
         const int v = __shfl_sync(0xffffffffu, p_j < 32 ? p_cl0 : p_cl1, p_j & 31);
@@ -472,14 +520,15 @@ int launch_router_screen(const moe_shape* s, const uint16_t* x, const uint16_t* 
   if (rc) return rc;
   rc = make_bf16_tmap(&tmw, wr, H, E, sp.EP);
   if (rc) return rc;
-  const int smem = 1024 + kScrStages * (kScrRows * kScrK * 2 + sp.EP * kScrK * 2) + 256;
+  const int smem = screen_smem_bytes(sp.EP, sp.k);
   static int attr = 0;
   if (attr < smem) {
     if (cudaFuncSetAttribute(router_screen_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return MOE_ERR_CUDA;
     attr = smem;
   }
-  rc = launch_pdl(router_screen_kernel, dim3(ceil_div(T, kScrRows)), dim3(256), (size_t)smem, st, tmx, tmw, sp);
+  rc = launch_pdl(router_screen_kernel, dim3(ceil_div(T, kScrRows)), dim3(kScrThreads), (size_t)smem, st, tmx, tmw,
+                  sp);
   if (rc) return rc;
   CUtensorMap tex, tew;
   const int NC = H / kRouterChunk;

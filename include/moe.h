@@ -33,6 +33,8 @@
  *    returns MOE_ERR_TIMEOUT. Zero those 4 bytes once before first use (or call
  *    moe_check_device_status, which clears them).
  *  - bf16 tensors travel as uint16_t bit patterns.
+ *  - Alignment (checked, MOE_ERR_INVALID_ARG otherwise): x, w_router, xq, hq, out, swiglu_debug
+ *    16 bytes; xs, hs, topk_idx, topk_w 4 bytes; packed codes 32 bytes, packed scales 16 bytes.
  *  - Supported shapes: H % 128 == 0, I % 64 == 0, 1 <= k <= 32, k <= E <= 1024, T >= 0,
  *    H <= 16384, I <= 16384. T == 0 is a valid no-op. Anything else -> MOE_ERR_UNSUPPORTED_SHAPE.
  *

@@ -276,8 +276,9 @@ def w2_slots(hq: np.ndarray, hs: np.ndarray, w2: ExpertWeights, routing: Routing
     return y
 
 
-def combine(y_by_slot: dict[int, np.ndarray], t_: int, k: int, h_: int, tokens) -> np.ndarray:
-    """out[t] = bf16(((y_0 + y_1) + ...) ) for the given tokens; absent slots (dead) give +0."""
+def combine_exact(y_by_slot: dict[int, np.ndarray], t_: int, k: int, h_: int, tokens) -> np.ndarray:
+    """((y_0 + y_1) + ...) in float64 for the given tokens, before the output rounding; absent
+    slots (dead) give 0."""
     out = np.zeros((len(tokens), h_), dtype=np.float64)
     for n, t in enumerate(tokens):
         acc = np.zeros(h_, dtype=np.float64)
@@ -288,7 +289,12 @@ def combine(y_by_slot: dict[int, np.ndarray], t_: int, k: int, h_: int, tokens) 
                 acc = acc + yj
                 live = True
         out[n] = acc if live else 0.0
-    return F.round_to_bf16(out) + 0.0             # + 0.0 turns a -0.0 into +0.0
+    return out
+
+
+def combine(y_by_slot: dict[int, np.ndarray], t_: int, k: int, h_: int, tokens) -> np.ndarray:
+    """out[t] = bf16(((y_0 + y_1) + ...) ) for the given tokens; absent slots (dead) give +0."""
+    return F.round_to_bf16(combine_exact(y_by_slot, t_, k, h_, tokens)) + 0.0   # + 0.0: -0.0 -> +0.0
 
 
 @dataclass
@@ -299,6 +305,7 @@ class ForwardResult:
     w13: W13Result
     out: np.ndarray            # float64 values of the bf16 output [len(tokens), H]
     tokens: np.ndarray
+    out_exact: np.ndarray      # the same sums before the bf16 rounding
 
 
 def forward(x, wr, bias, k, w13: ExpertWeights, w2: ExpertWeights, inter: int,
@@ -320,7 +327,8 @@ def forward(x, wr, bias, k, w13: ExpertWeights, w2: ExpertWeights, inter: int,
     r13 = w13_swiglu(xq, xs, w13, routing, k, inter, rows)
     y = w2_slots(r13.hq, r13.hs, w2, routing, k, rows)
     y_by_slot = {int(routing.slot_of_row[p]): y[n] for n, p in enumerate(rows)}
-    out = combine(y_by_slot, t_, k, h_, tokens)
+    out_exact = combine_exact(y_by_slot, t_, k, h_, tokens)
+    out = F.round_to_bf16(out_exact) + 0.0
     r13_rows = r13
     r13_rows.rows = rows
-    return ForwardResult(routing, xq, xs, r13_rows, out, tokens)
+    return ForwardResult(routing, xq, xs, r13_rows, out, tokens, out_exact)

@@ -103,6 +103,24 @@ inline int num_sms() {
   return n;
 }
 
+// CTAs of `smem_bytes` dynamic shared memory that fit on one SM, capped at `cap` (the per-SM
+// shared-memory capacity minus the per-block reservation, as the device reports them).
+inline int ctas_per_sm_by_smem(size_t smem_bytes, int cap) {
+  static int per_sm = 0, reserved = 0;
+  if (!per_sm) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        per_sm <= 0)
+      per_sm = 228 * 1024;
+    if (cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+      reserved = 1024;
+  }
+  int n = (int)((size_t)per_sm / (smem_bytes + (size_t)reserved));
+  if (n > cap) n = cap;
+  return n < 1 ? 1 : n;
+}
+
 // Launch with the programmatic-stream-serialization attribute: the kernel may begin while the
 // previous kernel on `st` finishes (it calls pdl_wait() before reading anything produced upstream).
 template <typename... KArgs, typename... Args>

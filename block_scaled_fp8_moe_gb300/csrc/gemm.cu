@@ -74,12 +74,24 @@ struct GemmParams {
   uint32_t* status;
 };
 
+#ifndef MOE_DEC_KT
+#define MOE_DEC_KT 1                // K-chunks per stage, decode tiles (16 / 32 token rows)
+#endif
+#ifndef MOE_DEC_STAGES
+#define MOE_DEC_STAGES 3
+#endif
+#ifndef MOE_DEC_CTAS
+#define MOE_DEC_CTAS 3              // decode-tile CTAs per SM
+#endif
+
+__host__ __device__ constexpr int pow2_at_least(int v, int p) { return p >= v ? p : pow2_at_least(v, 2 * p); }
+
 template <int BN>
 struct Smem {
   // A pipeline stage holds KT consecutive K-chunks (weight tiles) of 128: small token tiles are
   // weight-streaming bound and each stage hand-off costs a fixed few hundred ns per CTA, so they
   // move 16 KB of packed weights per TMA request.
-  static constexpr int KT = (BN <= 32) ? 2 : (BN <= 64 ? 1 : (BN == 128 ? MOE_KT_WIDE : 1));
+  static constexpr int KT = (BN <= 32) ? MOE_DEC_KT : (BN <= 64 ? 1 : (BN == 128 ? MOE_KT_WIDE : 1));
   static constexpr int kTileA = 16384;                           // one unpacked 128 x 128 FP4 tile
   static constexpr int kTileB = BN * 128;                        // BN rows x 128 FP8
   static constexpr int kStageA = KT * kTileA;
@@ -87,14 +99,16 @@ struct Smem {
   static constexpr int kSfbChunk = 512 * ((BN + 127) / 128);     // B scale atoms of one K-chunk
   static constexpr int kSfChunk = 512 + kSfbChunk;
   static constexpr int kStageBytes = (int)((kStageA + kStageB + KT * kSfChunk + 1023) / 1024 * 1024);
-  static constexpr int kStages = (BN <= 32) ? 2 : (BN <= 64 ? 3 : (BN == 128 ? 6 / MOE_KT_WIDE : 4));
-  static constexpr int kCtasPerSm = (BN <= 64) ? 2 : 1;
+  static constexpr int kStages = (BN <= 32) ? MOE_DEC_STAGES : (BN <= 64 ? 3 : (BN == 128 ? 6 / MOE_KT_WIDE : 4));
+  static constexpr int kCtasPerSm = (BN <= 32) ? MOE_DEC_CTAS : (BN <= 64 ? 2 : 1);
   // TMEM: two accumulator slots of kAccStride columns, then the ring of scale blocks (one slot of
-  // kSfSlot columns per K-chunk in flight: 4 for A, 4 per 128 token rows for B)
-  static constexpr int kAccStride = (BN <= 64) ? 64 : BN;
+  // kSfSlot columns per K-chunk in flight: 4 for A, 4 per 128 token rows for B); the allocation is
+  // the next power of two, small enough for kCtasPerSm CTAs to share the SM's 512 columns
+  static constexpr int kAccStride = (BN <= 32) ? 32 : (BN <= 64 ? 64 : BN);
   static constexpr int kSfCol = 2 * kAccStride;
   static constexpr int kSfSlot = 4 + 4 * ((BN + 127) / 128);
-  static constexpr int kTmemCols = (BN <= 64) ? 256 : 512;
+  static constexpr int kTmemCols = pow2_at_least(kSfCol + kStages * KT * kSfSlot, 32);
+  static_assert(kTmemCols * kCtasPerSm <= 512, "TMEM columns per SM");
   static_assert(kSfCol + kStages * KT * kSfSlot <= kTmemCols, "TMEM columns");
   // wide token tiles read the activation operand with TMA (one 2D box of plan-order rows per
   // K-chunk) instead of cp.async gathers, and size each expert's tiles to its row count
@@ -131,7 +145,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 }
 
 template <int BN, bool W13>
-__global__ void __launch_bounds__(Threads<BN>::kCount, (BN <= 64) ? 2 : 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+__global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                     const __grid_constant__ CUtensorMap tmap_b,
                                                                     const GemmParams p) {
   using L = Smem<BN>;
@@ -438,7 +452,7 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, (BN <= 64) ? 2 : 1) group
       tc_fence_after();
       const uint32_t d_tmem = tmem + (uint32_t)(acc * L::kAccStride);
       // TMEM is read kGrp 16-column chunks per round trip (one wait for several loads)
-      constexpr int kGrp = W13 ? 2 : 4;
+      constexpr int kGrp = W13 ? 2 : (BN >= 64 ? 4 : BN / 16);
       for (int cg = 16 * kGrp * half; cg < tw; cg += 16 * kGrp * kHalves) {
         uint32_t rg[kGrp][16];
         if (ok) {
@@ -616,7 +630,9 @@ static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const G
       return MOE_ERR_CUDA;
     attr = L::total(kMaxE);
   }
-  const long long grid = std::min<long long>(max_items, (long long)L::kCtasPerSm * num_sms());
+  // persistent grid: as many CTAs as fit on the GPU at once (smem depends on E)
+  const int occ = ctas_per_sm_by_smem((size_t)smem, L::kCtasPerSm);
+  const long long grid = std::min<long long>(max_items, (long long)occ * num_sms());
   if (grid <= 0) return MOE_OK;
   return launch_pdl(kern, dim3((unsigned)grid), dim3(Threads<BN>::kCount), (size_t)smem, st, tm, tmb, gp);
 }

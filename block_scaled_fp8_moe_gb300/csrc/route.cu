@@ -73,19 +73,25 @@ __global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __res
 }
 
 // ---------------------------------------------------------------------------------------------
-// Logits, small T (decode), x staged in shared memory. A CTA owns kDecEpc experts; each thread
-// item (expert, chunk) streams its 128 bytes of Wr once (8 loads in flight) and runs the
-// sequential fma chain of that chunk for every token from shared memory; the chunk partials are
-// then folded left to right per (expert, token). The same order as router_small_kernel and the
-// tiled kernel. Optionally each CTA also MXFP8-quantises a share of the rows it already holds.
+// Logits, small T (decode), x staged in shared memory kDecGroup rows at a time by cp.async (all
+// of a group's 16-byte copies in flight at once; chunk pitch 144 B so a quarter-warp's 16-byte
+// reads of consecutive chunks hit distinct banks). A CTA owns kDecEpc experts; each thread item
+// (expert, chunk) loads its 128 bytes of Wr once (8 loads in flight) and, for every staged token,
+// runs the sequential fma chain of that chunk (bf16 operands, fp32 accumulate); the chunk
+// partials are then folded left to right per (expert, token). The same order as
+// router_small_kernel and the tiled kernel. Optionally each CTA also MXFP8-quantises a share of
+// the rows it has staged.
 // ---------------------------------------------------------------------------------------------
 constexpr int kDecEpc = 4;          // experts per CTA
-constexpr size_t kDecodeSmemMax = 160 * 1024;
-constexpr int kDecPad = 66;         // bf16 per staged 64-element chunk (2 pad -> conflict-free)
+constexpr int kDecGroup = 16;       // token rows staged at a time
+constexpr int kDecMaxT = 64;
+constexpr size_t kDecodeSmemMax = 210 * 1024;
+constexpr int kDecPitch = 144;      // bytes per staged 64-element chunk
 
 __host__ __device__ inline size_t router_decode_smem(int T, int H) {
   const int NC = H / kRouterChunk;
-  return (size_t)T * NC * kDecPad * 2 + (size_t)kDecEpc * T * NC * 4;
+  const int G = T < kDecGroup ? T : kDecGroup;
+  return (size_t)G * NC * kDecPitch + (size_t)kDecEpc * T * NC * 4;
 }
 
 __global__ void __launch_bounds__(256) router_decode_kernel(const uint16_t* __restrict__ x,
@@ -97,66 +103,79 @@ __global__ void __launch_bounds__(256) router_decode_kernel(const uint16_t* __re
   pdl_wait();
   extern __shared__ __align__(16) uint8_t dsm_dec[];
   const int NC = H / kRouterChunk;
-  uint16_t* xsm = reinterpret_cast<uint16_t*>(dsm_dec);                                // [T][NC][kDecPad]
-  float* part = reinterpret_cast<float*>(dsm_dec + (size_t)T * NC * kDecPad * 2);     // [kDecEpc][T][NC]
+  const int G = T < kDecGroup ? T : kDecGroup;
+  uint8_t* xsm = dsm_dec;                                                        // [G][NC] chunks
+  float* part = reinterpret_cast<float*>(dsm_dec + (size_t)G * NC * kDecPitch);  // [kDecEpc][T][NC]
   const int e0 = blockIdx.x * kDecEpc;
-  // stage x (16-byte global loads, 4-byte shared stores into the padded chunk layout)
-  for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) {
-    const int t = i / (H / 8), h = (i % (H / 8)) * 8;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + h));
-    uint32_t* d = reinterpret_cast<uint32_t*>(xsm + ((size_t)t * NC + h / kRouterChunk) * kDecPad + (h % kRouterChunk));
-    d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
-  }
-  __syncthreads();
-  for (int it = threadIdx.x; it < kDecEpc * NC; it += blockDim.x) {
-    const int el = it / NC, c = it % NC;
-    const int e = e0 + el;
-    if (e >= E) continue;
-    const uint4* wp = reinterpret_cast<const uint4*>(wr + (size_t)e * H + (size_t)c * kRouterChunk);
-    uint4 wv[8];
+  // this thread's (expert, chunk) item and its Wr chunk, loaded once for every token group
+  const int items = kDecEpc * NC;
+  const int it0 = threadIdx.x;
+  const bool has_item = it0 < items && e0 + it0 / NC < E;     // kDecEpc * NC <= blockDim.x
+  uint4 wv[8];
+  if (has_item) {
+    const uint4* wp =
+        reinterpret_cast<const uint4*>(wr + (size_t)(e0 + it0 / NC) * H + (size_t)(it0 % NC) * kRouterChunk);
 #pragma unroll
     for (int i = 0; i < 8; ++i) wv[i] = __ldg(wp + i);
-    for (int t = 0; t < T; ++t) {
-      const uint32_t* xp = reinterpret_cast<const uint32_t*>(xsm + ((size_t)t * NC + c) * kDecPad);
-      float p = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t xw = xp[i * 4 + q];
-          p = __fmaf_rn(bf_lo(xw), bf_lo(ww[q]), p);
-          p = __fmaf_rn(bf_hi(xw), bf_hi(ww[q]), p);
-        }
-      }
-      part[((size_t)el * T + t) * NC + c] = p;
-    }
   }
-  // MXFP8 quantisation of a share of the staged rows (one 32-block per thread item)
-  if (xq) {
-    const int nblk = T * H / 32;
-    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += gridDim.x * blockDim.x) {
-      const int t = b / (H / 32), h = (b % (H / 32)) * 32;
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(xsm + ((size_t)t * NC + h / kRouterChunk) * kDecPad +
-                                                              (h % kRouterChunk));
-      float f[32];
-      float m = 0.f;
+  for (int g0 = 0; g0 < T; g0 += G) {
+    const int gn = min(G, T - g0);
+    if (g0 > 0) __syncthreads();                  // previous group's rows no longer read
+    // stage rows g0 .. g0 + gn: 16-byte unit u of chunk (t, c) from x[g0 + t, 64 c + 8 u]
+    for (int i = threadIdx.x; i < gn * NC * 8; i += blockDim.x) {
+      const int u = i & 7, tc = i >> 3;
+      const int t = tc / NC, c = tc - t * NC;
+      cp_async_16(xsm + (size_t)tc * kDecPitch + u * 16, x + (size_t)(g0 + t) * H + c * kRouterChunk + u * 8, 16);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    if (has_item) {
+      const int el = it0 / NC, c = it0 % NC;
+      for (int t = 0; t < gn; ++t) {
+        const uint4* xp = reinterpret_cast<const uint4*>(xsm + ((size_t)t * NC + c) * kDecPitch);
+        float p = 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        f[2 * i] = bf_lo(src[i]);
-        f[2 * i + 1] = bf_hi(src[i]);
-        m = fmaxf(m, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+        for (int i = 0; i < 8; ++i) {
+          const uint4 xv = xp[i];
+          p = fma2_bf16(xv.x, wv[i].x, p);
+          p = fma2_bf16(xv.y, wv[i].y, p);
+          p = fma2_bf16(xv.z, wv[i].z, p);
+          p = fma2_bf16(xv.w, wv[i].w, p);
+        }
+        part[((size_t)el * T + g0 + t) * NC + c] = p;
       }
-      const int se = e4m3_scale_exp(m);
-      const float sc = pow2_neg(se);
-      uint32_t o[8];
+    }
+    // MXFP8 quantisation of a share of the staged rows (one 32-block per thread item)
+    if (xq) {
+      const int nblk = gn * H / 32;
+      for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += gridDim.x * blockDim.x) {
+        const int t = b / (H / 32), h = (b % (H / 32)) * 32;
+        const uint4* src = reinterpret_cast<const uint4*>(xsm + ((size_t)t * NC + h / kRouterChunk) * kDecPitch +
+                                                          (h % kRouterChunk) * 2);
+        float f[32];
+        float m = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        o[i] = e4m3x2(f[4 * i] * sc, f[4 * i + 1] * sc) | (e4m3x2(f[4 * i + 2] * sc, f[4 * i + 3] * sc) << 16);
-      uint4* dq = reinterpret_cast<uint4*>(xq + (size_t)t * H + h);
-      dq[0] = make_uint4(o[0], o[1], o[2], o[3]);
-      dq[1] = make_uint4(o[4], o[5], o[6], o[7]);
-      xs[(size_t)t * (H / 32) + h / 32] = (uint8_t)(se + 127);
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = src[i];
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            f[8 * i + 2 * q] = bf_lo(w4[q]);
+            f[8 * i + 2 * q + 1] = bf_hi(w4[q]);
+            m = fmaxf(m, fmaxf(fabsf(f[8 * i + 2 * q]), fabsf(f[8 * i + 2 * q + 1])));
+          }
+        }
+        const int se = e4m3_scale_exp(m);
+        const float sc = pow2_neg(se);
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          o[i] = e4m3x2(f[4 * i] * sc, f[4 * i + 1] * sc) | (e4m3x2(f[4 * i + 2] * sc, f[4 * i + 3] * sc) << 16);
+        uint4* dq = reinterpret_cast<uint4*>(xq + (size_t)(g0 + t) * H + h);
+        dq[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dq[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        xs[(size_t)(g0 + t) * (H / 32) + h / 32] = (uint8_t)(se + 127);
+      }
     }
   }
   __syncthreads();
@@ -596,7 +615,7 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
   float* key = ws_ptr<float>(ws, L.key);
   const size_t dec_smem = router_decode_smem(T, H);
   int rc0 = MOE_OK;
-  if (T <= kSmallT && dec_smem <= kDecodeSmemMax) {
+  if (T <= kDecMaxT && kDecEpc * (H / kRouterChunk) <= 256 && dec_smem <= kDecodeSmemMax) {
     static bool dec_attr = false;
     if (!dec_attr) {
       if (cudaFuncSetAttribute(router_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

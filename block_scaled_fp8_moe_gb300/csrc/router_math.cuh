@@ -40,4 +40,17 @@ __device__ __forceinline__ float sigmoid_cw(float z) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// acc <- fma(lo(x), lo(w), acc), then the same for the high halves (elements 2i, 2i + 1): fp32
+// fused multiply-add of bf16 operands, one rounding per step -- the same value as widening first.
+__device__ __forceinline__ float fma2_bf16(uint32_t x, uint32_t w, float acc) {
+  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+      "mov.b32 {xl, xh}, %1;\n\t"
+      "mov.b32 {wl, wh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, xl, wl, %0;\n\t"
+      "fma.rn.f32.bf16 %0, xh, wh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(x), "r"(w));
+  return acc;
+}
+
 }  // namespace moe

@@ -302,18 +302,6 @@ static size_t exact_smem_bytes(int H) {
          kExactStages * (sizeof(ExactItem) + 8) + 16;
 }
 
-// acc <- fma(lo(x), lo(w), acc), then the same for the high halves (elements 2i, 2i + 1)
-__device__ __forceinline__ float fma2_bf16(uint32_t x, uint32_t w, float acc) {
-  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
-      "mov.b32 {xl, xh}, %1;\n\t"
-      "mov.b32 {wl, wh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, xl, wl, %0;\n\t"
-      "fma.rn.f32.bf16 %0, xh, wh, %0;\n\t}"
-      : "+f"(acc)
-      : "r"(x), "r"(w));
-  return acc;
-}
-
 __global__ void __launch_bounds__(32, 16) router_exact_kernel(
     const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw, const float* __restrict__ bias,
     const int32_t* __restrict__ cand, const int32_t* __restrict__ ncand, int T, int H, int E,
@@ -538,16 +526,13 @@ int launch_router_screen(const moe_shape* s, const uint16_t* x, const uint16_t* 
   if (rc) return rc;
   const size_t esmem = exact_smem_bytes(H);
   static size_t eattr = 0;
-  static int eper_sm = 0;
   if (eattr < esmem) {
     if (cudaFuncSetAttribute(router_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)esmem) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     eattr = esmem;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&eper_sm, router_exact_kernel, 32, esmem) != cudaSuccess ||
-        eper_sm < 1)
-      eper_sm = 1;
   }
+  const int eper_sm = ctas_per_sm_by_smem(esmem, 16);
   const int eg = (int)std::min<long long>(T, (long long)num_sms() * eper_sm);
   return launch_pdl(router_exact_kernel, dim3(eg), dim3(32), esmem, st, tex, tew, bias, cand, ncand, T, H, E, score,
                     key, sp.status);

@@ -242,10 +242,20 @@ class ClockSampler:
 # GPU arm
 # ----------------------------------------------------------------------------------------------
 def launches_per_step(cfg) -> int:
-    n = 1 + 1                     # router logits + top-k/plan
-    if cfg.T > 256:
-        n += 2                    # plan scan + scatter
-    return n + 1 + 1 + 1 + 1      # quant, W13, W2, combine
+    """Kernels one moe_forward launches for this shape (mirrors the library's dispatch)."""
+    T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
+    nc = H // 64
+    decode_router = T <= 64 and 4 * nc <= 256 and (min(T, 16) * nc * 144 + 4 * T * nc * 4) <= 210 * 1024
+    if decode_router:
+        n = 1                                         # logits (+ fused MXFP8 quantisation)
+    elif T > 16 and E <= 256 and H % 64 == 0 and H <= 4096:
+        n = 3                                         # norms, tensor-core screen, exact recompute
+    else:
+        n = 1                                         # small-T or tiled logits
+    n += 1 if T <= 256 else 4                         # top-k + plan (+ grid-wide select, scan, scatter)
+    if not decode_router:
+        n += 1                                        # MXFP8 quantisation (straight into plan order when wide)
+    return n + 3                                      # W13, W2, combine
 
 
 def gpu_arm(args):

@@ -23,7 +23,7 @@ EXPORTED = [
     "moe_status_string", "moe_workspace_bytes", "moe_packed_w13_bytes", "moe_packed_w2_bytes",
     "moe_quant_mxfp4", "moe_pack_w13", "moe_pack_w2", "moe_route_topk", "moe_quant_mxfp8",
     "moe_w13_swiglu_grouped", "moe_w2_combine_grouped", "moe_forward", "moe_check_device_status",
-    "moe_route_topk_noalloc", "moe_selftest_timeout",
+    "moe_route_topk_noalloc", "moe_selftest_timeout", "moe_route_topk_anchored", "moe_forward_anchored",
 ]
 
 
@@ -61,6 +61,8 @@ lib.moe_forward.argtypes = [_SHP] + [_P] * 9 + [ctypes.POINTER(MoeIntermediates)
 lib.moe_check_device_status.argtypes = [_P, _P]
 lib.moe_route_topk_noalloc.argtypes = [_SHP] + [_P] * 10 + [_P]
 lib.moe_selftest_timeout.argtypes = [_P, ctypes.c_uint64, _P]
+lib.moe_route_topk_anchored.argtypes = [_SHP] + [_P] * 11 + [_P, _SZ, _P]
+lib.moe_forward_anchored.argtypes = [_SHP] + [_P] * 10 + [ctypes.POINTER(MoeIntermediates), _P, _SZ, _P]
 for _n in EXPORTED:
     if _n not in ("moe_status_string", "moe_workspace_bytes", "moe_packed_w13_bytes", "moe_packed_w2_bytes"):
         getattr(lib, _n).restype = ctypes.c_int
@@ -180,14 +182,18 @@ class Plan:
         self.row_of_slot = torch.empty(max(T * k, 1), dtype=torch.int32, device=device)
 
 
-def moe_route_topk(shp: MoeShape, x, w_router, bias, dead, ws, plan: Plan | None = None, stream=None) -> Plan:
+def moe_route_topk(shp: MoeShape, x, w_router, bias, dead, ws, plan: Plan | None = None, stream=None,
+                   anchor=None) -> Plan:
+    """anchor (optional int32 [T]): -1 routes the row itself, a >= 0 reuses row a's experts."""
     plan = Plan(shp, x.device) if plan is None else plan
     T, H, E = shp.T, shp.H, shp.E
-    _check(lib.moe_route_topk(
+    _check(lib.moe_route_topk_anchored(
         ctypes.byref(shp), _ptr(x, torch.bfloat16, T * H, "x"), _ptr(w_router, torch.bfloat16, E * H, "w_router"),
         _ptr(bias, torch.float32, E, "bias"), _ptr(dead, torch.uint8, T, "dead"),
+        _ptr(anchor, torch.int32, T, "anchor"),
         _ptr(plan.topk_idx), _ptr(plan.topk_w), _ptr(plan.expert_counts), _ptr(plan.expert_offsets),
-        _ptr(plan.slot_of_row), _ptr(plan.row_of_slot), _ptr(ws), ws.numel(), _stream(stream)), "moe_route_topk")
+        _ptr(plan.slot_of_row), _ptr(plan.row_of_slot), _ptr(ws), ws.numel(), _stream(stream)),
+        "moe_route_topk_anchored")
     return plan
 
 
@@ -229,18 +235,28 @@ def moe_w2_combine_grouped(shp: MoeShape, hq, hs, w2p, w2sp, plan: Plan, ws, out
 
 
 def moe_forward(shp: MoeShape, x, w_router, bias, dead, w13p, w13sp, w2p, w2sp, ws, out=None,
-                inter: dict | None = None, stream=None):
+                inter: dict | None = None, stream=None, anchor=None):
     out = torch.empty(shp.T, shp.H, dtype=torch.bfloat16, device=x.device) if out is None else out
     im = None
     if inter:
         im = MoeIntermediates(*[ctypes.c_void_p(inter[n].data_ptr()) if inter.get(n) is not None else None
                                 for n, _ in MoeIntermediates._fields_])
-    _check(lib.moe_forward(
-        ctypes.byref(shp), _ptr(x, torch.bfloat16, shp.T * shp.H, "x"),
-        _ptr(w_router, torch.bfloat16, shp.E * shp.H, "w_router"), _ptr(bias, torch.float32, shp.E, "bias"),
-        _ptr(dead, torch.uint8, shp.T, "dead"), _ptr(w13p, torch.uint8), _ptr(w13sp, torch.uint8),
-        _ptr(w2p, torch.uint8), _ptr(w2sp, torch.uint8), _ptr(out, torch.bfloat16, shp.T * shp.H, "out"),
-        ctypes.byref(im) if im is not None else None, _ptr(ws), ws.numel(), _stream(stream)), "moe_forward")
+    if anchor is None:
+        _check(lib.moe_forward(
+            ctypes.byref(shp), _ptr(x, torch.bfloat16, shp.T * shp.H, "x"),
+            _ptr(w_router, torch.bfloat16, shp.E * shp.H, "w_router"), _ptr(bias, torch.float32, shp.E, "bias"),
+            _ptr(dead, torch.uint8, shp.T, "dead"), _ptr(w13p, torch.uint8), _ptr(w13sp, torch.uint8),
+            _ptr(w2p, torch.uint8), _ptr(w2sp, torch.uint8), _ptr(out, torch.bfloat16, shp.T * shp.H, "out"),
+            ctypes.byref(im) if im is not None else None, _ptr(ws), ws.numel(), _stream(stream)), "moe_forward")
+    else:
+        _check(lib.moe_forward_anchored(
+            ctypes.byref(shp), _ptr(x, torch.bfloat16, shp.T * shp.H, "x"),
+            _ptr(w_router, torch.bfloat16, shp.E * shp.H, "w_router"), _ptr(bias, torch.float32, shp.E, "bias"),
+            _ptr(dead, torch.uint8, shp.T, "dead"), _ptr(anchor, torch.int32, shp.T, "anchor"),
+            _ptr(w13p, torch.uint8), _ptr(w13sp, torch.uint8),
+            _ptr(w2p, torch.uint8), _ptr(w2sp, torch.uint8), _ptr(out, torch.bfloat16, shp.T * shp.H, "out"),
+            ctypes.byref(im) if im is not None else None, _ptr(ws), ws.numel(), _stream(stream)),
+            "moe_forward_anchored")
     return out
 
 
@@ -281,7 +297,7 @@ class MoeLayer:
             self._ws[T] = alloc_workspace(self.shape(T), self.w_router.device)
         return self._ws[T]
 
-    def forward(self, x, dead=None, out=None, inter=None, stream=None):
+    def forward(self, x, dead=None, out=None, inter=None, stream=None, anchor=None):
         T = x.shape[0]
         return moe_forward(self.shape(T), x, self.w_router, self.bias, dead, self.w13p, self.w13sp, self.w2p,
-                           self.w2sp, self.workspace(T), out=out, inter=inter, stream=stream)
+                           self.w2sp, self.workspace(T), out=out, inter=inter, stream=stream, anchor=anchor)

@@ -72,7 +72,17 @@ extern "C" int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t
                            const uint8_t* dead, const uint8_t* w13, const uint8_t* w13_s, const uint8_t* w2,
                            const uint8_t* w2_s, uint16_t* out, const moe_intermediates* inter, void* ws,
                            size_t ws_bytes, void* stream) {
+  return moe_forward_anchored(s, x, w_router, bias, dead, nullptr, w13, w13_s, w2, w2_s, out, inter, ws, ws_bytes,
+                              stream);
+}
+
+extern "C" int moe_forward_anchored(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
+                                    const float* bias, const uint8_t* dead, const int32_t* anchor,
+                                    const uint8_t* w13, const uint8_t* w13_s, const uint8_t* w2, const uint8_t* w2_s,
+                                    uint16_t* out, const moe_intermediates* inter, void* ws, size_t ws_bytes,
+                                    void* stream) {
   if (!s) return MOE_ERR_INVALID_ARG;
+  if (!aligned(anchor, 4)) return MOE_ERR_INVALID_ARG;
   if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
   int rc = ws_check(s, ws, ws_bytes);
   if (rc) return rc;
@@ -107,7 +117,7 @@ extern "C" int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t
 
   bool quant_done = false;
   rc = launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, ws, st,
-                    xq, xs, &quant_done);
+                    xq, xs, &quant_done, anchor);
   if (rc) return rc;
   uint8_t* xqp = ws_ptr<uint8_t>(ws, L.xqp);
   uint8_t* xsp = ws_ptr<uint8_t>(ws, L.xsp);

@@ -150,10 +150,11 @@ int launch_quant_mxfp8_plan(int rows, int cols, int k, const uint16_t* x, uint8_
 // True when W13 runs wide token tiles, whose activation operand is read in plan order.
 bool w13_wants_plan_rows(const moe_shape* s);
 // When xq/xs are given and the small-batch router runs, it also writes the MXFP8 quantisation of x
-// and sets *quant_done.
+// and sets *quant_done. anchor (nullable): rows that reuse another row's experts.
 int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, const uint8_t* dead,
                  int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
-                 int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done);
+                 int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done,
+                 const int32_t* anchor);
 int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
                const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
                uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, bool plan_rows_ready, cudaStream_t st);
@@ -165,6 +166,6 @@ int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slo
 // the same score/key rows as the exact router for every expert that can be selected.
 bool router_screen_supported(const moe_shape* s);
 int launch_router_screen(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, void* ws,
-                         float* score, float* key, cudaStream_t st);
+                         float* score, float* key, cudaStream_t st, const int32_t* anchor);
 
 }  // namespace moe

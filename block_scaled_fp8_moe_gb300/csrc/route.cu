@@ -308,6 +308,30 @@ __device__ void block_exclusive_scan(int* vals, int n, int* total) {
   __syncthreads();
 }
 
+// Anchored verify rows (TP4 serving profile README, settings table row "Verify length"): a row
+// with anchor[t] = a reuses row a's experts (a routes itself) and weights them with its own scores,
+// so it reaches no expert its anchor does not. An anchor outside [0, T) or one that is itself
+// anchored is ignored (the row routes itself) and recorded in the status word.
+__device__ __forceinline__ int anchor_of(const int32_t* __restrict__ anchor, int t, int T, uint32_t* status) {
+  if (!anchor) return -1;
+  const int a = anchor[t];
+  if (a < 0) return -1;
+  if (a >= T || anchor[a] != -1) {
+    if (status) atomicCAS(status, 0u, (uint32_t)DEV_BAD_PLAN);
+    return -1;
+  }
+  return a;
+}
+
+// Lane j < k gets expert e (the anchor's j-th choice) and the row's weight score[e] / sum, the sum
+// taken in rank order (identical on every lane).
+__device__ __forceinline__ void anchored_weights(const float* __restrict__ srow, int e, int k, int lane, float* w) {
+  const float sc = lane < k ? srow[e] : 0.f;
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, sc, j));
+  *w = __fdiv_rn(sc, sum);
+}
+
 // One token's top-k on one warp. Lane l holds experts l, l + 32, ... (NI of them) and its own
 // best untaken (key desc, expert asc); each round is a warp arg-max over the lanes' bests (two
 // warp reductions), after which only the winning lane rescans its NI values. Selected weights: sigma_j / sum, the sum
@@ -367,17 +391,40 @@ template <int NI>
 __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restrict__ score,
                                                           const float* __restrict__ key, int T, int E, int k,
                                                           int32_t* __restrict__ topk_idx,
-                                                          float* __restrict__ topk_w) {
+                                                          float* __restrict__ topk_w,
+                                                          const int32_t* __restrict__ anchor, uint32_t* status) {
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+    if (anchor_of(anchor, t, T, status) >= 0) continue;      // filled in by anchor_fixup_kernel
     int my_e = -1;
     float my_s = 0.f, sum = 0.f;
     warp_topk<NI>(key + (size_t)t * E, score + (size_t)t * E, E, k, lane, nullptr, &my_e, &my_s, &sum);
     if (lane < k) {
       topk_idx[(size_t)t * k + lane] = my_e;
       topk_w[(size_t)t * k + lane] = __fdiv_rn(my_s, sum);
+    }
+  }
+}
+
+// Anchored rows of the grid-wide selection: one warp per row copies the anchor's choices.
+__global__ void __launch_bounds__(256) anchor_fixup_kernel(const float* __restrict__ score, int T, int E, int k,
+                                                           const int32_t* __restrict__ anchor,
+                                                           int32_t* __restrict__ topk_idx,
+                                                           float* __restrict__ topk_w) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+    const int a = anchor_of(anchor, t, T, nullptr);
+    if (a < 0) continue;
+    const int e = lane < k ? topk_idx[(size_t)a * k + lane] : 0;
+    float w;
+    anchored_weights(score + (size_t)t * E, e, k, lane, &w);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = e;
+      topk_w[(size_t)t * k + lane] = w;
     }
   }
 }
@@ -391,7 +438,8 @@ __global__ void __launch_bounds__(512) topk_plan_kernel(const float* __restrict_
                                                         int32_t* __restrict__ cnt, int32_t* __restrict__ rank,
                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                         int32_t* __restrict__ slot_of_row,
-                                                        int32_t* __restrict__ row_of_slot) {
+                                                        int32_t* __restrict__ row_of_slot,
+                                                        const int32_t* __restrict__ anchor, uint32_t* status) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ uint32_t dsm[];
@@ -407,12 +455,30 @@ __global__ void __launch_bounds__(512) topk_plan_kernel(const float* __restrict_
   if (SELECT) {
     for (int tl = warp; tl < nt; tl += kTopkWarps) {
       const int t = tb0 + tl;
+      if (anchor_of(anchor, t, T, status) >= 0) continue;    // after every self-routed row
       int my_e = -1;
       float my_s = 0.f, sum = 0.f;
       warp_topk<NI>(key + (size_t)t * E, score + (size_t)t * E, E, k, lane, sidx + tl * k, &my_e, &my_s, &sum);
       if (lane < k) {
         topk_idx[(size_t)t * k + lane] = my_e;
         topk_w[(size_t)t * k + lane] = __fdiv_rn(my_s, sum);
+      }
+    }
+    if (anchor) {
+      // one block holds every row here (T <= kPlanBlock): the anchor's choices are in sidx
+      __syncthreads();
+      for (int tl = warp; tl < nt; tl += kTopkWarps) {
+        const int t = tb0 + tl;
+        const int a = anchor_of(anchor, t, T, nullptr);
+        if (a < 0) continue;
+        const int e = lane < k ? (int)sidx[(a - tb0) * k + lane] : 0;
+        float w;
+        anchored_weights(score + (size_t)t * E, e, k, lane, &w);
+        if (lane < k) {
+          topk_idx[(size_t)t * k + lane] = e;
+          topk_w[(size_t)t * k + lane] = w;
+          sidx[tl * k + lane] = (int16_t)e;
+        }
       }
     }
   } else {
@@ -524,7 +590,7 @@ template <int NI>
 static int launch_topk_plan_ni(int nb, int E, size_t smem, cudaStream_t st, const float* score, const float* key,
                                const uint8_t* dead, int T, int k, int32_t* topk_idx, float* topk_w, int32_t* cnt,
                                int32_t* rank, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
-                               int32_t* row_of_slot) {
+                               int32_t* row_of_slot, const int32_t* anchor, uint32_t* status) {
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(topk_plan_kernel<NI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
@@ -536,25 +602,29 @@ static int launch_topk_plan_ni(int nb, int E, size_t smem, cudaStream_t st, cons
   }
   if (nb == 1)
     return launch_pdl(topk_plan_kernel<NI, true>, dim3(1), dim3(512), smem, st, score, key, dead, T, E, k, topk_idx,
-                      topk_w, cnt, rank, counts, offsets, slot_of_row, row_of_slot);
-  // many blocks: selection spread over the whole GPU, then the per-block plan
+                      topk_w, cnt, rank, counts, offsets, slot_of_row, row_of_slot, anchor, status);
+  // many blocks: selection spread over the whole GPU (anchored rows next), then the per-block plan
   const int sel_blocks = (int)std::min<long long>(((long long)T + 7) / 8, (long long)num_sms() * 8);
   int rc = launch_pdl(topk_select_kernel<NI>, dim3(sel_blocks), dim3(256), 0, st, score, key, T, E, k, topk_idx,
-                      topk_w);
+                      topk_w, anchor, status);
   if (rc) return rc;
+  if (anchor) {
+    rc = launch_pdl(anchor_fixup_kernel, dim3(sel_blocks), dim3(256), 0, st, score, T, E, k, anchor, topk_idx, topk_w);
+    if (rc) return rc;
+  }
   return launch_pdl(topk_plan_kernel<NI, false>, dim3(nb), dim3(512), smem, st, score, key, dead, T, E, k, topk_idx,
-                    topk_w, cnt, rank, counts, offsets, slot_of_row, row_of_slot);
+                    topk_w, cnt, rank, counts, offsets, slot_of_row, row_of_slot, nullptr, nullptr);
 }
 
 // NI = experts per lane, the smallest power of two with 32 * NI >= E.
 static int launch_topk_plan(int nb, int E, size_t smem, cudaStream_t st, const float* score, const float* key,
                             const uint8_t* dead, int T, int k, int32_t* topk_idx, float* topk_w, int32_t* cnt,
                             int32_t* rank, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
-                            int32_t* row_of_slot) {
+                            int32_t* row_of_slot, const int32_t* anchor, uint32_t* status) {
 #define MOE_TOPK_CASE(N)                                                                                        \
   if (E <= 32 * N)                                                                                              \
     return launch_topk_plan_ni<N>(nb, E, smem, st, score, key, dead, T, k, topk_idx, topk_w, cnt, rank, counts, \
-                                  offsets, slot_of_row, row_of_slot);
+                                  offsets, slot_of_row, row_of_slot, anchor, status);
   MOE_TOPK_CASE(1)
   MOE_TOPK_CASE(2)
   MOE_TOPK_CASE(4)
@@ -579,7 +649,7 @@ static int launch_topk_single_plain_ni(size_t smem, cudaStream_t st, const float
     attr_set = true;
   }
   topk_plan_kernel<NI, true><<<1, 512, smem, st>>>(score, key, dead, T, E, k, topk_idx, topk_w, nullptr, nullptr,
-                                                   counts, offsets, slot_of_row, row_of_slot);
+                                                   counts, offsets, slot_of_row, row_of_slot, nullptr, nullptr);
   return launch_status();
 }
 
@@ -602,7 +672,8 @@ static int launch_topk_single_plain(int E, size_t smem, cudaStream_t st, const f
 
 int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, const uint8_t* dead,
                  int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
-                 int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done) {
+                 int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done,
+                 const int32_t* anchor) {
   if (quant_done) *quant_done = false;
   const Workspace L = workspace_layout(s);
   const int T = s->T, E = s->E, k = s->k, H = s->H;
@@ -632,7 +703,7 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
   } else if (T <= kSmallT) {
     rc0 = launch_pdl(router_small_kernel, dim3(ceil_div(E, 8)), dim3(256), 0, st, x, wr, bias, T, H, E, score, key);
   } else if (router_screen_supported(s)) {
-    rc0 = launch_router_screen(s, x, wr, bias, ws, score, key, st);
+    rc0 = launch_router_screen(s, x, wr, bias, ws, score, key, st, anchor);
   } else {
     rc0 = launch_pdl(router_tiled_kernel, dim3(ceil_div(T, 64), ceil_div(E, 64)), dim3(256), 0, st, x, wr, bias, T,
                      H, E, score, key);
@@ -645,7 +716,7 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
   int32_t* base = ws_ptr<int32_t>(ws, L.base);
   int32_t* rank = ws_ptr<int32_t>(ws, L.rank);
   rc = launch_topk_plan(nb, E, smem, st, score, key, dead, T, k, topk_idx, topk_w, cnt, rank, counts, offsets,
-                        slot_of_row, row_of_slot);
+                        slot_of_row, row_of_slot, anchor, ws_ptr<uint32_t>(ws, L.status));
   if (rc || nb == 1) return rc;
   rc = launch_pdl(plan_scan_kernel, dim3(1), dim3(512), 0, st, cnt, nb, E, base, counts, offsets);
   if (rc) return rc;
@@ -706,7 +777,17 @@ extern "C" int moe_route_topk(const moe_shape* s, const uint16_t* x, const uint1
                               const uint8_t* dead, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
                               int32_t* expert_offsets, int32_t* slot_of_row, int32_t* row_of_slot, void* ws,
                               size_t ws_bytes, void* stream) {
+  return moe_route_topk_anchored(s, x, w_router, bias, dead, nullptr, topk_idx, topk_w, expert_counts,
+                                 expert_offsets, slot_of_row, row_of_slot, ws, ws_bytes, stream);
+}
+
+extern "C" int moe_route_topk_anchored(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
+                                       const float* bias, const uint8_t* dead, const int32_t* anchor,
+                                       int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                                       int32_t* expert_offsets, int32_t* slot_of_row, int32_t* row_of_slot, void* ws,
+                                       size_t ws_bytes, void* stream) {
   if (!s) return MOE_ERR_INVALID_ARG;
+  if (anchor && (reinterpret_cast<uintptr_t>(anchor) & 3)) return MOE_ERR_INVALID_ARG;
   if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!expert_counts || !expert_offsets) return MOE_ERR_INVALID_ARG;
   if (s->T > 0 && (!x || !w_router || !bias || !topk_idx || !topk_w || !slot_of_row || !row_of_slot))
@@ -716,7 +797,7 @@ extern "C" int moe_route_topk(const moe_shape* s, const uint16_t* x, const uint1
   int rc = ws_check(s, ws, ws_bytes);
   if (rc) return rc;
   return launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, expert_counts, expert_offsets, slot_of_row,
-                      row_of_slot, ws, static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr);
+                      row_of_slot, ws, static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, anchor);
 }
 
 // ---------------------------------------------------------------------------------------------

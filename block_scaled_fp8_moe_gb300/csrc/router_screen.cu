@@ -79,6 +79,7 @@ struct ScreenParams {
   int32_t* cand;         // [T, kCandMax]
   int32_t* ncand;        // [T]; -1 = too many candidates, recompute every expert
   uint32_t* status;
+  const int32_t* anchor; // [T] or null: anchored rows need their own exact score of every expert
 };
 
 // Epilogue layout: 16 warps, four per TMEM lane quarter; warp group g (0..3) of a quarter takes
@@ -265,7 +266,14 @@ __global__ void __launch_bounds__(kScrThreads, 1) router_screen_kernel(const __g
     named_bar_sync(1, 32 * kScrEpiWarps);
     if (g == 0 && tok < p.T) {
       const int n = cnt_s[tl];
-      p.ncand[tok] = (!ok || n > kCandMax) ? -1 : n;
+      // an anchored row is weighted by its own scores of its anchor's experts, which the screen
+      // may have pruned: such rows recompute every expert exactly
+      bool anchored = false;
+      if (p.anchor) {
+        const int a = p.anchor[tok];
+        anchored = a >= 0 && a < p.T && p.anchor[a] == -1;
+      }
+      p.ncand[tok] = (!ok || n > kCandMax || anchored) ? -1 : n;
     }
   }
   tc_fence_before();
@@ -480,7 +488,7 @@ static int make_bf16_tmap(CUtensorMap* m, const uint16_t* base, int cols, int ro
 }
 
 int launch_router_screen(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, void* ws,
-                         float* score, float* key, cudaStream_t st) {
+                         float* score, float* key, cudaStream_t st, const int32_t* anchor) {
   const Workspace L = workspace_layout(s);
   const int T = s->T, H = s->H, E = s->E;
   float* xnorm = ws_ptr<float>(ws, L.xnorm);
@@ -503,6 +511,7 @@ int launch_router_screen(const moe_shape* s, const uint16_t* x, const uint16_t* 
   sp.cand = cand;
   sp.ncand = ncand;
   sp.status = ws_ptr<uint32_t>(ws, L.status);
+  sp.anchor = anchor;
   CUtensorMap tmx, tmw;
   rc = make_bf16_tmap(&tmx, x, H, T, kScrRows);
   if (rc) return rc;

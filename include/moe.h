@@ -179,6 +179,26 @@ MOE_API int moe_forward(const moe_shape* shape, const uint16_t* x, const uint16_
                 const uint8_t* w2_s, uint16_t* out, const moe_intermediates* inter, void* ws,
                 size_t ws_bytes, void* stream);
 
+/* Anchored verify rows (TP4 serving profile README, settings table row "Verify length": verify
+ * rows that the confidence head does not expect to survive reuse the anchor row's experts inside
+ * the router, so they read no extra expert weights).
+ *   anchor  i32 [T] or NULL: -1 = the row routes itself; a in [0, T) = the row takes row a's
+ *           experts (in a's rank order) and weights them with its own scores,
+ *           w_j = score[t, e_j] / ((score[t, e_0] + score[t, e_1]) + ...). Row a must route itself.
+ * An anchor outside [0, T) or pointing at an anchored row is ignored (that row routes itself) and
+ * recorded in the workspace status word (moe_check_device_status then returns MOE_ERR_TIMEOUT, the
+ * generic device-side error). Otherwise identical to moe_route_topk / moe_forward, which are these
+ * calls with anchor = NULL. anchor must be 4-byte aligned. */
+MOE_API int moe_route_topk_anchored(const moe_shape* shape, const uint16_t* x, const uint16_t* w_router,
+                                    const float* bias, const uint8_t* dead, const int32_t* anchor,
+                                    int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                                    int32_t* expert_offsets, int32_t* slot_of_row, int32_t* row_of_slot, void* ws,
+                                    size_t ws_bytes, void* stream);
+MOE_API int moe_forward_anchored(const moe_shape* shape, const uint16_t* x, const uint16_t* w_router,
+                                 const float* bias, const uint8_t* dead, const int32_t* anchor, const uint8_t* w13,
+                                 const uint8_t* w13_s, const uint8_t* w2, const uint8_t* w2_s, uint16_t* out,
+                                 const moe_intermediates* inter, void* ws, size_t ws_bytes, void* stream);
+
 /* Test hook for the bounded waits: launches one thread that waits on a barrier nothing arrives at,
  * for limit_ns (<= 2 s). The wait expires, writes its code into the status word at the start of
  * `ws` and the kernel returns; moe_check_device_status then reports MOE_ERR_TIMEOUT. No fault, no

@@ -114,13 +114,39 @@ def topk_select(key: np.ndarray, k: int) -> np.ndarray:
     return out
 
 
+def check_anchors(anchor, t_: int) -> np.ndarray | None:
+    """anchor[t] = -1 (route row t itself) or the index a of a row routed by itself (anchor[a] = -1).
+    TP4 serving profile README ("DeepSeek-V4.1-Flash-4x-DGX-Spark-TP4"), settings table row
+    "Verify length": verify rows the confidence head does not expect to survive reuse the anchor
+    row's experts inside the router, so they read no extra expert weights."""
+    if anchor is None:
+        return None
+    a = np.asarray(anchor, dtype=np.int64)
+    if a.shape != (t_,):
+        raise ValueError("anchor must have one entry per row")
+    bad = (a < -1) | (a >= t_)
+    if np.any(bad):
+        raise ValueError("anchor index out of range")
+    ref = a[a >= 0]
+    if np.any(a[ref] != -1):
+        raise ValueError("an anchor row must route itself")
+    return a
+
+
 def route(x: np.ndarray, wr: np.ndarray, bias: np.ndarray, k: int,
-          dead: np.ndarray | None = None) -> Routing:
+          dead: np.ndarray | None = None, anchor: np.ndarray | None = None) -> Routing:
+    """Top-k sigmoid gating; rows with anchor[t] = a >= 0 take row a's experts (in a's rank order)
+    and weight them with their own scores: w_j = score[t, e_j] / ((score[t, e_0] + ...) + ...)."""
     logits = router_logits(x, wr)
     score = sigmoid_f32(logits)
     key = (score + np.asarray(bias, dtype=np.float32)[None, :]).astype(np.float32)
     idx = topk_select(key, k)
     t_, e_ = key.shape
+    a = check_anchors(anchor, t_)
+    if a is not None:
+        for t in range(t_):
+            if a[t] >= 0:
+                idx[t] = idx[a[t]]
     sel = np.take_along_axis(score, idx, axis=1)               # fp32 [T, k], rank order
     total = np.zeros(t_, dtype=np.float32)
     for j in range(k):
@@ -309,12 +335,12 @@ class ForwardResult:
 
 
 def forward(x, wr, bias, k, w13: ExpertWeights, w2: ExpertWeights, inter: int,
-            dead=None, tokens=None) -> ForwardResult:
+            dead=None, tokens=None, anchor=None) -> ForwardResult:
     """The whole layer. With `tokens`, only those output rows (and their slots) are computed;
     routing and quantisation of every row are still computed (they are cheap and row-local)."""
     x = np.asarray(x, dtype=np.float32)
     t_, h_ = x.shape
-    routing = route(x, wr, bias, k, dead)
+    routing = route(x, wr, bias, k, dead, anchor)
     xq, xs = quant_mxfp8(x)
     tokens = np.arange(t_) if tokens is None else np.asarray(tokens)
     rows = []

@@ -227,6 +227,33 @@ class ExpertWeights:
         return self._cache[e]
 
 
+class DenseWeights:
+    """One dense MXFP8 projection (the shared expert): codes u8 [R, K] E4M3 and scales u8 [R, K/32],
+    presented like a one-expert ExpertWeights (index 0)."""
+
+    def __init__(self, codes: np.ndarray, scales: np.ndarray):
+        self.codes = np.asarray(codes)[None]
+        self.scales = np.asarray(scales)[None]
+        self._dec = None
+
+    def __getitem__(self, e: int) -> np.ndarray:
+        if e != 0:
+            raise IndexError("a dense projection has one expert")
+        if self._dec is None:
+            self._dec = decode_mxfp8(self.codes[0], self.scales[0])
+        return self._dec
+
+
+@dataclass
+class SharedExpert:
+    """TP4 serving profile README, "Rank-0 decode profile" table (shared expert on a side stream) and
+    settings row DSV41_SHARED_PAD_K (the shared expert runs on an MXFP8 kernel): one dense SwiGLU
+    expert every live row passes through, weight 1, added after the routed slots."""
+    w13: DenseWeights          # [2 I_s, H]: rows 0..I_s-1 gate, I_s..2 I_s-1 up
+    w2: DenseWeights           # [H, I_s]
+    inter: int                 # I_s
+
+
 @dataclass
 class W13Result:
     a: np.ndarray              # float64 [S, I]  pre-requant SwiGLU, plan order
@@ -302,9 +329,10 @@ def w2_slots(hq: np.ndarray, hs: np.ndarray, w2: ExpertWeights, routing: Routing
     return y
 
 
-def combine_exact(y_by_slot: dict[int, np.ndarray], t_: int, k: int, h_: int, tokens) -> np.ndarray:
+def combine_exact(y_by_slot: dict[int, np.ndarray], t_: int, k: int, h_: int, tokens,
+                  y_shared: dict[int, np.ndarray] | None = None) -> np.ndarray:
     """((y_0 + y_1) + ...) in float64 for the given tokens, before the output rounding; absent
-    slots (dead) give 0."""
+    slots (dead) give 0. A shared-expert row, when given, is added after the routed slots."""
     out = np.zeros((len(tokens), h_), dtype=np.float64)
     for n, t in enumerate(tokens):
         acc = np.zeros(h_, dtype=np.float64)
@@ -314,6 +342,8 @@ def combine_exact(y_by_slot: dict[int, np.ndarray], t_: int, k: int, h_: int, to
             if yj is not None:
                 acc = acc + yj
                 live = True
+        if live and y_shared is not None and int(t) in y_shared:
+            acc = acc + y_shared[int(t)]
         out[n] = acc if live else 0.0
     return out
 
@@ -321,6 +351,20 @@ def combine_exact(y_by_slot: dict[int, np.ndarray], t_: int, k: int, h_: int, to
 def combine(y_by_slot: dict[int, np.ndarray], t_: int, k: int, h_: int, tokens) -> np.ndarray:
     """out[t] = bf16(((y_0 + y_1) + ...) ) for the given tokens; absent slots (dead) give +0."""
     return F.round_to_bf16(combine_exact(y_by_slot, t_, k, h_, tokens)) + 0.0   # + 0.0: -0.0 -> +0.0
+
+
+def shared_expert(xq: np.ndarray, xs: np.ndarray, shared: SharedExpert, tokens) -> tuple[W13Result, np.ndarray]:
+    """The shared expert for `tokens`: the same SwiGLU, requantisation and down projection as a
+    routed expert (one expert, every token, weight 1). Returns the W13 result (rows in `tokens`
+    order) and y float64 [len(tokens), H]."""
+    tokens = np.asarray(tokens, dtype=np.int64)
+    t_ = len(tokens)
+    ident = Routing(None, None, None, np.zeros((t_, 1), np.int32), np.ones((t_, 1), np.float32),
+                    np.array([t_], np.int32), np.array([0, t_], np.int32), np.arange(t_, dtype=np.int32),
+                    np.arange(t_, dtype=np.int32))
+    r13 = w13_swiglu(xq[tokens], xs[tokens], shared.w13, ident, 1, shared.inter)
+    y = w2_slots(r13.hq, r13.hs, shared.w2, ident, 1)
+    return r13, y
 
 
 @dataclass
@@ -335,7 +379,7 @@ class ForwardResult:
 
 
 def forward(x, wr, bias, k, w13: ExpertWeights, w2: ExpertWeights, inter: int,
-            dead=None, tokens=None, anchor=None) -> ForwardResult:
+            dead=None, tokens=None, anchor=None, shared: SharedExpert | None = None) -> ForwardResult:
     """The whole layer. With `tokens`, only those output rows (and their slots) are computed;
     routing and quantisation of every row are still computed (they are cheap and row-local)."""
     x = np.asarray(x, dtype=np.float32)
@@ -353,7 +397,14 @@ def forward(x, wr, bias, k, w13: ExpertWeights, w2: ExpertWeights, inter: int,
     r13 = w13_swiglu(xq, xs, w13, routing, k, inter, rows)
     y = w2_slots(r13.hq, r13.hs, w2, routing, k, rows)
     y_by_slot = {int(routing.slot_of_row[p]): y[n] for n, p in enumerate(rows)}
-    out_exact = combine_exact(y_by_slot, t_, k, h_, tokens)
+    y_sh = None
+    if shared is not None:
+        live = np.ones(t_, bool) if dead is None else ~np.asarray(dead, bool)
+        toks = np.array([t for t in tokens if live[t]], dtype=np.int64)
+        if len(toks):
+            _, ys = shared_expert(xq, xs, shared, toks)
+            y_sh = {int(t): ys[n] for n, t in enumerate(toks)}
+    out_exact = combine_exact(y_by_slot, t_, k, h_, tokens, y_sh)
     out = F.round_to_bf16(out_exact) + 0.0
     r13_rows = r13
     r13_rows.rows = rows

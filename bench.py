@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--cpu-tokens", type=int, default=1)
     ap.add_argument("--tokens", type=int, default=0, help="override T of the workload (profiling aid)")
     ap.add_argument("--experts", type=int, default=0, help="override E of the workload (profiling aid)")
+    ap.add_argument("--shared-inter", type=int, default=0,
+                    help="add a dense MXFP8 shared expert of this intermediate size on a side stream")
     ap.add_argument("--record-traffic", default="", metavar="RAW_CSV",
                     help="store DRAM bytes per launch of the grouped GEMMs from `ncu -i REP --page raw --csv` "
                          "output into profiles/traffic.json for --config (stamped with the GEMM source hash)")
@@ -289,6 +291,21 @@ def gpu_arm(args):
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    shared = side_s = None
+    if args.shared_inter:
+        # synthetic shared expert: N(0, 0.02) weights -> bf16 -> MXFP8 by the library's quantiser
+        n_s = args.shared_inter
+        g = torch.Generator(device=dev)
+        g.manual_seed(cfg.seed + 1000)
+        q = []
+        for rows, cols in ((2 * n_s, cfg.H), (cfg.H, n_s)):
+            w = (torch.randn((rows, cols), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+            q.extend(B.moe_quant_mxfp8(w))
+        shared = B.SharedExpert(cfg.H, n_s, *q)
+        side_s = torch.cuda.Stream()
+
+    def fwd(xx, dd):
+        return layer.forward(xx, dead=dd, out=out, shared=shared, side_stream=side_s)
 
     def barrier():
         if world > 1:
@@ -296,7 +313,7 @@ def gpu_arm(args):
 
     # ---- warm-up ----
     for _ in range(args.warmup):
-        layer.forward(x, dead=dead, out=out)
+        fwd(x, dead)
     B.moe_check_device_status(ws)
     torch.cuda.synchronize()
 
@@ -310,7 +327,7 @@ def gpu_arm(args):
     for i in range(args.steps):
         flush.fill_(float(i))
         evs[i][0].record(stream)
-        layer.forward(x, dead=dead, out=out)
+        fwd(x, dead)
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -327,12 +344,12 @@ def gpu_arm(args):
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
-            layer.forward(x, dead=dead, out=out)
+            fwd(x, dead)
         stream.wait_stream(side)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            layer.forward(x, dead=dead, out=out)
+            fwd(x, dead)
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
@@ -415,7 +432,7 @@ def gpu_arm(args):
         x_dev.copy_(x_host, non_blocking=True)
         if dead_dev is not None:
             dead_dev.copy_(dead_host, non_blocking=True)
-        layer.forward(x_dev, dead=dead_dev, out=out)
+        fwd(x_dev, dead_dev)
         out_host.copy_(out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
@@ -438,8 +455,11 @@ def gpu_arm(args):
             "data": "synthetic (seeded; weights N(0,0.02) quantised to MXFP4 by the library)",
             "config": {"workload": workload_name(cfg), "l2": "flushed between timed steps (256 MiB write)",
                        "parallelism": f"replica per GPU x{world}", "touched_experts": touched,
-                       "live_slots": live_slots},
-            "e2e": e2e, "gpu_launches": launches_per_step(cfg) * args.steps, "clocks": clk,
+                       "live_slots": live_slots,
+                       **({"shared_expert_inter": args.shared_inter, "shared_expert": "MXFP8, side stream"}
+                          if args.shared_inter else {})},
+            "e2e": e2e, "gpu_launches": (launches_per_step(cfg) + (3 if args.shared_inter else 0)) * args.steps,
+            "clocks": clk,
             "roofline": roofline,
             "kernels_ms": {"w13": round(w13_ms, 5), "w2_combine": round(w2_ms, 5)},
             "graph_replay": ({"ms_per_step": round(graph_ms, 5),

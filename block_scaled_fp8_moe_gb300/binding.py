@@ -24,12 +24,20 @@ EXPORTED = [
     "moe_quant_mxfp4", "moe_pack_w13", "moe_pack_w2", "moe_route_topk", "moe_quant_mxfp8",
     "moe_w13_swiglu_grouped", "moe_w2_combine_grouped", "moe_forward", "moe_check_device_status",
     "moe_route_topk_noalloc", "moe_selftest_timeout", "moe_route_topk_anchored", "moe_forward_anchored",
+    "moe_packed_shared_w13_bytes", "moe_packed_shared_w2_bytes", "moe_pack_shared_w13", "moe_pack_shared_w2",
+    "moe_shared_workspace_bytes", "moe_forward_shared",
 ]
 
 
 class MoeShape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("k", ctypes.c_int32), ("I", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+class MoeSharedExpert(ctypes.Structure):
+    _fields_ = [("I", ctypes.c_int32), ("w13", ctypes.c_void_p), ("w13_s", ctypes.c_void_p),
+                ("w2", ctypes.c_void_p), ("w2_s", ctypes.c_void_p), ("ws", ctypes.c_void_p),
+                ("ws_bytes", ctypes.c_size_t)]
 
 
 class MoeIntermediates(ctypes.Structure):
@@ -63,8 +71,19 @@ lib.moe_route_topk_noalloc.argtypes = [_SHP] + [_P] * 10 + [_P]
 lib.moe_selftest_timeout.argtypes = [_P, ctypes.c_uint64, _P]
 lib.moe_route_topk_anchored.argtypes = [_SHP] + [_P] * 11 + [_P, _SZ, _P]
 lib.moe_forward_anchored.argtypes = [_SHP] + [_P] * 10 + [ctypes.POINTER(MoeIntermediates), _P, _SZ, _P]
+lib.moe_packed_shared_w13_bytes.restype = _SZ
+lib.moe_packed_shared_w13_bytes.argtypes = [_SHP, ctypes.POINTER(_SZ)]
+lib.moe_packed_shared_w2_bytes.restype = _SZ
+lib.moe_packed_shared_w2_bytes.argtypes = [_SHP, ctypes.POINTER(_SZ)]
+lib.moe_pack_shared_w13.argtypes = [_SHP, _P, _P, _P, _P, _P]
+lib.moe_pack_shared_w2.argtypes = [_SHP, _P, _P, _P, _P, _P]
+lib.moe_shared_workspace_bytes.restype = _SZ
+lib.moe_shared_workspace_bytes.argtypes = [_SHP, _I32]
+lib.moe_forward_shared.argtypes = ([_SHP] + [_P] * 9 + [ctypes.POINTER(MoeSharedExpert), _P,
+                                   ctypes.POINTER(MoeIntermediates), _P, _SZ, _P, _P])
 for _n in EXPORTED:
-    if _n not in ("moe_status_string", "moe_workspace_bytes", "moe_packed_w13_bytes", "moe_packed_w2_bytes"):
+    if _n not in ("moe_status_string", "moe_workspace_bytes", "moe_packed_w13_bytes", "moe_packed_w2_bytes",
+                  "moe_packed_shared_w13_bytes", "moe_packed_shared_w2_bytes", "moe_shared_workspace_bytes"):
         getattr(lib, _n).restype = ctypes.c_int
 
 
@@ -234,14 +253,59 @@ def moe_w2_combine_grouped(shp: MoeShape, hq, hs, w2p, w2sp, plan: Plan, ws, out
     return out
 
 
+class SharedExpert:
+    """A shared expert's packed MXFP8 weights on the device (canonical E4M3 codes and UE8M0 scales
+    in, see include/moe.h) and its per-T scratch."""
+
+    def __init__(self, H: int, I: int, q13, s13, q2, s2, stream=None):
+        self.H, self.I = H, I
+        dev = q13.device
+        shp = shape(1, H, 1, 1, I)
+        sb = ctypes.c_size_t(0)
+        n = lib.moe_packed_shared_w13_bytes(ctypes.byref(shp), ctypes.byref(sb))
+        if n == 0:
+            raise MoeError(MOE_ERR_UNSUPPORTED_SHAPE, "moe_packed_shared_w13_bytes")
+        self.w13p = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.w13sp = torch.empty(sb.value, dtype=torch.uint8, device=dev)
+        _check(lib.moe_pack_shared_w13(ctypes.byref(shp), _ptr(q13, torch.uint8, 2 * I * H), _ptr(s13, torch.uint8),
+                                       _ptr(self.w13p), _ptr(self.w13sp), _stream(stream)), "moe_pack_shared_w13")
+        n = lib.moe_packed_shared_w2_bytes(ctypes.byref(shp), ctypes.byref(sb))
+        self.w2p = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.w2sp = torch.empty(sb.value, dtype=torch.uint8, device=dev)
+        _check(lib.moe_pack_shared_w2(ctypes.byref(shp), _ptr(q2, torch.uint8, H * I), _ptr(s2, torch.uint8),
+                                      _ptr(self.w2p), _ptr(self.w2sp), _stream(stream)), "moe_pack_shared_w2")
+        self._ws = {}
+
+    def descriptor(self, shp: MoeShape) -> MoeSharedExpert:
+        if shp.T not in self._ws:
+            n = lib.moe_shared_workspace_bytes(ctypes.byref(shp), self.I)
+            if n == 0:
+                raise MoeError(MOE_ERR_UNSUPPORTED_SHAPE, "moe_shared_workspace_bytes")
+            self._ws[shp.T] = torch.empty(n, dtype=torch.uint8, device=self.w13p.device)
+        ws = self._ws[shp.T]
+        return MoeSharedExpert(self.I, self.w13p.data_ptr(), self.w13sp.data_ptr(), self.w2p.data_ptr(),
+                               self.w2sp.data_ptr(), ws.data_ptr(), ws.numel())
+
+
 def moe_forward(shp: MoeShape, x, w_router, bias, dead, w13p, w13sp, w2p, w2sp, ws, out=None,
-                inter: dict | None = None, stream=None, anchor=None):
+                inter: dict | None = None, stream=None, anchor=None, shared: SharedExpert | None = None,
+                side_stream=None):
     out = torch.empty(shp.T, shp.H, dtype=torch.bfloat16, device=x.device) if out is None else out
     im = None
     if inter:
         im = MoeIntermediates(*[ctypes.c_void_p(inter[n].data_ptr()) if inter.get(n) is not None else None
                                 for n, _ in MoeIntermediates._fields_])
-    if anchor is None:
+    if shared is not None:
+        desc = shared.descriptor(shp)
+        _check(lib.moe_forward_shared(
+            ctypes.byref(shp), _ptr(x, torch.bfloat16, shp.T * shp.H, "x"),
+            _ptr(w_router, torch.bfloat16, shp.E * shp.H, "w_router"), _ptr(bias, torch.float32, shp.E, "bias"),
+            _ptr(dead, torch.uint8, shp.T, "dead"), _ptr(anchor, torch.int32, shp.T, "anchor"),
+            _ptr(w13p, torch.uint8), _ptr(w13sp, torch.uint8), _ptr(w2p, torch.uint8), _ptr(w2sp, torch.uint8),
+            ctypes.byref(desc), _ptr(out, torch.bfloat16, shp.T * shp.H, "out"),
+            ctypes.byref(im) if im is not None else None, _ptr(ws), ws.numel(), _stream(stream),
+            _stream(side_stream) if side_stream is not None else None), "moe_forward_shared")
+    elif anchor is None:
         _check(lib.moe_forward(
             ctypes.byref(shp), _ptr(x, torch.bfloat16, shp.T * shp.H, "x"),
             _ptr(w_router, torch.bfloat16, shp.E * shp.H, "w_router"), _ptr(bias, torch.float32, shp.E, "bias"),
@@ -297,7 +361,8 @@ class MoeLayer:
             self._ws[T] = alloc_workspace(self.shape(T), self.w_router.device)
         return self._ws[T]
 
-    def forward(self, x, dead=None, out=None, inter=None, stream=None, anchor=None):
+    def forward(self, x, dead=None, out=None, inter=None, stream=None, anchor=None, shared=None, side_stream=None):
         T = x.shape[0]
         return moe_forward(self.shape(T), x, self.w_router, self.bias, dead, self.w13p, self.w13sp, self.w2p,
-                           self.w2sp, self.workspace(T), out=out, inter=inter, stream=stream, anchor=anchor)
+                           self.w2sp, self.workspace(T), out=out, inter=inter, stream=stream, anchor=anchor,
+                           shared=shared, side_stream=side_stream)

@@ -1,6 +1,8 @@
 // C-ABI entry points that compose the kernels: W13, W2 + combine, the whole layer, status.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 using namespace moe;
@@ -76,16 +78,59 @@ extern "C" int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t
                               stream);
 }
 
-extern "C" int moe_forward_anchored(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
-                                    const float* bias, const uint8_t* dead, const int32_t* anchor,
-                                    const uint8_t* w13, const uint8_t* w13_s, const uint8_t* w2, const uint8_t* w2_s,
-                                    uint16_t* out, const moe_intermediates* inter, void* ws, size_t ws_bytes,
-                                    void* stream) {
+namespace {
+
+// Shared-expert scratch: identity plan (one expert, row t = token t, weight 1) and the expert's
+// intermediates. Every piece 256-byte aligned.
+struct SharedWs {
+  size_t offsets, slot, ones, hq, hs, y, total;
+};
+
+SharedWs shared_layout(int T, int H, int Is) {
+  SharedWs w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + (bytes ? bytes : 1), 256); return o; };
+  w.offsets = take(2 * 4);
+  w.slot = take((size_t)T * 4);
+  w.ones = take((size_t)T * 4);
+  w.hq = take((size_t)T * Is);
+  w.hs = take((size_t)T * hs_pitch(Is));
+  w.y = take((size_t)T * H * 4);
+  w.total = off;
+  return w;
+}
+
+__global__ void shared_plan_kernel(int T, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
+                                   float* __restrict__ ones) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
+    slot[t] = t;
+    ones[t] = 1.0f;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    offsets[0] = 0;
+    offsets[1] = T;
+  }
+}
+
+int forward_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* bias,
+                 const uint8_t* dead, const int32_t* anchor, const uint8_t* w13, const uint8_t* w13_s,
+                 const uint8_t* w2, const uint8_t* w2_s, const moe_shared_expert* shared, uint16_t* out,
+                 const moe_intermediates* inter, void* ws, size_t ws_bytes, void* stream, void* side_stream) {
   if (!s) return MOE_ERR_INVALID_ARG;
   if (!aligned(anchor, 4)) return MOE_ERR_INVALID_ARG;
   if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
   int rc = ws_check(s, ws, ws_bytes);
   if (rc) return rc;
+  moe_shape ss{s->T, s->H, 1, 1, 0, 0};
+  if (shared) {
+    ss.I = shared->I;
+    if (!shape_ok(&ss)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!shared->ws || !aligned(shared->ws, 256) || shared->ws_bytes < shared_layout(s->T, s->H, ss.I).total)
+      return MOE_ERR_WORKSPACE;
+    if (!shared->w13 || !shared->w13_s || !shared->w2 || !shared->w2_s || !aligned(shared->w13, 32) ||
+        !aligned(shared->w2, 32) || !aligned(shared->w13_s, 16) || !aligned(shared->w2_s, 16))
+      return MOE_ERR_INVALID_ARG;
+  }
   if (s->T == 0) return MOE_OK;
   if (!x || !w_router || !bias || !w13 || !w13_s || !w2 || !w2_s || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(w13, 32) || !aligned(w2, 32) || !aligned(w13_s, 16) ||
@@ -122,10 +167,10 @@ extern "C" int moe_forward_anchored(const moe_shape* s, const uint16_t* x, const
   uint8_t* xqp = ws_ptr<uint8_t>(ws, L.xqp);
   uint8_t* xsp = ws_ptr<uint8_t>(ws, L.xsp);
   // wide-tile W13 reads the activations in plan order: quantise straight into it (token-order
-  // codes are written too only when the caller asked for them)
+  // codes are written too when the caller asked for them or the shared expert reads them)
   const bool plan_rows = !quant_done && w13_wants_plan_rows(s);
   if (plan_rows) {
-    const bool token_order = im.xq || im.xs;
+    const bool token_order = im.xq || im.xs || shared;
     rc = launch_quant_mxfp8_plan(s->T, s->H, s->k, x, token_order ? xq : nullptr, token_order ? xs : nullptr,
                                  row_of_slot, xqp, xsp, st);
     if (rc) return rc;
@@ -133,11 +178,79 @@ extern "C" int moe_forward_anchored(const moe_shape* s, const uint16_t* x, const
     rc = launch_quant_mxfp8(s->T, s->H, x, xq, xs, st);
     if (rc) return rc;
   }
+  // shared expert ("TP4 serving profile": on a side stream): one dense MXFP8 expert over every
+  // row, weight 1, with the same GEMM kernels (identity plan); joined before the combine
+  float* y_shared = nullptr;
+  cudaEvent_t ev_join = nullptr;
+  if (shared) {
+    const SharedWs SL = shared_layout(s->T, s->H, ss.I);
+    cudaStream_t side = side_stream ? static_cast<cudaStream_t>(side_stream) : st;
+    if (side != st) {
+      cudaEvent_t ev_fork = nullptr;
+      if (cudaEventCreateWithFlags(&ev_fork, cudaEventDisableTiming) != cudaSuccess) return MOE_ERR_CUDA;
+      const bool ok = cudaEventRecord(ev_fork, st) == cudaSuccess && cudaStreamWaitEvent(side, ev_fork, 0) == cudaSuccess;
+      cudaEventDestroy(ev_fork);
+      if (!ok) return MOE_ERR_CUDA;
+    }
+    int32_t* s_off = ws_ptr<int32_t>(shared->ws, SL.offsets);
+    int32_t* s_slot = ws_ptr<int32_t>(shared->ws, SL.slot);
+    float* s_ones = ws_ptr<float>(shared->ws, SL.ones);
+    uint8_t* s_hq = ws_ptr<uint8_t>(shared->ws, SL.hq);
+    uint8_t* s_hs = ws_ptr<uint8_t>(shared->ws, SL.hs);
+    y_shared = ws_ptr<float>(shared->ws, SL.y);
+    const int blocks = (int)std::min<long long>((s->T + 255) / 256, (long long)num_sms() * 4);
+    shared_plan_kernel<<<blocks, 256, 0, side>>>(s->T, s_off, s_slot, s_ones);
+    rc = launch_status();
+    if (rc) return rc;
+    rc = launch_w13(&ss, xq, xs, shared->w13, shared->w13_s, s_off, s_slot, s_hq, s_hs, nullptr, status, xq, xs,
+                    true, side, true);
+    if (rc) return rc;
+    rc = launch_w2(&ss, s_hq, s_hs, shared->w2, shared->w2_s, s_ones, s_off, s_slot, y_shared, status, side, true);
+    if (rc) return rc;
+    if (side != st) {
+      if (cudaEventCreateWithFlags(&ev_join, cudaEventDisableTiming) != cudaSuccess) return MOE_ERR_CUDA;
+      if (cudaEventRecord(ev_join, side) != cudaSuccess) {
+        cudaEventDestroy(ev_join);
+        return MOE_ERR_CUDA;
+      }
+    }
+  }
   rc = launch_w13(s, xq, xs, w13, w13_s, offsets, slot_of_row, hq, hs, im.swiglu, status, xqp, xsp, plan_rows, st);
+  if (!rc) rc = launch_w2(s, hq, hs, w2, w2_s, topk_w, offsets, slot_of_row, y, status, st);
+  if (ev_join) {
+    if (!rc && cudaStreamWaitEvent(st, ev_join, 0) != cudaSuccess) rc = MOE_ERR_CUDA;
+    cudaEventDestroy(ev_join);
+  }
   if (rc) return rc;
-  rc = launch_w2(s, hq, hs, w2, w2_s, topk_w, offsets, slot_of_row, y, status, st);
-  if (rc) return rc;
-  return launch_combine(s, y, row_of_slot, out, st);
+  return launch_combine(s, y, row_of_slot, out, st, y_shared);
+}
+
+}  // namespace
+
+extern "C" int moe_forward_anchored(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
+                                    const float* bias, const uint8_t* dead, const int32_t* anchor,
+                                    const uint8_t* w13, const uint8_t* w13_s, const uint8_t* w2, const uint8_t* w2_s,
+                                    uint16_t* out, const moe_intermediates* inter, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  return forward_impl(s, x, w_router, bias, dead, anchor, w13, w13_s, w2, w2_s, nullptr, out, inter, ws, ws_bytes,
+                      stream, nullptr);
+}
+
+extern "C" size_t moe_shared_workspace_bytes(const moe_shape* s, int32_t I_shared) {
+  if (!s || !shape_ok(s)) return 0;
+  moe_shape ss{s->T, s->H, 1, 1, I_shared, 0};
+  if (!shape_ok(&ss)) return 0;
+  return shared_layout(s->T, s->H, I_shared).total;
+}
+
+extern "C" int moe_forward_shared(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* bias,
+                                  const uint8_t* dead, const int32_t* anchor, const uint8_t* w13,
+                                  const uint8_t* w13_s, const uint8_t* w2, const uint8_t* w2_s,
+                                  const moe_shared_expert* shared, uint16_t* out, const moe_intermediates* inter,
+                                  void* ws, size_t ws_bytes, void* stream, void* side_stream) {
+  if (!shared) return MOE_ERR_INVALID_ARG;
+  return forward_impl(s, x, w_router, bias, dead, anchor, w13, w13_s, w2, w2_s, shared, out, inter, ws, ws_bytes,
+                      stream, side_stream);
 }
 
 extern "C" int moe_check_device_status(void* ws, void* stream) {

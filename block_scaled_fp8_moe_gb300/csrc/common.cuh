@@ -157,11 +157,14 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
                  const int32_t* anchor);
 int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
                const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
-               uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, bool plan_rows_ready, cudaStream_t st);
+               uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, bool plan_rows_ready, cudaStream_t st,
+               bool fp8_weights = false);
 int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2s,
               const float* topk_w, const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
-              cudaStream_t st);
-int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, uint16_t* out, cudaStream_t st);
+              cudaStream_t st, bool fp8_weights = false);
+// y_shared (nullable): a per-token row added after the routed slots (the shared expert)
+int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, uint16_t* out, cudaStream_t st,
+                   const float* y_shared = nullptr);
 // Large-T router: certified tensor-core screen + exact recompute of the surviving experts; writes
 // the same score/key rows as the exact router for every expert that can be selected.
 bool router_screen_supported(const moe_shape* s);

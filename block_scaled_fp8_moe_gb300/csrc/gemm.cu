@@ -58,6 +58,7 @@ struct GemmParams {
   int b_scale_pitch;        // bytes per scale row
   // A side (packed weights)
   const uint8_t* a_scales;  // packed 512-byte scale blocks
+  int a_fp8;                // 0: E2M1 codes (8 KB packed tiles, unpacked by the TMA); 1: E4M3 (16 KB tiles)
   // plan
   const int32_t* offsets;   // [E + 1]
   const int32_t* slot_of_row;
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
           uint8_t* sSFA = sA + L::kStageA + L::kStageB;
           // the box always moves KT tiles (past the panel: the next panel's tiles or TMA fill);
           // the scale copy stops at the panel's end
-          mbar_arrive_expect_tx(&full[stage], L::KT * kTileCodeBytes + nv * kTileScaleBytes +
+          mbar_arrive_expect_tx(&full[stage], L::KT * (p.a_fp8 ? 2 * kTileCodeBytes : kTileCodeBytes) + nv * kTileScaleBytes +
                                                   (kTmaB ? L::kStageB : 0));
           tma_load_2d(sA, &tmap_a, 0, (tile0 + kc0) * 128, &full[stage]);
           bulk_load(sSFA, p.a_scales + (size_t)(tile0 + kc0) * kTileScaleBytes, nv * kTileScaleBytes, &full[stage]);
@@ -368,7 +369,7 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it) {
         int e, m, nt, row0, nrows, tw;
         decode(w, e, m, nt, row0, nrows, tw);
-        const uint32_t idesc_base = idesc_mxf8f6f4(5 /*E2M1*/, 0 /*E4M3*/, 128, tw, 0, 0);
+        const uint32_t idesc_base = idesc_mxf8f6f4(p.a_fp8 ? 0 : 5 /*weights E4M3 or E2M1*/, 0 /*E4M3*/, 128, tw, 0, 0);
         const int acc = (NACC == 2) ? (it & 1) : 0;
         const int use = (NACC == 2) ? (it >> 1) : it;       // how many times this slot was used before
         if (use > 0 &&
@@ -593,6 +594,21 @@ static int make_weight_tmap(CUtensorMap* m, const uint8_t* codes, long long tile
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Packed E4M3 weight codes viewed as [tiles * 128 rows, 128 bytes]; one box covers `box_tiles`
+// consecutive tiles (the same 128-byte swizzled shared layout as the unpacked FP4 tiles).
+static int make_weight_tmap_fp8(CUtensorMap* m, const uint8_t* codes, long long tiles, int box_tiles) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return MOE_ERR_CUDA;
+  cuuint64_t gdim[2] = {128, (cuuint64_t)tiles * 128};
+  cuuint64_t gstride[1] = {128};
+  cuuint32_t box[2] = {128, (cuuint32_t)(128 * box_tiles)};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), gdim, gstride, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 // Activation codes viewed as [rows, row_bytes] bytes, 128-byte swizzled boxes of box_rows rows.
 static int make_act_tmap(CUtensorMap* m, const uint8_t* base, int row_bytes, long long rows, int box_rows) {
   EncodeTiledFn enc = get_encode();
@@ -648,7 +664,8 @@ static int launch_gemm(const moe_shape* s, const uint8_t* codes, const GemmParam
   if (!W13 && bn > 128 && gp.KC < 8) bn = 128;
   CUtensorMap tm;
   const int box_tiles = (bn <= 32) ? Smem<16>::KT : (bn <= 64 ? Smem<64>::KT : (bn == 128 ? Smem<128>::KT : Smem<MOE_WIDE_BN>::KT));
-  int rc0 = make_weight_tmap(&tm, codes, (long long)s->E * gp.MT * gp.KC, box_tiles);
+  int rc0 = gp.a_fp8 ? make_weight_tmap_fp8(&tm, codes, (long long)s->E * gp.MT * gp.KC, box_tiles)
+                     : make_weight_tmap(&tm, codes, (long long)s->E * gp.MT * gp.KC, box_tiles);
   if (rc0) return rc0;
   // activation operand of the wide token tile as a TMA tensor: [T*k plan rows, K] bytes, boxes of
   // bn plan rows (W13: the plan-order copy of xq; W2: hq)
@@ -696,9 +713,11 @@ bool w13_wants_plan_rows(const moe_shape* s) { return pick_bn(s) >= 128; }
 
 int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
                const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
-               uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, bool plan_rows_ready, cudaStream_t st) {
+               uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, bool plan_rows_ready, cudaStream_t st,
+               bool fp8_weights) {
   if (s->T == 0) return MOE_OK;
   GemmParams gp{};
+  gp.a_fp8 = fp8_weights ? 1 : 0;
   gp.bq = xq;
   gp.bs = xs;
   if (pick_bn(s) >= 128 && plan_rows_ready) {
@@ -736,9 +755,10 @@ int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const u
 
 int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2s,
               const float* topk_w, const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
-              cudaStream_t st) {
+              cudaStream_t st, bool fp8_weights) {
   if (s->T == 0) return MOE_OK;
   GemmParams gp{};
+  gp.a_fp8 = fp8_weights ? 1 : 0;
   gp.bq = hq;
   gp.bs = hs;
   gp.b_row_bytes = s->I;

@@ -83,15 +83,17 @@ __device__ __forceinline__ int pack_src_row(bool gate_up, int mt, int r, int I) 
   return gate_up ? (r < 64 ? 64 * mt + r : I + 64 * mt + (r - 64)) : 128 * mt + r;
 }
 
+// `chunk_bytes` = bytes of one row's 128-element K-chunk: 64 for E2M1 codes, 128 for E4M3 codes.
 __global__ void pack_codes_kernel(const uint8_t* __restrict__ q, uint8_t* __restrict__ qp, int E, int MT, int KC,
-                                  int rows_per_e, int K, int I, bool gate_up) {
-  // one thread per 16 packed bytes (32 elements)
-  const long long total = (long long)E * MT * KC * 128 * 4;
-  const int row_bytes = K / 2;
+                                  int rows_per_e, int K, int I, bool gate_up, int chunk_bytes) {
+  // one thread per 16 packed bytes
+  const int parts = chunk_bytes / 16;
+  const long long total = (long long)E * MT * KC * 128 * parts;
+  const int row_bytes = K * chunk_bytes / kTileK;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
-    int part = (int)(i & 3);
-    long long rr = i >> 2;
+    int part = (int)(i % parts);
+    long long rr = i / parts;
     int r = (int)(rr % 128);
     long long tile = rr / 128;
     int kc = (int)(tile % KC);
@@ -99,11 +101,11 @@ __global__ void pack_codes_kernel(const uint8_t* __restrict__ q, uint8_t* __rest
     int mt = (int)(em % MT);
     int e = (int)(em / MT);
     int src_row = pack_src_row(gate_up, mt, r, I);
-    int byte0 = kc * 64 + part * 16;
+    int byte0 = kc * chunk_bytes + part * 16;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (byte0 < row_bytes)
       v = *reinterpret_cast<const uint4*>(q + ((long long)e * rows_per_e + src_row) * row_bytes + byte0);
-    *reinterpret_cast<uint4*>(qp + tile * 8192 + r * 64 + part * 16) = v;
+    *reinterpret_cast<uint4*>(qp + tile * (128LL * chunk_bytes) + r * chunk_bytes + part * 16) = v;
   }
 }
 
@@ -244,7 +246,7 @@ extern "C" size_t moe_packed_w2_bytes(const moe_shape* sh, size_t* scale_bytes) 
 }
 
 static int pack_common(const moe_shape* sh, const uint8_t* q, const uint8_t* s, uint8_t* qp, uint8_t* sp,
-                       void* stream, bool gate_up) {
+                       void* stream, bool gate_up, int chunk_bytes = 64) {
   if (!sh || !q || !s || !qp || !sp) return MOE_ERR_INVALID_ARG;
   if (!shape_ok(sh)) return MOE_ERR_UNSUPPORTED_SHAPE;
   for (const void* p : {(const void*)q, (const void*)qp})
@@ -256,7 +258,7 @@ static int pack_common(const moe_shape* sh, const uint8_t* q, const uint8_t* s, 
   const int rows_per_e = gate_up ? 2 * sh->I : sh->H;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int blocks = num_sms() * 8;
-  pack_codes_kernel<<<blocks, 256, 0, st>>>(q, qp, E, MT, KC, rows_per_e, K, sh->I, gate_up);
+  pack_codes_kernel<<<blocks, 256, 0, st>>>(q, qp, E, MT, KC, rows_per_e, K, sh->I, gate_up, chunk_bytes);
   int rc = launch_status();
   if (rc) return rc;
   pack_scales_kernel<<<blocks, 256, 0, st>>>(s, sp, E, MT, KC, rows_per_e, K, sh->I, gate_up);
@@ -271,4 +273,34 @@ extern "C" int moe_pack_w13(const moe_shape* sh, const uint8_t* q, const uint8_t
 extern "C" int moe_pack_w2(const moe_shape* sh, const uint8_t* q, const uint8_t* s, uint8_t* qp, uint8_t* sp,
                            void* stream) {
   return pack_common(sh, q, s, qp, sp, stream, false);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Shared expert weights: dense MXFP8 (E4M3 codes, one byte per element), packed like the routed
+// experts' tiles with 128 bytes per row and K-chunk (16 KB of codes per tile).
+// ---------------------------------------------------------------------------------------------
+static bool shared_shape_ok(const moe_shape* sh) { return sh && shape_ok(sh) && sh->E == 1 && sh->k == 1; }
+
+extern "C" size_t moe_packed_shared_w13_bytes(const moe_shape* sh, size_t* scale_bytes) {
+  if (!shared_shape_ok(sh)) return 0;
+  return 2 * packed_bytes(1, sh->I / 64, sh->H / kTileK, scale_bytes);
+}
+
+extern "C" size_t moe_packed_shared_w2_bytes(const moe_shape* sh, size_t* scale_bytes) {
+  if (!shared_shape_ok(sh)) return 0;
+  return 2 * packed_bytes(1, sh->H / 128, ceil_div(sh->I, kTileK), scale_bytes);
+}
+
+extern "C" int moe_pack_shared_w13(const moe_shape* sh, const uint8_t* q, const uint8_t* s, uint8_t* qp,
+                                   uint8_t* sp, void* stream) {
+  if (!sh) return MOE_ERR_INVALID_ARG;
+  if (!shared_shape_ok(sh)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return pack_common(sh, q, s, qp, sp, stream, true, 128);
+}
+
+extern "C" int moe_pack_shared_w2(const moe_shape* sh, const uint8_t* q, const uint8_t* s, uint8_t* qp,
+                                  uint8_t* sp, void* stream) {
+  if (!sh) return MOE_ERR_INVALID_ARG;
+  if (!shared_shape_ok(sh)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return pack_common(sh, q, s, qp, sp, stream, false, 128);
 }

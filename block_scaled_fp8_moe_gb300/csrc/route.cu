@@ -727,11 +727,12 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
 }
 
 // ---------------------------------------------------------------------------------------------
-// Combine: out[t] = bf16_rne(((y[t,0] + y[t,1]) + ...) + y[t,k-1]) in fp32, slots in rank order;
-// rows without live slots get +0.0. 8 hidden elements per thread.
+// Combine: out[t] = bf16_rne(((y[t,0] + y[t,1]) + ...) + y[t,k-1]) in fp32, slots in rank order,
+// then + y_shared[t] when a shared expert ran; rows without live slots get +0.0. 8 hidden elements
+// per thread.
 // ---------------------------------------------------------------------------------------------
 __global__ void combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_of_slot, int T, int H,
-                               int k, uint16_t* __restrict__ out) {
+                               int k, uint16_t* __restrict__ out, const float* __restrict__ y_shared) {
   pdl_trigger();
   pdl_wait();
   const int H8 = H / 8;
@@ -750,6 +751,13 @@ __global__ void combine_kernel(const float* __restrict__ y, const int32_t* __res
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = (j == 0) ? v[q] : __fadd_rn(acc[q], v[q]);
       }
+      if (y_shared) {
+        const float4* yp = reinterpret_cast<const float4*>(y_shared + (size_t)t * H) + 2 * h8;
+        const float4 a = __ldg(yp), b = __ldg(yp + 1);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], v[q]);
+      }
     }
     uint32_t o[4];
 #pragma unroll
@@ -762,11 +770,12 @@ __global__ void combine_kernel(const float* __restrict__ y, const int32_t* __res
   }
 }
 
-int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, uint16_t* out, cudaStream_t st) {
+int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, uint16_t* out, cudaStream_t st,
+                   const float* y_shared) {
   const long long n = (long long)s->T * (s->H / 8);
   if (n == 0) return MOE_OK;
   const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);
-  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, st, y, row_of_slot, s->T, s->H, s->k, out);
+  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, st, y, row_of_slot, s->T, s->H, s->k, out, y_shared);
 }
 
 }  // namespace moe

@@ -199,6 +199,44 @@ MOE_API int moe_forward_anchored(const moe_shape* shape, const uint16_t* x, cons
                                  const uint8_t* w13_s, const uint8_t* w2, const uint8_t* w2_s, uint16_t* out,
                                  const moe_intermediates* inter, void* ws, size_t ws_bytes, void* stream);
 
+/* Shared expert (TP4 serving profile README: "Rank-0 decode profile" table, shared expert on a side
+ * stream; settings row DSV41_SHARED_PAD_K, the shared expert runs on an MXFP8 kernel): one dense
+ * SwiGLU expert every live row passes through beside the routed ones, with MXFP8 (E4M3 + UE8M0/32)
+ * weights, the same SwiGLU and MXFP8 requantisation as a routed expert, weight 1; its row is added
+ * after the routed slots: out[t] = bf16_rne((((y[t,0] + y[t,1]) + ...) + y[t,k-1]) + y_shared[t]).
+ * Dead rows stay +0.0.
+ * Shapes: the shared expert is described by moe_shape {T, H, E = 1, k = 1, I = I_shared}.
+ *  canonical codes  u8 [2 I_s, H] E4M3 (rows 0..I_s-1 gate, I_s..2I_s-1 up), scales u8 [2 I_s, H/32];
+ *                   u8 [H, I_s] / [H, I_s/32] for the down projection.
+ *  packed           tiles of 128 rows x 128 K elements, 16384 B of codes per tile (128 B per row),
+ *                   scale blocks as for the routed experts; gate/up interleave as W13 above. */
+typedef struct {
+  int32_t I;                                 /* shared intermediate size (I % 64 == 0)            */
+  const uint8_t* w13;                        /* packed by moe_pack_shared_w13                     */
+  const uint8_t* w13_s;
+  const uint8_t* w2;                         /* packed by moe_pack_shared_w2                      */
+  const uint8_t* w2_s;
+  void* ws;                                  /* moe_shared_workspace_bytes(shape, I), 256-B aligned */
+  size_t ws_bytes;
+} moe_shared_expert;
+
+MOE_API size_t moe_packed_shared_w13_bytes(const moe_shape* shared_shape, size_t* scale_bytes);
+MOE_API size_t moe_packed_shared_w2_bytes(const moe_shape* shared_shape, size_t* scale_bytes);
+MOE_API int moe_pack_shared_w13(const moe_shape* shared_shape, const uint8_t* q, const uint8_t* s,
+                                uint8_t* q_packed, uint8_t* s_packed, void* stream);
+MOE_API int moe_pack_shared_w2(const moe_shape* shared_shape, const uint8_t* q, const uint8_t* s,
+                               uint8_t* q_packed, uint8_t* s_packed, void* stream);
+/* Scratch of the shared expert for a layer of `shape` (T rows); 0 for an unsupported I_shared. */
+MOE_API size_t moe_shared_workspace_bytes(const moe_shape* shape, int32_t I_shared);
+/* moe_forward_anchored plus the shared expert. With side_stream non-NULL the shared expert's
+ * GEMMs run there, forked from `stream` after the activation quantisation and joined before the
+ * combine (events created and released inside the call); with NULL they run on `stream`. */
+MOE_API int moe_forward_shared(const moe_shape* shape, const uint16_t* x, const uint16_t* w_router,
+                               const float* bias, const uint8_t* dead, const int32_t* anchor, const uint8_t* w13,
+                               const uint8_t* w13_s, const uint8_t* w2, const uint8_t* w2_s,
+                               const moe_shared_expert* shared, uint16_t* out, const moe_intermediates* inter,
+                               void* ws, size_t ws_bytes, void* stream, void* side_stream);
+
 /* Test hook for the bounded waits: launches one thread that waits on a barrier nothing arrives at,
  * for limit_ns (<= 2 s). The wait expires, writes its code into the status word at the start of
  * `ws` and the kernel returns; moe_check_device_status then reports MOE_ERR_TIMEOUT. No fault, no

@@ -49,9 +49,9 @@ class GpuLayer:
     def shape(self, T=None, flags=0):
         return self.layer.shape(self.cfg.T if T is None else T, flags)
 
-    def forward(self, x=None, dead=None, inter=None, anchor=None):
+    def forward(self, x=None, dead=None, inter=None, anchor=None, shared=None, side_stream=None):
         x = self.x if x is None else x
-        return self.layer.forward(x, dead=dead, inter=inter, anchor=anchor)
+        return self.layer.forward(x, dead=dead, inter=inter, anchor=anchor, shared=shared, side_stream=side_stream)
 
     def run_steps(self, use_dead=True):
         """Route -> quant -> W13 (debug on) -> W2+combine through the four step entry points."""
@@ -70,7 +70,7 @@ class GpuLayer:
         return dict(plan=plan, xq=xq, xs=xs, hq=hq, hs=hs, dbg=dbg, out=out)
 
 
-def oracle_forward(inp: synth.MoeInputs, tokens=None, w13=None, w2=None, use_dead=True, anchor=None):
+def oracle_forward(inp: synth.MoeInputs, tokens=None, w13=None, w2=None, use_dead=True, anchor=None, shared=None):
     cfg = inp.cfg
     x = bf16_to_np(inp.x)
     wr = bf16_to_np(inp.w_router)
@@ -82,7 +82,8 @@ def oracle_forward(inp: synth.MoeInputs, tokens=None, w13=None, w2=None, use_dea
         used = sorted(set(r.topk_idx.reshape(-1).tolist()))
         w13 = oracle_weights(inp.w13, used) if w13 is None else w13
         w2 = oracle_weights(inp.w2, used) if w2 is None else w2
-    return M.forward(x, wr, bias, cfg.k, w13, w2, cfg.I, dead=dead, tokens=tokens, anchor=anchor), w13, w2
+    return (M.forward(x, wr, bias, cfg.k, w13, w2, cfg.I, dead=dead, tokens=tokens, anchor=anchor, shared=shared),
+            w13, w2)
 
 
 def assert_out_close(got: np.ndarray, ref_exact: np.ndarray, rel=OUT_REL_RMS):

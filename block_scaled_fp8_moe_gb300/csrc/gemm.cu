@@ -41,6 +41,9 @@ namespace moe {
 #ifndef MOE_WIDE_BN
 #define MOE_WIDE_BN 224             // widest token tile (MMA N) of the prefill path
 #endif
+#ifndef MOE_WIDE_STAGES
+#define MOE_WIDE_STAGES 4           // pipeline stages (one K-chunk each) of the widest tiles
+#endif
 // 4 producer/MMA warps + 4 epilogue warps; wide token tiles take 8 epilogue warps (two per TMEM
 // lane quarter, splitting the tile's columns), since their epilogue, not the MMA, sets the pace.
 template <int BN>
@@ -100,7 +103,8 @@ struct Smem {
   static constexpr int kSfbChunk = 512 * ((BN + 127) / 128);     // B scale atoms of one K-chunk
   static constexpr int kSfChunk = 512 + kSfbChunk;
   static constexpr int kStageBytes = (int)((kStageA + kStageB + KT * kSfChunk + 1023) / 1024 * 1024);
-  static constexpr int kStages = (BN <= 32) ? MOE_DEC_STAGES : (BN <= 64 ? 3 : (BN == 128 ? 6 / MOE_KT_WIDE : 4));
+  static constexpr int kStages =
+      (BN <= 32) ? MOE_DEC_STAGES : (BN <= 64 ? 3 : (BN == 128 ? 6 / MOE_KT_WIDE : MOE_WIDE_STAGES));
   static constexpr int kCtasPerSm = (BN <= 32) ? MOE_DEC_CTAS : (BN <= 64 ? 2 : 1);
   // TMEM: two accumulator slots of kAccStride columns, then the ring of scale blocks (one slot of
   // kSfSlot columns per K-chunk in flight: 4 for A, 4 per 128 token rows for B); the allocation is

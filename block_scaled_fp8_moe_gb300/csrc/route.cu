@@ -549,12 +549,15 @@ __global__ void __launch_bounds__(512) plan_scan_kernel(const int32_t* __restric
   pdl_wait();
   __shared__ int tot[kMaxE];
   __shared__ int total_s;
+  constexpr int U = 8;                            // block counts loaded per step (all in flight)
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
-    for (int b = 0; b < nb; ++b) {
-      const int c = cnt[(size_t)b * E + e];
-      base[(size_t)b * E + e] = run;
-      run += c;
+    for (int b0 = 0; b0 < nb; b0 += U) {
+      int c[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) c[j] = b0 + j < nb ? cnt[(size_t)(b0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < U; ++j) run += c[j];
     }
     tot[e] = run;
     counts[e] = run;
@@ -563,8 +566,20 @@ __global__ void __launch_bounds__(512) plan_scan_kernel(const int32_t* __restric
   block_exclusive_scan(tot, E, &total_s);
   for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = tot[e];
   if (threadIdx.x == 0) offsets[E] = total_s;
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    for (int b = 0; b < nb; ++b) base[(size_t)b * E + e] += tot[e];
+  // base[b][e] = offset of expert e + rows of e in blocks before b
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = tot[e];
+    for (int b0 = 0; b0 < nb; b0 += U) {
+      int c[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) c[j] = b0 + j < nb ? cnt[(size_t)(b0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        if (b0 + j < nb) base[(size_t)(b0 + j) * E + e] = run;
+        run += c[j];
+      }
+    }
+  }
 }
 
 // Multi-block plan, step 3: scatter every live slot to its plan row.

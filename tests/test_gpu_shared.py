@@ -70,3 +70,26 @@ def test_zero_shared_expert_is_no_shared_expert_and_rows_are_batch_invariant():
     for lo, hi in ((0, 1), (7, 40), (89, 90)):
         part = g.forward(x=g.x[lo:hi].contiguous(), shared=sh)
         assert torch.equal(part, full[lo:hi]), (lo, hi)
+
+
+def test_shared_expert_side_stream_captures_into_a_cuda_graph():
+    from block_scaled_fp8_moe_gb300 import binding as B
+    inp = synth.make_inputs_cpu(synth.custom("sh_graph", 24, 256, 8, 2, 128, seed=12))
+    g = H.GpuLayer(inp)
+    sh = _gpu_shared(B, 256, 192, _shared_codes(256, 192, seed=5))
+    side = torch.cuda.Stream()
+    out = torch.empty(24, 256, dtype=torch.bfloat16, device="cuda")
+    ref = g.forward(shared=sh, side_stream=side).clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g.layer.forward(g.x, out=out, shared=sh, side_stream=side)      # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.layer.forward(g.x, out=out, shared=sh, side_stream=side)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)

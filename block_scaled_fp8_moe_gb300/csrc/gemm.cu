@@ -82,10 +82,10 @@ struct GemmParams {
 #define MOE_DEC_KT 1                // K-chunks per stage, decode tiles (16 / 32 token rows)
 #endif
 #ifndef MOE_DEC_STAGES
-#define MOE_DEC_STAGES 3
+#define MOE_DEC_STAGES 2
 #endif
 #ifndef MOE_DEC_CTAS
-#define MOE_DEC_CTAS 3              // decode-tile CTAs per SM
+#define MOE_DEC_CTAS 4              // decode-tile CTAs per SM
 #endif
 
 __host__ __device__ constexpr int pow2_at_least(int v, int p) { return p >= v ? p : pow2_at_least(v, 2 * p); }
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
       tc_fence_after();
       const uint32_t d_tmem = tmem + (uint32_t)(acc * L::kAccStride);
       // TMEM is read kGrp 16-column chunks per round trip (one wait for several loads)
-      constexpr int kGrp = W13 ? 2 : (BN >= 64 ? 4 : BN / 16);
+      constexpr int kGrp = W13 ? (BN <= 32 ? 1 : 2) : (BN >= 64 ? 4 : BN / 16);
       for (int cg = 16 * kGrp * half; cg < tw; cg += 16 * kGrp * kHalves) {
         uint32_t rg[kGrp][16];
         if (ok) {

@@ -42,7 +42,10 @@ namespace moe {
 #define MOE_WIDE_BN 224             // widest token tile (MMA N) of the prefill path
 #endif
 #ifndef MOE_WIDE_STAGES
-#define MOE_WIDE_STAGES 4           // pipeline stages (one K-chunk each) of the widest tiles
+#define MOE_WIDE_STAGES 4           // pipeline stages of the widest tiles
+#endif
+#ifndef MOE_WIDE_KT
+#define MOE_WIDE_KT 1               // K-chunks per stage of the widest tiles
 #endif
 // 4 producer/MMA warps + 4 epilogue warps; wide token tiles take 8 epilogue warps (two per TMEM
 // lane quarter, splitting the tile's columns), since their epilogue, not the MMA, sets the pace.
@@ -60,6 +63,7 @@ struct GemmParams {
   int b_row_bytes;          // K in bytes (= elements)
   int b_scale_pitch;        // bytes per scale row
   // A side (packed weights)
+  const uint8_t* a_codes;   // packed tiles (the tensor map's memory), for L2 prefetch
   const uint8_t* a_scales;  // packed 512-byte scale blocks
   int a_fp8;                // 0: E2M1 codes (8 KB packed tiles, unpacked by the TMA); 1: E4M3 (16 KB tiles)
   // plan
@@ -87,6 +91,12 @@ struct GemmParams {
 #ifndef MOE_DEC_CTAS
 #define MOE_DEC_CTAS 4              // decode-tile CTAs per SM
 #endif
+#ifndef MOE_DEC_PF
+#define MOE_DEC_PF 2                // weight tiles prefetched into L2 ahead of the loads, decode tiles
+#endif
+#ifndef MOE_WIDE_PF
+#define MOE_WIDE_PF 0               // the same for 64-row and wider token tiles
+#endif
 
 __host__ __device__ constexpr int pow2_at_least(int v, int p) { return p >= v ? p : pow2_at_least(v, 2 * p); }
 
@@ -95,7 +105,7 @@ struct Smem {
   // A pipeline stage holds KT consecutive K-chunks (weight tiles) of 128: small token tiles are
   // weight-streaming bound and each stage hand-off costs a fixed few hundred ns per CTA, so they
   // move 16 KB of packed weights per TMA request.
-  static constexpr int KT = (BN <= 32) ? MOE_DEC_KT : (BN <= 64 ? 1 : (BN == 128 ? MOE_KT_WIDE : 1));
+  static constexpr int KT = (BN <= 32) ? MOE_DEC_KT : (BN <= 64 ? 1 : (BN == 128 ? MOE_KT_WIDE : MOE_WIDE_KT));
   static constexpr int kTileA = 16384;                           // one unpacked 128 x 128 FP4 tile
   static constexpr int kTileB = BN * 128;                        // BN rows x 128 FP8
   static constexpr int kStageA = KT * kTileA;
@@ -106,6 +116,10 @@ struct Smem {
   static constexpr int kStages =
       (BN <= 32) ? MOE_DEC_STAGES : (BN <= 64 ? 3 : (BN == 128 ? 6 / MOE_KT_WIDE : MOE_WIDE_STAGES));
   static constexpr int kCtasPerSm = (BN <= 32) ? MOE_DEC_CTAS : (BN <= 64 ? 2 : 1);
+  // the weight producer keeps kPrefetch K-chunks of its own upcoming tiles (codes and scales)
+  // requested into L2 beyond the stages in flight: more bytes in flight per SM than shared memory
+  // holds, so a stage's load finds its data in L2 instead of waiting a full DRAM round trip
+  static constexpr int kPrefetch = (BN <= 32) ? MOE_DEC_PF : MOE_WIDE_PF;
   // TMEM: two accumulator slots of kAccStride columns, then the ring of scale blocks (one slot of
   // kSfSlot columns per K-chunk in flight: 4 for A, 4 per 128 token rows for B); the allocation is
   // the next power of two, small enough for kCtasPerSm CTAs to share the SM's 512 columns
@@ -249,6 +263,31 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
       uint32_t phase = 0;
       bool ok = true;
       const int KC = p.KC;
+      const uint32_t tile_bytes = p.a_fp8 ? 2 * kTileCodeBytes : kTileCodeBytes;
+      // L2 prefetch cursor: walks this CTA's (item, K-chunk) sequence kPrefetch chunks ahead of
+      // the loads. It starts kPrefetch chunks in without prefetching: the first chunks are loaded
+      // at once, and a burst of prefetches for them would only queue ahead of those loads.
+      int pf_w = blockIdx.x, pf_kc = 0;
+      long long pf_tile0 = -1;
+      auto pf_step = [&](bool issue) {
+        if (pf_w >= total) return;
+        if (issue) {
+          if (pf_tile0 < 0) {
+            int e, m, nt, row0, nrows, tw;
+            decode(pf_w, e, m, nt, row0, nrows, tw);
+            pf_tile0 = (long long)(e * p.MT + m) * KC;
+          }
+          const long long g = pf_tile0 + pf_kc;
+          prefetch_l2_bulk(p.a_codes + g * tile_bytes, tile_bytes);
+          prefetch_l2_bulk(p.a_scales + g * kTileScaleBytes, kTileScaleBytes);
+        }
+        if (++pf_kc == KC) {
+          pf_kc = 0;
+          pf_w += gridDim.x;
+          pf_tile0 = -1;
+        }
+      };
+      for (int i = 0; i < L::kPrefetch; ++i) pf_step(false);
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         int e, m, nt, row0, nrows, tw;
         decode(w, e, m, nt, row0, nrows, tw);
@@ -267,6 +306,8 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
                                                   (kTmaB ? L::kStageB : 0));
           tma_load_2d(sA, &tmap_a, 0, (tile0 + kc0) * 128, &full[stage]);
           bulk_load(sSFA, p.a_scales + (size_t)(tile0 + kc0) * kTileScaleBytes, nv * kTileScaleBytes, &full[stage]);
+          if (L::kPrefetch > 0)
+            for (int j = 0; j < nv; ++j) pf_step(true);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
@@ -739,6 +780,7 @@ int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const u
   }
   gp.b_row_bytes = s->H;
   gp.b_scale_pitch = s->H / 32;
+  gp.a_codes = w13;
   gp.a_scales = w13s;
   gp.offsets = offsets;
   gp.slot_of_row = slot_of_row;
@@ -767,6 +809,7 @@ int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const ui
   gp.bs = hs;
   gp.b_row_bytes = s->I;
   gp.b_scale_pitch = hs_pitch(s->I);
+  gp.a_codes = w2;
   gp.a_scales = w2s;
   gp.offsets = offsets;
   gp.slot_of_row = slot_of_row;

@@ -277,15 +277,12 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const uint16_t* __res
 }
 
 // ---------------------------------------------------------------------------------------------
-// Top-k + in-block plan. One CTA per block of kPlanBlock tokens, 16 warps. Each warp routes its
-// tokens one at a time: k rounds of a warp arg-max over (key descending, expert ascending).
-// Then the CTA builds, per expert, a bitmask of the block's live tokens that chose it: the rank
-// of a slot inside its expert is the number of lower token bits set, so the plan order inside an
-// expert is token order, with no atomics whose order matters.
-// With a single block (T <= kPlanBlock) the same CTA also scans and scatters the plan.
+// Top-k + plan. Each warp routes its tokens one at a time: k rounds of a warp arg-max over
+// (key descending, expert ascending). A CTA then builds, per expert, a bitmask of its block's
+// live tokens that chose it: the rank of a slot inside its expert is the number of lower token
+// bits set, so the plan order inside an expert is token order, with no atomics whose order
+// matters. With a single block (T <= kPlanBlock) one CTA also scans and scatters the plan.
 // ---------------------------------------------------------------------------------------------
-constexpr int kTopkWarps = 16;
-
 
 __device__ void block_exclusive_scan(int* vals, int n, int* total) {
   // vals in shared memory, n <= 1024; blockDim.x == 512
@@ -308,6 +305,43 @@ __device__ void block_exclusive_scan(int* vals, int n, int* total) {
   __syncthreads();
 }
 
+// Exclusive scan of vals[0..n) in shared memory by the whole block (any multiple of 32 threads):
+// each thread sums a contiguous segment, a two-level warp scan gives the segment offsets, each
+// thread rewrites its segment. *total = the sum. wsum: 32 ints of shared scratch.
+__device__ void block_scan_segments(int* vals, int n, int* total, int* wsum) {
+  const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
+  const int c = (n + nt - 1) / nt;
+  const int b = min(n, tid * c), e = min(n, b + c);
+  int s = 0;
+  for (int i = b; i < e; ++i) s += vals[i];
+  int x = s;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) wsum[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    if (lane < nw) wsum[lane] = w;
+  }
+  __syncthreads();
+  int base = (wid > 0 ? wsum[wid - 1] : 0) + x - s;
+  for (int i = b; i < e; ++i) {
+    const int v = vals[i];
+    vals[i] = base;
+    base += v;
+  }
+  if (tid == 0) *total = wsum[nw - 1];
+  __syncthreads();
+}
+
 // Anchored verify rows (TP4 serving profile README, settings table row "Verify length"): a row
 // with anchor[t] = a reuses row a's experts (a routes itself) and weights them with its own scores,
 // so it reaches no expert its anchor does not. An anchor outside [0, T) or one that is itself
@@ -326,7 +360,7 @@ __device__ __forceinline__ int anchor_of(const int32_t* __restrict__ anchor, int
 // Lane j < k gets expert e (the anchor's j-th choice) and the row's weight score[e] / sum, the sum
 // taken in rank order (identical on every lane).
 __device__ __forceinline__ void anchored_weights(const float* __restrict__ srow, int e, int k, int lane, float* w) {
-  const float sc = lane < k ? srow[e] : 0.f;
+  const float sc = lane < k ? __ldcg(srow + e) : 0.f;
   float sum = 0.f;
   for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, sc, j));
   *w = __fdiv_rn(sc, sum);
@@ -343,8 +377,8 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ krow, const 
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int e = lane + 32 * i;
-    kv[i] = (e < E) ? krow[e] : 0.f;
-    sv[i] = (e < E) ? srow[e] : 0.f;
+    kv[i] = (e < E) ? __ldcg(krow + e) : 0.f;          // through L2: another CTA may have written them
+    sv[i] = (e < E) ? __ldcg(srow + e) : 0.f;
   }
   uint32_t taken = 0;
   auto local_best = [&](float& bk, int& be) {
@@ -429,68 +463,52 @@ __global__ void __launch_bounds__(256) anchor_fixup_kernel(const float* __restri
   }
 }
 
-// SELECT: this CTA routes its tokens (16 warps, one token at a time each); otherwise the choices
-// are read back from topk_idx (written by topk_select_kernel).
-template <int NI, bool SELECT>
-__global__ void __launch_bounds__(512) topk_plan_kernel(const float* __restrict__ score, const float* __restrict__ key,
-                                                        const uint8_t* __restrict__ dead, int T, int E, int k,
-                                                        int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                                                        int32_t* __restrict__ cnt, int32_t* __restrict__ rank,
-                                                        int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                                                        int32_t* __restrict__ slot_of_row,
-                                                        int32_t* __restrict__ row_of_slot,
-                                                        const int32_t* __restrict__ anchor, uint32_t* status) {
-  pdl_trigger();
-  pdl_wait();
-  extern __shared__ uint32_t dsm[];
-  uint32_t* mask = dsm;                                         // [E][8]
-  int16_t* sidx = reinterpret_cast<int16_t*>(dsm + E * 8);      // [kPlanBlock][k]
-  __shared__ int scnt[kMaxE];
-  __shared__ int total_s;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tb0 = blockIdx.x * kPlanBlock;
-  const int nt = min(kPlanBlock, T - tb0);
+// Top-k and the whole plan for T <= kPlanBlock rows in one CTA (any multiple of 32 threads, one
+// token per warp at a time): selection (self-routed rows, then anchored rows), per-expert token
+// bitmasks (plan order inside an expert = token order), counts, offsets, scatter.
+// Shared scratch: mask [E * 8] u32, sidx [kPlanBlock * k] i16, scnt [E] i32, wsum [32] i32, total.
+template <int NI>
+__device__ void plan_single_block(const float* __restrict__ score, const float* __restrict__ key,
+                                  const uint8_t* __restrict__ dead, int T, int E, int k, int32_t* __restrict__ topk_idx,
+                                  float* __restrict__ topk_w, int32_t* __restrict__ counts,
+                                  int32_t* __restrict__ offsets, int32_t* __restrict__ slot_of_row,
+                                  int32_t* __restrict__ row_of_slot, const int32_t* __restrict__ anchor,
+                                  uint32_t* status, uint32_t* mask, int16_t* sidx, int* scnt, int* wsum, int* total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   for (int i = threadIdx.x; i < E * 8; i += blockDim.x) mask[i] = 0;
-
-  if (SELECT) {
-    for (int tl = warp; tl < nt; tl += kTopkWarps) {
-      const int t = tb0 + tl;
-      if (anchor_of(anchor, t, T, status) >= 0) continue;    // after every self-routed row
-      int my_e = -1;
-      float my_s = 0.f, sum = 0.f;
-      warp_topk<NI>(key + (size_t)t * E, score + (size_t)t * E, E, k, lane, sidx + tl * k, &my_e, &my_s, &sum);
+  for (int t = warp; t < T; t += nwarps) {
+    if (anchor_of(anchor, t, T, status) >= 0) continue;      // after every self-routed row
+    int my_e = -1;
+    float my_s = 0.f, sum = 0.f;
+    warp_topk<NI>(key + (size_t)t * E, score + (size_t)t * E, E, k, lane, sidx + t * k, &my_e, &my_s, &sum);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = my_e;
+      topk_w[(size_t)t * k + lane] = __fdiv_rn(my_s, sum);
+    }
+  }
+  if (anchor) {
+    __syncthreads();
+    for (int t = warp; t < T; t += nwarps) {
+      const int a = anchor_of(anchor, t, T, nullptr);
+      if (a < 0) continue;
+      const int e = lane < k ? (int)sidx[a * k + lane] : 0;
+      float w;
+      anchored_weights(score + (size_t)t * E, e, k, lane, &w);
       if (lane < k) {
-        topk_idx[(size_t)t * k + lane] = my_e;
-        topk_w[(size_t)t * k + lane] = __fdiv_rn(my_s, sum);
+        topk_idx[(size_t)t * k + lane] = e;
+        topk_w[(size_t)t * k + lane] = w;
+        sidx[t * k + lane] = (int16_t)e;
       }
     }
-    if (anchor) {
-      // one block holds every row here (T <= kPlanBlock): the anchor's choices are in sidx
-      __syncthreads();
-      for (int tl = warp; tl < nt; tl += kTopkWarps) {
-        const int t = tb0 + tl;
-        const int a = anchor_of(anchor, t, T, nullptr);
-        if (a < 0) continue;
-        const int e = lane < k ? (int)sidx[(a - tb0) * k + lane] : 0;
-        float w;
-        anchored_weights(score + (size_t)t * E, e, k, lane, &w);
-        if (lane < k) {
-          topk_idx[(size_t)t * k + lane] = e;
-          topk_w[(size_t)t * k + lane] = w;
-          sidx[tl * k + lane] = (int16_t)e;
-        }
-      }
-    }
-  } else {
-    for (int i = threadIdx.x; i < nt * k; i += blockDim.x) sidx[i] = (int16_t)topk_idx[(size_t)tb0 * k + i];
   }
   __syncthreads();
-  // per-expert token bitmasks of this block (bit order = token order)
-  for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
-    const int tl = i / k;
-    if (dead && dead[tb0 + tl]) continue;
-    const int e = sidx[i];
-    atomicOr(&mask[e * 8 + (tl >> 5)], 1u << (tl & 31));
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    const int t = i / k;
+    if (dead && dead[t]) {
+      sidx[i] = -1;                                          // dead slot: no plan row
+      continue;
+    }
+    atomicOr(&mask[sidx[i] * 8 + (t >> 5)], 1u << (t & 31));
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -498,11 +516,86 @@ __global__ void __launch_bounds__(512) topk_plan_kernel(const float* __restrict_
 #pragma unroll
     for (int w = 0; w < 8; ++w) c += __popc(mask[e * 8 + w]);
     scnt[e] = c;
+    counts[e] = c;
   }
   __syncthreads();
-  const bool single = (gridDim.x == 1);
-  if (!single) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[(size_t)blockIdx.x * E + e] = scnt[e];
+  block_scan_segments(scnt, E, total, wsum);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = scnt[e];
+  if (threadIdx.x == 0) offsets[E] = *total;
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    const int t = i / k;
+    const int e = sidx[i];
+    if (e < 0) {
+      row_of_slot[i] = -1;
+      continue;
+    }
+    const int w = t >> 5;
+    int r = 0;
+    for (int q = 0; q < w; ++q) r += __popc(mask[e * 8 + q]);
+    r += __popc(mask[e * 8 + w] & ((1u << (t & 31)) - 1u));
+    const int p = scnt[e] + r;
+    slot_of_row[p] = i;
+    row_of_slot[i] = p;
+  }
+}
+
+inline size_t plan_single_smem(int E, int k) {
+  return align_up((size_t)E * 8 * 4, 16) + align_up((size_t)kPlanBlock * k * 2, 16) + align_up((size_t)E * 4, 16) +
+         32 * 4 + 16;
+}
+
+// T <= kPlanBlock: top-k and plan in one CTA.
+template <int NI>
+__global__ void __launch_bounds__(512) topk_plan_single_kernel(const float* __restrict__ score,
+                                                               const float* __restrict__ key,
+                                                               const uint8_t* __restrict__ dead, int T, int E, int k,
+                                                               int32_t* __restrict__ topk_idx,
+                                                               float* __restrict__ topk_w,
+                                                               int32_t* __restrict__ counts,
+                                                               int32_t* __restrict__ offsets,
+                                                               int32_t* __restrict__ slot_of_row,
+                                                               int32_t* __restrict__ row_of_slot,
+                                                               const int32_t* __restrict__ anchor, uint32_t* status) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(16) uint8_t psm[];
+  uint32_t* mask = reinterpret_cast<uint32_t*>(psm);
+  int16_t* sidx = reinterpret_cast<int16_t*>(psm + align_up((size_t)E * 8 * 4, 16));
+  int* scnt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(sidx) + align_up((size_t)kPlanBlock * k * 2, 16));
+  int* wsum = scnt + align_up((size_t)E * 4, 16) / 4;
+  int* total = wsum + 32;
+  plan_single_block<NI>(score, key, dead, T, E, k, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot,
+                        anchor, status, mask, sidx, scnt, wsum, total);
+}
+
+// Multi-block plan, step 1: one CTA per kPlanBlock tokens reads the choices from topk_idx (written
+// by topk_select_kernel / anchor_fixup_kernel) and writes its per-expert counts and each slot's
+// rank inside its expert (the number of lower token bits set in the block's bitmask).
+__global__ void __launch_bounds__(512) topk_plan_kernel(const uint8_t* __restrict__ dead, int T, int E, int k,
+                                                        const int32_t* __restrict__ topk_idx,
+                                                        int32_t* __restrict__ cnt, int32_t* __restrict__ rank) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ uint32_t dsm[];
+  uint32_t* mask = dsm;                                         // [E][8]
+  int16_t* sidx = reinterpret_cast<int16_t*>(dsm + E * 8);      // [kPlanBlock][k]
+  const int tb0 = blockIdx.x * kPlanBlock;
+  const int nt = min(kPlanBlock, T - tb0);
+  for (int i = threadIdx.x; i < E * 8; i += blockDim.x) mask[i] = 0;
+  for (int i = threadIdx.x; i < nt * k; i += blockDim.x) sidx[i] = (int16_t)topk_idx[(size_t)tb0 * k + i];
+  __syncthreads();
+  // per-expert token bitmasks of this block (bit order = token order)
+  for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
+    const int tl = i / k;
+    if (dead && dead[tb0 + tl]) continue;
+    atomicOr(&mask[sidx[i] * 8 + (tl >> 5)], 1u << (tl & 31));
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) c += __popc(mask[e * 8 + w]);
+    cnt[(size_t)blockIdx.x * E + e] = c;
   }
   for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
     const int tl = i / k;
@@ -515,29 +608,7 @@ __global__ void __launch_bounds__(512) topk_plan_kernel(const float* __restrict_
       for (int q = 0; q < w; ++q) r += __popc(mask[e * 8 + q]);
       r += __popc(mask[e * 8 + w] & ((1u << (tl & 31)) - 1u));
     }
-    if (!single) rank[(size_t)t * k + (i % k)] = r;
-    else if (r < 0) sidx[i] = -1;     // dead slot: no plan row
-  }
-  if (!single) return;
-  // single block: counts, offsets, scatter
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = scnt[e];
-  __syncthreads();
-  block_exclusive_scan(scnt, E, &total_s);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = scnt[e];
-  if (threadIdx.x == 0) offsets[E] = total_s;
-  for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
-    const int tl = i / k;
-    const int t = tb0 + tl;
-    const int e = sidx[i];
-    if (e < 0) { row_of_slot[(size_t)t * k + (i % k)] = -1; continue; }
-    const int w = tl >> 5;
-    int r = 0;
-    for (int q = 0; q < w; ++q) r += __popc(mask[e * 8 + q]);
-    r += __popc(mask[e * 8 + w] & ((1u << (tl & 31)) - 1u));
-    const int p = scnt[e] + r;
-    slot_of_row[p] = t * k + (i % k);
-    row_of_slot[(size_t)t * k + (i % k)] = p;
+    rank[(size_t)t * k + (i % k)] = r;
   }
 }
 
@@ -608,16 +679,15 @@ static int launch_topk_plan_ni(int nb, int E, size_t smem, cudaStream_t st, cons
                                int32_t* row_of_slot, const int32_t* anchor, uint32_t* status) {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(topk_plan_kernel<NI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
+    if (cudaFuncSetAttribute(topk_plan_single_kernel<NI>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(topk_plan_kernel<NI, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
-            cudaSuccess)
+        cudaFuncSetAttribute(topk_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) != cudaSuccess)
       return MOE_ERR_CUDA;
     attr_set = true;
   }
   if (nb == 1)
-    return launch_pdl(topk_plan_kernel<NI, true>, dim3(1), dim3(512), smem, st, score, key, dead, T, E, k, topk_idx,
-                      topk_w, cnt, rank, counts, offsets, slot_of_row, row_of_slot, anchor, status);
+    return launch_pdl(topk_plan_single_kernel<NI>, dim3(1), dim3(512), plan_single_smem(E, k), st, score, key, dead, T,
+                      E, k, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, anchor, status);
   // many blocks: selection spread over the whole GPU (anchored rows next), then the per-block plan
   const int sel_blocks = (int)std::min<long long>(((long long)T + 7) / 8, (long long)num_sms() * 8);
   int rc = launch_pdl(topk_select_kernel<NI>, dim3(sel_blocks), dim3(256), 0, st, score, key, T, E, k, topk_idx,
@@ -627,8 +697,8 @@ static int launch_topk_plan_ni(int nb, int E, size_t smem, cudaStream_t st, cons
     rc = launch_pdl(anchor_fixup_kernel, dim3(sel_blocks), dim3(256), 0, st, score, T, E, k, anchor, topk_idx, topk_w);
     if (rc) return rc;
   }
-  return launch_pdl(topk_plan_kernel<NI, false>, dim3(nb), dim3(512), smem, st, score, key, dead, T, E, k, topk_idx,
-                    topk_w, cnt, rank, counts, offsets, slot_of_row, row_of_slot, nullptr, nullptr);
+  return launch_pdl(topk_plan_kernel, dim3(nb), dim3(512), smem, st, dead, T, E, k, (const int32_t*)topk_idx, cnt,
+                    rank);
 }
 
 // NI = experts per lane, the smallest power of two with 32 * NI >= E.
@@ -656,15 +726,17 @@ static int launch_topk_single_plain_ni(size_t smem, cudaStream_t st, const float
                                        const uint8_t* dead, int T, int E, int k, int32_t* topk_idx, float* topk_w,
                                        int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
                                        int32_t* row_of_slot) {
+  (void)smem;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(topk_plan_kernel<NI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
+    if (cudaFuncSetAttribute(topk_plan_single_kernel<NI>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     attr_set = true;
   }
-  topk_plan_kernel<NI, true><<<1, 512, smem, st>>>(score, key, dead, T, E, k, topk_idx, topk_w, nullptr, nullptr,
-                                                   counts, offsets, slot_of_row, row_of_slot, nullptr, nullptr);
+  topk_plan_single_kernel<NI><<<1, 512, plan_single_smem(E, k), st>>>(score, key, dead, T, E, k, topk_idx, topk_w,
+                                                                       counts, offsets, slot_of_row, row_of_slot,
+                                                                       nullptr, nullptr);
   return launch_status();
 }
 

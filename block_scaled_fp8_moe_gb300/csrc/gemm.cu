@@ -42,10 +42,10 @@ namespace moe {
 #define MOE_WIDE_BN 224             // widest token tile (MMA N) of the prefill path
 #endif
 #ifndef MOE_WIDE_STAGES
-#define MOE_WIDE_STAGES 4           // pipeline stages of the widest tiles
+#define MOE_WIDE_STAGES 2           // pipeline stages of the widest tiles
 #endif
 #ifndef MOE_WIDE_KT
-#define MOE_WIDE_KT 1               // K-chunks per stage of the widest tiles
+#define MOE_WIDE_KT 2               // K-chunks per stage of the widest tiles
 #endif
 // 4 producer/MMA warps + 4 epilogue warps; wide token tiles take 8 epilogue warps (two per TMEM
 // lane quarter, splitting the tile's columns), since their epilogue, not the MMA, sets the pace.
@@ -519,22 +519,27 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
             // goes to shared memory as [column][feature]; then thread t owns column t / 8 and the
             // eight features 8 (t % 8) .. +7: SwiGLU, a four-thread amax per 32-block, and one
             // 8-byte store of codes.
+            // Feature f of a column sits at f ^ (4 * (f / 32 % 2)): the second 32-feature half has
+            // its float4 slots swapped in pairs, so the eight 16-byte reads of a quarter-warp
+            // (features 8 j and 8 j + 4 of one column) fall on distinct banks.
             float* gs = xchg + half * 2 * 16 * 64;   // [16][64] gate
             float* us = gs + 16 * 64;                 // [16][64] up
             if (ok) {
               float* dst = (q < 2) ? gs : us;
+              const int fsw = (32 * (q & 1) + lane) ^ (4 * (q & 1));
 #pragma unroll
-              for (int c = 0; c < 16; ++c) dst[c * 64 + 32 * (q & 1) + lane] = __uint_as_float(r[c]);
+              for (int c = 0; c < 16; ++c) dst[c * 64 + fsw] = __uint_as_float(r[c]);
             }
             named_bar_sync(bar_id, 128);
             if (ok) {
               const int t = threadIdx.x - 128 - 128 * half;
               const int cc = t >> 3, f0 = (t & 7) * 8;
               const int col = c0 + cc;
-              const float4 g0 = *reinterpret_cast<const float4*>(gs + cc * 64 + f0);
-              const float4 g1 = *reinterpret_cast<const float4*>(gs + cc * 64 + f0 + 4);
-              const float4 u0 = *reinterpret_cast<const float4*>(us + cc * 64 + f0);
-              const float4 u1 = *reinterpret_cast<const float4*>(us + cc * 64 + f0 + 4);
+              const int s0 = f0 ^ (4 * (f0 >> 5)), s1 = (f0 + 4) ^ (4 * (f0 >> 5));
+              const float4 g0 = *reinterpret_cast<const float4*>(gs + cc * 64 + s0);
+              const float4 g1 = *reinterpret_cast<const float4*>(gs + cc * 64 + s1);
+              const float4 u0 = *reinterpret_cast<const float4*>(us + cc * 64 + s0);
+              const float4 u1 = *reinterpret_cast<const float4*>(us + cc * 64 + s1);
               const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
               const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
               float a[8];

@@ -11,7 +11,7 @@
 // order for every output element: the K loop is identical, never split, and a token's column
 // position does not change the arithmetic of its column.
 //
-// Roles (256 threads; 384 for wide token tiles):
+// Roles (256 threads; 384 for 128-row token tiles):
 //   warp 0      TMA producer: packed weight tile (FP4, unpacked to 8-bit containers by the TMA)
 //               and its 512-byte scale block (bulk copy); one mbarrier transaction per stage.
 //   warps 1, 3  token-operand producers: cp.async gathers of the BN activation rows (128 B each,
@@ -21,7 +21,7 @@
 //   warp 2      TMEM owner and MMA issuer: tcgen05.cp of the scale blocks to TMEM, four K=32
 //               MMAs per K-chunk, tcgen05.commit releases the stage only after the MMAs (and
 //               copies) that read it are complete.
-//   warps 4-7   epilogue (and 8-11 for wide tiles): tcgen05.ld of the fp32 accumulator, SwiGLU +
+//   warps 4-7   epilogue (and 8-11 for 128-row tiles): tcgen05.ld of the fp32 accumulator, SwiGLU +
 //               MXFP8 requant (W13) or routing-weight scaling into the per-slot buffer (W2).
 // Work items (expert, weight panel, token tile) are walked with the token tile fastest, so CTAs
 // running at the same time share one weight panel through L2.
@@ -45,13 +45,17 @@ namespace moe {
 #define MOE_WIDE_STAGES 2           // pipeline stages of the widest tiles
 #endif
 #ifndef MOE_WIDE_KT
-#define MOE_WIDE_KT 2               // K-chunks per stage of the widest tiles
+#define MOE_WIDE_KT 1               // K-chunks per stage of the widest tiles
 #endif
-// 4 producer/MMA warps + 4 epilogue warps; wide token tiles take 8 epilogue warps (two per TMEM
-// lane quarter, splitting the tile's columns), since their epilogue, not the MMA, sets the pace.
+#ifndef MOE_WIDE_CTAS
+#define MOE_WIDE_CTAS 2             // CTAs per SM of the widest tiles (2: one accumulator each)
+#endif
+// 4 producer/MMA warps + 4 epilogue warps; 128-row token tiles (one CTA per SM) take 8 epilogue
+// warps (two per TMEM lane quarter, splitting the tile's columns), since their epilogue, not the
+// MMA, sets the pace. The widest tiles run two CTAs per SM with 4 epilogue warps each.
 template <int BN>
 struct Threads {
-  static constexpr int kEpiWarps = (BN >= 128) ? 8 : 4;
+  static constexpr int kEpiWarps = (BN == 128 || (BN > 128 && MOE_WIDE_CTAS == 1)) ? 8 : 4;
   static constexpr int kCount = 128 + 32 * kEpiWarps;
 };
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
@@ -115,7 +119,10 @@ struct Smem {
   static constexpr int kStageBytes = (int)((kStageA + kStageB + KT * kSfChunk + 1023) / 1024 * 1024);
   static constexpr int kStages =
       (BN <= 32) ? MOE_DEC_STAGES : (BN <= 64 ? 3 : (BN == 128 ? 6 / MOE_KT_WIDE : MOE_WIDE_STAGES));
-  static constexpr int kCtasPerSm = (BN <= 32) ? MOE_DEC_CTAS : (BN <= 64 ? 2 : 1);
+  static constexpr int kCtasPerSm = (BN <= 32) ? MOE_DEC_CTAS : (BN <= 64 ? 2 : (BN == 128 ? 1 : MOE_WIDE_CTAS));
+  // accumulator slots in TMEM: two (the epilogue of one tile overlaps the next tile's MMAs), or
+  // one when two wide CTAs share the SM (the other CTA's MMAs fill the epilogue's time)
+  static constexpr int kAcc = (BN > 128 && MOE_WIDE_CTAS == 2) ? 1 : 2;
   // the weight producer keeps kPrefetch K-chunks of its own upcoming tiles (codes and scales)
   // requested into L2 beyond the stages in flight: more bytes in flight per SM than shared memory
   // holds, so a stage's load finds its data in L2 instead of waiting a full DRAM round trip
@@ -124,7 +131,7 @@ struct Smem {
   // kSfSlot columns per K-chunk in flight: 4 for A, 4 per 128 token rows for B); the allocation is
   // the next power of two, small enough for kCtasPerSm CTAs to share the SM's 512 columns
   static constexpr int kAccStride = (BN <= 32) ? 32 : (BN <= 64 ? 64 : BN);
-  static constexpr int kSfCol = 2 * kAccStride;
+  static constexpr int kSfCol = kAcc * kAccStride;
   static constexpr int kSfSlot = 4 + 4 * ((BN + 127) / 128);
   static constexpr int kTmemCols = pow2_at_least(kSfCol + kStages * KT * kSfSlot, 32);
   static_assert(kTmemCols * kCtasPerSm <= 512, "TMEM columns per SM");
@@ -169,7 +176,7 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
                                                                     const GemmParams p) {
   using L = Smem<BN>;
   constexpr int S = L::kStages;
-  constexpr int NACC = 2;                          // accumulator slots in TMEM
+  constexpr int NACC = L::kAcc;                    // accumulator slots in TMEM
   constexpr bool kTmaB = L::kTmaB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -498,7 +505,7 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
       tc_fence_after();
       const uint32_t d_tmem = tmem + (uint32_t)(acc * L::kAccStride);
       // TMEM is read kGrp 16-column chunks per round trip (one wait for several loads)
-      constexpr int kGrp = W13 ? (BN <= 32 ? 1 : 2) : (BN >= 64 ? 4 : BN / 16);
+      constexpr int kGrp = W13 ? (BN <= 32 ? 1 : 2) : (BN >= 64 ? (L::kAcc == 1 ? 2 : 4) : BN / 16);
       for (int cg = 16 * kGrp * half; cg < tw; cg += 16 * kGrp * kHalves) {
         uint32_t rg[kGrp][16];
         if (ok) {

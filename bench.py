@@ -3,8 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode-6] [--impl reference]
 
 A step is one whole layer call (route -> MXFP8 quant -> W13+SwiGLU+requant -> W2 -> combine) over
-one batch of the workload, inputs resident in HBM. L2 is flushed (256 MiB write) between timed
-steps; each step is timed with CUDA events on the launching stream and the per-step times summed.
+one batch of the workload, inputs resident in HBM. L2 is flushed between timed steps (a 256 MiB
+write, then a 256 MiB read of a second buffer so that the write's dirty lines are drained before
+the step rather than written back inside it); each step is timed with CUDA events on the launching stream and the per-step times summed.
 `value` is tokens/s over all ranks (rows are independent: every rank runs its own replica of the
 batch, weak scaling). `e2e` repeats the measurement through the public API with the batch
 copied host->device (pinned) and the output copied back inside the timed region. `roofline`
@@ -290,6 +291,15 @@ def gpu_arm(args):
     ws = layer.workspace(cfg.T)
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_clean = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def flush_l2(v: float) -> None:
+        """Write a buffer larger than L2, then read another one: L2 then holds none of the previous
+        step's data and no dirty lines whose write-back would land in the next timed region."""
+        flush.fill_(v)
+        torch.sum(flush_clean, dim=0, out=flush_sink)
+
     stream = torch.cuda.current_stream()
     shared = side_s = None
     if args.shared_inter:
@@ -325,7 +335,7 @@ def gpu_arm(args):
     barrier()
     torch.cuda.synchronize()
     for i in range(args.steps):
-        flush.fill_(float(i))
+        flush_l2(float(i))
         evs[i][0].record(stream)
         fwd(x, dead)
         evs[i][1].record(stream)
@@ -356,7 +366,7 @@ def gpu_arm(args):
         gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.fill_(float(i))
+            flush_l2(float(i))
             gev[i][0].record(stream)
             g.replay()
             gev[i][1].record(stream)
@@ -375,13 +385,13 @@ def gpu_arm(args):
     k13 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     k2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.fill_(float(i))
+        flush_l2(float(i))
         B.moe_route_topk(shp, x, layer.w_router, layer.bias, dead, ws, plan=plan)
         B.moe_quant_mxfp8(x, xq, xs)
         k13[i][0].record(stream)
         B.moe_w13_swiglu_grouped(shp, xq, xs, layer.w13p, layer.w13sp, plan, ws, hq=hq, hs=hs)
         k13[i][1].record(stream)
-        flush.fill_(float(i) + 0.5)
+        flush_l2(float(i) + 0.5)
         k2[i][0].record(stream)
         B.moe_w2_combine_grouped(shp, hq, hs, layer.w2p, layer.w2sp, plan, ws, out=out)
         k2[i][1].record(stream)
@@ -427,7 +437,7 @@ def gpu_arm(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
     for i in range(args.steps):
-        flush.fill_(float(i))
+        flush_l2(float(i))
         e0.record(stream)
         x_dev.copy_(x_host, non_blocking=True)
         if dead_dev is not None:
@@ -453,7 +463,7 @@ def gpu_arm(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8 x mxfp4 -> f32",
             "data": "synthetic (seeded; weights N(0,0.02) quantised to MXFP4 by the library)",
-            "config": {"workload": workload_name(cfg), "l2": "flushed between timed steps (256 MiB write)",
+            "config": {"workload": workload_name(cfg), "l2": "flushed between timed steps (256 MiB write, then 256 MiB read of another buffer)",
                        "parallelism": f"replica per GPU x{world}", "touched_experts": touched,
                        "live_slots": live_slots,
                        **({"shared_expert_inter": args.shared_inter, "shared_expert": "MXFP8, side stream"}

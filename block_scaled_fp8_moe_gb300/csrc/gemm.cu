@@ -47,6 +47,9 @@ namespace moe {
 #ifndef MOE_WIDE_KT
 #define MOE_WIDE_KT 1               // K-chunks per stage of the widest tiles
 #endif
+#ifndef MOE_N128_CTAS
+#define MOE_N128_CTAS 1             // CTAs per SM of 128-row token tiles (2: one accumulator each)
+#endif
 #ifndef MOE_WIDE_CTAS
 #define MOE_WIDE_CTAS 2             // CTAs per SM of the widest tiles (2: one accumulator each)
 #endif
@@ -55,7 +58,7 @@ namespace moe {
 // MMA, sets the pace. The widest tiles run two CTAs per SM with 4 epilogue warps each.
 template <int BN>
 struct Threads {
-  static constexpr int kEpiWarps = (BN == 128 || (BN > 128 && MOE_WIDE_CTAS == 1)) ? 8 : 4;
+  static constexpr int kEpiWarps = ((BN == 128 && MOE_N128_CTAS == 1) || (BN > 128 && MOE_WIDE_CTAS == 1)) ? 8 : 4;
   static constexpr int kCount = 128 + 32 * kEpiWarps;
 };
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
@@ -109,7 +112,8 @@ struct Smem {
   // A pipeline stage holds KT consecutive K-chunks (weight tiles) of 128: small token tiles are
   // weight-streaming bound and each stage hand-off costs a fixed few hundred ns per CTA, so they
   // move 16 KB of packed weights per TMA request.
-  static constexpr int KT = (BN <= 32) ? MOE_DEC_KT : (BN <= 64 ? 1 : (BN == 128 ? MOE_KT_WIDE : MOE_WIDE_KT));
+  static constexpr int KT =
+      (BN <= 32) ? MOE_DEC_KT : (BN <= 64 ? 1 : (BN == 128 ? (MOE_N128_CTAS == 2 ? 1 : MOE_KT_WIDE) : MOE_WIDE_KT));
   static constexpr int kTileA = 16384;                           // one unpacked 128 x 128 FP4 tile
   static constexpr int kTileB = BN * 128;                        // BN rows x 128 FP8
   static constexpr int kStageA = KT * kTileA;
@@ -118,11 +122,13 @@ struct Smem {
   static constexpr int kSfChunk = 512 + kSfbChunk;
   static constexpr int kStageBytes = (int)((kStageA + kStageB + KT * kSfChunk + 1023) / 1024 * 1024);
   static constexpr int kStages =
-      (BN <= 32) ? MOE_DEC_STAGES : (BN <= 64 ? 3 : (BN == 128 ? 6 / MOE_KT_WIDE : MOE_WIDE_STAGES));
-  static constexpr int kCtasPerSm = (BN <= 32) ? MOE_DEC_CTAS : (BN <= 64 ? 2 : (BN == 128 ? 1 : MOE_WIDE_CTAS));
+      (BN <= 32) ? MOE_DEC_STAGES
+                 : (BN <= 64 ? 3 : (BN == 128 ? (MOE_N128_CTAS == 2 ? 2 : 6 / MOE_KT_WIDE) : MOE_WIDE_STAGES));
+  static constexpr int kCtasPerSm =
+      (BN <= 32) ? MOE_DEC_CTAS : (BN <= 64 ? 2 : (BN == 128 ? MOE_N128_CTAS : MOE_WIDE_CTAS));
   // accumulator slots in TMEM: two (the epilogue of one tile overlaps the next tile's MMAs), or
   // one when two wide CTAs share the SM (the other CTA's MMAs fill the epilogue's time)
-  static constexpr int kAcc = (BN > 128 && MOE_WIDE_CTAS == 2) ? 1 : 2;
+  static constexpr int kAcc = ((BN == 128 && MOE_N128_CTAS == 2) || (BN > 128 && MOE_WIDE_CTAS == 2)) ? 1 : 2;
   // the weight producer keeps kPrefetch K-chunks of its own upcoming tiles (codes and scales)
   // requested into L2 beyond the stages in flight: more bytes in flight per SM than shared memory
   // holds, so a stage's load finds its data in L2 instead of waiting a full DRAM round trip

@@ -722,11 +722,9 @@ static int launch_topk_plan(int nb, int E, size_t smem, cudaStream_t st, const f
 
 // One plan block, plain launch (no programmatic serialisation): used by the allocation-free router.
 template <int NI>
-static int launch_topk_single_plain_ni(size_t smem, cudaStream_t st, const float* score, const float* key,
-                                       const uint8_t* dead, int T, int E, int k, int32_t* topk_idx, float* topk_w,
-                                       int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
-                                       int32_t* row_of_slot) {
-  (void)smem;
+static int launch_topk_single_plain_ni(cudaStream_t st, const float* score, const float* key, const uint8_t* dead,
+                                       int T, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                       int32_t* offsets, int32_t* slot_of_row, int32_t* row_of_slot) {
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(topk_plan_single_kernel<NI>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
@@ -740,12 +738,12 @@ static int launch_topk_single_plain_ni(size_t smem, cudaStream_t st, const float
   return launch_status();
 }
 
-static int launch_topk_single_plain(int E, size_t smem, cudaStream_t st, const float* score, const float* key,
+static int launch_topk_single_plain(int E, cudaStream_t st, const float* score, const float* key,
                                     const uint8_t* dead, int T, int k, int32_t* topk_idx, float* topk_w,
                                     int32_t* counts, int32_t* offsets, int32_t* slot_of_row, int32_t* row_of_slot) {
 #define MOE_TOPK_CASE(N)                                                                                          \
   if (E <= 32 * N)                                                                                                \
-    return launch_topk_single_plain_ni<N>(smem, st, score, key, dead, T, E, k, topk_idx, topk_w, counts, offsets, \
+    return launch_topk_single_plain_ni<N>(st, score, key, dead, T, E, k, topk_idx, topk_w, counts, offsets,      \
                                           slot_of_row, row_of_slot);
   MOE_TOPK_CASE(1)
   MOE_TOPK_CASE(2)
@@ -964,9 +962,8 @@ extern "C" int moe_route_topk_noalloc(const moe_shape* s, const uint16_t* x, con
   if (rc) return rc;
   // one plan block (T <= kPlanBlock): the kernel scans and scatters itself and never touches the
   // multi-block count/rank arrays
-  const size_t smem = (size_t)E * 8 * 4 + (size_t)kPlanBlock * k * 2;
-  rc = launch_topk_single_plain(E, smem, st, score, key, dead, T, k, topk_idx, topk_w, expert_counts,
-                               expert_offsets, slot_of_row, row_of_slot);
+  rc = launch_topk_single_plain(E, st, score, key, dead, T, k, topk_idx, topk_w, expert_counts, expert_offsets,
+                                slot_of_row, row_of_slot);
   if (rc) return rc;
   return launch_status();
 }

@@ -47,6 +47,9 @@ namespace moe {
 #ifndef MOE_WIDE_KT
 #define MOE_WIDE_KT 1               // K-chunks per stage of the widest tiles
 #endif
+#ifndef MOE_PANEL_FAST
+#define MOE_PANEL_FAST 0            // 1: work items walk the weight panels fastest (token tile outer)
+#endif
 #ifndef MOE_N128_CTAS
 #define MOE_N128_CTAS 1             // CTAs per SM of 128-row token tiles (2: one accumulator each)
 #endif
@@ -263,8 +266,13 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
     tw = BN;
     if (kTmaB) tw = min(BN, ((cnt + ntiles - 1) / ntiles + 15) / 16 * 16);
     const int local = w - s_cum[e];
-    m = local / ntiles;
-    nt = local - m * ntiles;
+    if (MOE_PANEL_FAST) {
+      nt = local / p.MT;
+      m = local - nt * p.MT;
+    } else {
+      m = local / ntiles;
+      nt = local - m * ntiles;
+    }
     row0 = s_off[e] + nt * tw;
     nrows = min(tw, cnt - nt * tw);
   };

@@ -112,9 +112,9 @@ __host__ __device__ constexpr int pow2_at_least(int v, int p) { return p >= v ? 
 
 template <int BN>
 struct Smem {
-  // A pipeline stage holds KT consecutive K-chunks (weight tiles) of 128: small token tiles are
-  // weight-streaming bound and each stage hand-off costs a fixed few hundred ns per CTA, so they
-  // move 16 KB of packed weights per TMA request.
+  // A pipeline stage holds KT consecutive K-chunks (weight tiles) of 128. A CTA completes a stage
+  // in a roughly fixed time, so the bytes per stage and the CTAs per SM set its streaming rate:
+  // decode tiles run 4 CTAs/SM of 2 one-chunk stages, 128-row tiles stages of two chunks.
   static constexpr int KT =
       (BN <= 32) ? MOE_DEC_KT : (BN <= 64 ? 1 : (BN == 128 ? (MOE_N128_CTAS == 2 ? 1 : MOE_KT_WIDE) : MOE_WIDE_KT));
   static constexpr int kTileA = 16384;                           // one unpacked 128 x 128 FP4 tile
@@ -136,7 +136,7 @@ struct Smem {
   // requested into L2 beyond the stages in flight: more bytes in flight per SM than shared memory
   // holds, so a stage's load finds its data in L2 instead of waiting a full DRAM round trip
   static constexpr int kPrefetch = (BN <= 32) ? MOE_DEC_PF : MOE_WIDE_PF;
-  // TMEM: two accumulator slots of kAccStride columns, then the ring of scale blocks (one slot of
+  // TMEM: kAcc accumulator slots of kAccStride columns, then the ring of scale blocks (one slot of
   // kSfSlot columns per K-chunk in flight: 4 for A, 4 per 128 token rows for B); the allocation is
   // the next power of two, small enough for kCtasPerSm CTAs to share the SM's 512 columns
   static constexpr int kAccStride = (BN <= 32) ? 32 : (BN <= 64 ? 64 : BN);

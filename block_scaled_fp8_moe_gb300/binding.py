@@ -25,7 +25,7 @@ EXPORTED = [
     "moe_w13_swiglu_grouped", "moe_w2_combine_grouped", "moe_forward", "moe_check_device_status",
     "moe_route_topk_noalloc", "moe_selftest_timeout", "moe_route_topk_anchored", "moe_forward_anchored",
     "moe_packed_shared_w13_bytes", "moe_packed_shared_w2_bytes", "moe_pack_shared_w13", "moe_pack_shared_w2",
-    "moe_shared_workspace_bytes", "moe_forward_shared",
+    "moe_shared_workspace_bytes", "moe_forward_shared", "moe_dead_from_survival",
 ]
 
 
@@ -60,6 +60,7 @@ lib.moe_packed_w2_bytes.restype = _SZ
 lib.moe_packed_w2_bytes.argtypes = [_SHP, ctypes.POINTER(_SZ)]
 lib.moe_quant_mxfp4.argtypes = [_I32, _I32, _P, _P, _P, _P]
 lib.moe_quant_mxfp8.argtypes = [_I32, _I32, _P, _P, _P, _P]
+lib.moe_dead_from_survival.argtypes = [_I32, _P, ctypes.c_float, _P, _P]
 lib.moe_pack_w13.argtypes = [_SHP, _P, _P, _P, _P, _P]
 lib.moe_pack_w2.argtypes = [_SHP, _P, _P, _P, _P, _P]
 lib.moe_route_topk.argtypes = [_SHP] + [_P] * 10 + [_P, _SZ, _P]
@@ -166,6 +167,19 @@ def moe_quant_mxfp8(x: torch.Tensor, q: torch.Tensor | None = None, s: torch.Ten
     _check(lib.moe_quant_mxfp8(rows, cols, _ptr(x, torch.bfloat16, name="x"), _ptr(q, torch.uint8, rows * cols),
                                _ptr(s, torch.uint8, rows * cols // 32), _stream(stream)), "moe_quant_mxfp8")
     return q, s
+
+
+SURVIVAL_THRESHOLD = 0.2
+
+
+def moe_dead_from_survival(p_survive: torch.Tensor, threshold: float = SURVIVAL_THRESHOLD,
+                           dead: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """u8 [T] dead-row mask: 1 where the fp32 survival estimate is below the threshold."""
+    T = p_survive.numel()
+    dead = torch.empty(T, dtype=torch.uint8, device=p_survive.device) if dead is None else dead
+    _check(lib.moe_dead_from_survival(T, _ptr(p_survive, torch.float32, T, "p_survive"), float(threshold),
+                                      _ptr(dead, torch.uint8, T, "dead"), _stream(stream)), "moe_dead_from_survival")
+    return dead
 
 
 def moe_pack_w13(shp: MoeShape, q: torch.Tensor, s: torch.Tensor, stream=None):

@@ -214,6 +214,24 @@ extern "C" int moe_quant_mxfp8(int32_t rows, int32_t cols, const uint16_t* x, ui
   return launch_quant_mxfp8(rows, cols, x, q, s, static_cast<cudaStream_t>(stream));
 }
 
+// Dead verification rows from survival estimates (post 2, "Speculative decoding": rows below 0.2
+// skip the expert weight reads): dead[t] = p[t] < threshold in fp32 (NaN stays live).
+__global__ void dead_from_survival_kernel(const float* __restrict__ p, float threshold, uint8_t* __restrict__ dead,
+                                          int T) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < T) dead[t] = (p[t] < threshold) ? 1 : 0;
+}
+
+extern "C" int moe_dead_from_survival(int32_t T, const float* p_survive, float threshold, uint8_t* dead,
+                                      void* stream) {
+  if (T < 0 || !(threshold == threshold)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!p_survive || !dead || (reinterpret_cast<uintptr_t>(p_survive) & 3)) return MOE_ERR_INVALID_ARG;
+  dead_from_survival_kernel<<<(T + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(p_survive, threshold,
+                                                                                          dead, T);
+  return launch_status();
+}
+
 extern "C" int moe_quant_mxfp4(int32_t rows, int32_t cols, const float* w, uint8_t* q, uint8_t* s, void* stream) {
   if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
   if (cols % 32) return MOE_ERR_UNSUPPORTED_SHAPE;

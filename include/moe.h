@@ -147,6 +147,15 @@ MOE_API int moe_route_topk(const moe_shape* shape, const uint16_t* x, const uint
                    int32_t* expert_offsets, int32_t* slot_of_row, int32_t* row_of_slot, void* ws,
                    size_t ws_bytes, void* stream);
 
+/* Dead verification rows from the caller's survival estimates ("New Deepseek 4.1 flash recipe",
+ * post 2, "Speculative decoding": draft rows whose estimated chance of surviving verification is
+ * below 0.2 skip the MoE expert weight reads). dead[t] = (p_survive[t] < threshold) ? 1 : 0,
+ * compared in fp32; a row exactly at the threshold and a NaN estimate stay live. p_survive: fp32
+ * [T] (4-byte aligned), dead: u8 [T], both device memory owned by the caller; the result feeds the
+ * `dead` argument of the calls below. T == 0 is a no-op; T < 0, NULL pointers or a NaN threshold
+ * -> MOE_ERR_INVALID_ARG. */
+MOE_API int moe_dead_from_survival(int32_t T, const float* p_survive, float threshold, uint8_t* dead, void* stream);
+
 /* MXFP8 quantisation of bf16 rows ("How it works" item 3, quantisation casts):
  *   s = smallest integer with max|x| <= 448 * 2^s (clamped to [-127, 127]; zero block -> -127),
  *   code = E4M3 round-to-nearest-even of x * 2^-s (never saturates). cols % 32 == 0. */

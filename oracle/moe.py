@@ -114,6 +114,18 @@ def topk_select(key: np.ndarray, k: int) -> np.ndarray:
     return out
 
 
+SURVIVAL_THRESHOLD = 0.2
+
+
+def dead_from_survival(p_survive, threshold: float = SURVIVAL_THRESHOLD) -> np.ndarray:
+    """Dead verification rows (post 2, "Speculative decoding"): a draft row whose estimated chance
+    of surviving verification is below the threshold (0.2 there) skips the expert weight reads.
+    Compared in fp32, dead = p < threshold: a row exactly at the threshold, and a NaN estimate,
+    stay live."""
+    p = np.asarray(p_survive, dtype=np.float32)
+    return (p < np.float32(threshold)).astype(np.uint8)
+
+
 def check_anchors(anchor, t_: int) -> np.ndarray | None:
     """anchor[t] = -1 (route row t itself) or the index a of a row routed by itself (anchor[a] = -1).
     TP4 serving profile README ("DeepSeek-V4.1-Flash-4x-DGX-Spark-TP4"), settings table row

@@ -91,3 +91,13 @@ def test_packed_sizes(B):
     q2, s2 = B.moe_packed_w2_bytes(shp)
     assert q13 == 256 * (576 // 64) * (4096 // 128) * 8192 and s13 == q13 // 16
     assert q2 == 256 * (4096 // 128) * 5 * 8192 and s2 == q2 // 16     # K = 576 -> 5 chunks of 128
+
+
+def test_dead_from_survival_host_checks(B):
+    n = ctypes.c_void_p(0)
+    assert B.lib.moe_dead_from_survival(0, n, 0.2, n, n) == B.MOE_OK           # empty is a no-op
+    assert B.lib.moe_dead_from_survival(-1, n, 0.2, n, n) == B.MOE_ERR_INVALID_ARG
+    assert B.lib.moe_dead_from_survival(4, n, 0.2, n, n) == B.MOE_ERR_INVALID_ARG
+    assert B.lib.moe_dead_from_survival(4, n, float("nan"), n, n) == B.MOE_ERR_INVALID_ARG
+    odd = ctypes.c_void_p(0x1002)                                               # not 4-byte aligned
+    assert B.lib.moe_dead_from_survival(4, odd, 0.2, ctypes.c_void_p(0x2000), n) == B.MOE_ERR_INVALID_ARG

@@ -64,3 +64,40 @@ def test_route_skewed_bias_all_slots_to_few_experts():
     assert np.array_equal(plan.topk_idx.cpu().numpy(), ref.topk_idx)
     assert np.array_equal(plan.expert_counts.cpu().numpy(), ref.counts)
     assert (ref.counts == 0).sum() >= 10          # most experts empty
+
+
+def _survival_edges(n, seed):
+    rng = np.random.default_rng(seed)
+    p = rng.random(n).astype(np.float32)
+    p[:8] = [0.0, np.nextafter(np.float32(0.2), np.float32(0)), 0.2, np.nextafter(np.float32(0.2), np.float32(1)),
+             np.nan, -np.inf, np.inf, -0.0]
+    return p
+
+
+def test_dead_from_survival_bit_exact():
+    from block_scaled_fp8_moe_gb300 import binding as B
+    for n, thr in ((1, 0.2), (8, 0.2), (1000, 0.2), (4097, 0.35)):
+        p = _survival_edges(max(n, 8), n)[:n]
+        d = B.moe_dead_from_survival(torch.from_numpy(p).cuda(), thr)
+        torch.cuda.synchronize()
+        assert np.array_equal(d.cpu().numpy(), M.dead_from_survival(p, thr))
+
+
+def test_route_with_survival_mask_matches_oracle():
+    from block_scaled_fp8_moe_gb300 import binding as B
+    T, H, E, k = 37, 256, 16, 4
+    rng = np.random.default_rng(5)
+    x = _bf16(rng.standard_normal((T, H)))
+    wr = _bf16(rng.standard_normal((E, H)) * 0.02)
+    bias = (rng.standard_normal(E) * 0.1).astype(np.float32)
+    p = _survival_edges(T, 9)
+    dead = B.moe_dead_from_survival(torch.from_numpy(p).cuda())
+    shp = B.shape(T, H, E, k, 64)
+    ws = B.alloc_workspace(shp)
+    plan = B.moe_route_topk(shp, x.cuda(), wr.cuda(), torch.from_numpy(bias).cuda(), dead, ws)
+    B.moe_check_device_status(ws)
+    ref = M.route(x.float().numpy(), wr.float().numpy(), bias, k, M.dead_from_survival(p).astype(bool))
+    S = int(ref.offsets[-1])
+    assert np.array_equal(plan.expert_offsets.cpu().numpy(), ref.offsets)
+    assert np.array_equal(plan.slot_of_row.cpu().numpy()[:S], ref.slot_of_row)
+    assert np.array_equal(plan.row_of_slot.cpu().numpy(), ref.row_of_slot)

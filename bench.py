@@ -248,7 +248,7 @@ def launches_per_step(cfg) -> int:
     """Kernels one moe_forward launches for this shape (mirrors the library's dispatch)."""
     T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
     nc = H // 64
-    decode_router = T <= 64 and 4 * nc <= 256 and (min(T, 16) * nc * 144 + 4 * T * nc * 4) <= 210 * 1024
+    decode_router = T <= 64 and 2 * nc <= 256 and (min(T, 16) * nc * 144 + 2 * T * nc * 4) <= 210 * 1024
     if decode_router:
         n = 1                                         # logits (+ fused MXFP8 quantisation)
     elif T > 16 and E <= 256 and H % 64 == 0 and H <= 4096:

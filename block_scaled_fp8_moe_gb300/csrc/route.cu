@@ -82,7 +82,10 @@ __global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __res
 // router_small_kernel and the tiled kernel. Optionally each CTA also MXFP8-quantises a share of
 // the rows it has staged.
 // ---------------------------------------------------------------------------------------------
-constexpr int kDecEpc = 4;          // experts per CTA
+#ifndef MOE_DEC_EPC
+#define MOE_DEC_EPC 2
+#endif
+constexpr int kDecEpc = MOE_DEC_EPC;  // experts per CTA
 constexpr int kDecGroup = 16;       // token rows staged at a time
 constexpr int kDecMaxT = 64;
 constexpr size_t kDecodeSmemMax = 210 * 1024;

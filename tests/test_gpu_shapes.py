@@ -19,6 +19,7 @@ SHAPES = [
     (70, 256, 12, 1, 448),       # k = 1, 64 < avg rows per expert
     (129, 640, 24, 6, 128),
     (260, 128, 2, 2, 64),        # two experts, every row takes both: 260 rows each (wide tiles)
+    (3, 8192, 8, 2, 64),         # widest rows of the decode router (fused quantisation), K = 64 chunks
 ]
 
 

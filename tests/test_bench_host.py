@@ -1,0 +1,44 @@
+"""Host-side checks of bench.py: the per-step launch count it reports (`gpu_launches`) follows the
+library's dispatch, whose constants are read from the CUDA sources so that a change there that
+is not mirrored here fails on the CPU."""
+import os
+import re
+
+import bench
+from block_scaled_fp8_moe_gb300 import synth
+
+CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "block_scaled_fp8_moe_gb300",
+                    "csrc")
+
+
+def _const(name):
+    src = open(os.path.join(CSRC, "route.cu")).read()
+    m = re.search(r"#define %s (\d+)" % name, src) or re.search(r"constexpr \w+ %s = ([\d *]+);" % name, src)
+    assert m, name
+    return eval(m.group(1))  # noqa: S307 - integer literals / products from our own source
+
+
+def _decode_router(T, H):
+    nc = H // 64
+    epc, pitch, group = _const("MOE_DEC_EPC"), _const("kDecPitch"), _const("kDecGroup")
+    smem = min(T, group) * nc * pitch + epc * T * nc * 4
+    return T <= _const("kDecMaxT") and epc * nc <= 256 and smem <= _const("kDecodeSmemMax")
+
+
+def test_decode_router_predicate_matches_the_library_constants():
+    for T in (1, 6, 10, 11, 12, 16, 48, 64, 65):
+        for H in (256, 4096, 8192, 16384):
+            cfg = synth.custom("p", T, H, 256, 8, 128, seed=0)
+            n = bench.launches_per_step(cfg)
+            if _decode_router(T, H):
+                assert n == 5, (T, H)              # router (+ quant), top-k + plan, W13, W2, combine
+            else:
+                assert n >= 6, (T, H)              # separate quantiser and a non-decode router
+
+
+def test_launch_counts_of_the_benchmarked_workloads():
+    counts = {name: bench.launches_per_step(synth.CONFIGS[name]) for name in
+              ("decode-6", "decode-48", "prefill-4k", "prefill-32k")}
+    # decode: fused router+quant, top-k/plan, W13, W2, combine; prefill: norms, screen, exact
+    # recompute, grid-wide select, plan, scan, scatter, quantiser into plan order, W13, W2, combine
+    assert counts == {"decode-6": 5, "decode-48": 5, "prefill-4k": 11, "prefill-32k": 11}

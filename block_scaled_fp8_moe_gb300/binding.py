@@ -17,7 +17,8 @@ if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
 lib = ctypes.CDLL(LIB_PATH)
 
-MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(6)
+(MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT,
+ MOE_ERR_DEVICE_INPUT) = range(7)
 
 EXPORTED = [
     "moe_status_string", "moe_workspace_bytes", "moe_packed_w13_bytes", "moe_packed_w2_bytes",
@@ -25,7 +26,8 @@ EXPORTED = [
     "moe_w13_swiglu_grouped", "moe_w2_combine_grouped", "moe_forward", "moe_check_device_status",
     "moe_route_topk_noalloc", "moe_selftest_timeout", "moe_route_topk_anchored", "moe_forward_anchored",
     "moe_packed_shared_w13_bytes", "moe_packed_shared_w2_bytes", "moe_pack_shared_w13", "moe_pack_shared_w2",
-    "moe_shared_workspace_bytes", "moe_forward_shared", "moe_dead_from_survival",
+    "moe_shared_workspace_bytes", "moe_forward_shared", "moe_dead_from_survival", "moe_w2_grouped", "moe_combine",
+    "moe_probe_mma_rate",
 ]
 
 
@@ -65,7 +67,10 @@ lib.moe_pack_w13.argtypes = [_SHP, _P, _P, _P, _P, _P]
 lib.moe_pack_w2.argtypes = [_SHP, _P, _P, _P, _P, _P]
 lib.moe_route_topk.argtypes = [_SHP] + [_P] * 10 + [_P, _SZ, _P]
 lib.moe_w13_swiglu_grouped.argtypes = [_SHP] + [_P] * 9 + [_P, _SZ, _P]
-lib.moe_w2_combine_grouped.argtypes = [_SHP] + [_P] * 9 + [_P, _SZ, _P]
+lib.moe_w2_combine_grouped.argtypes = [_SHP] + [_P] * 10 + [_P, _SZ, _P]
+lib.moe_w2_grouped.argtypes = [_SHP] + [_P] * 8 + [_P, _SZ, _P]
+lib.moe_combine.argtypes = [_SHP] + [_P] * 4 + [_P, _SZ, _P]
+lib.moe_probe_mma_rate.argtypes = [_I32, ctypes.POINTER(_I32), ctypes.POINTER(ctypes.c_int64), _P, _SZ, _P]
 lib.moe_forward.argtypes = [_SHP] + [_P] * 9 + [ctypes.POINTER(MoeIntermediates), _P, _SZ, _P]
 lib.moe_check_device_status.argtypes = [_P, _P]
 lib.moe_route_topk_noalloc.argtypes = [_SHP] + [_P] * 10 + [_P]
@@ -257,13 +262,35 @@ def moe_w13_swiglu_grouped(shp: MoeShape, xq, xs, w13p, w13sp, plan: Plan, ws, h
     return hq, hs
 
 
-def moe_w2_combine_grouped(shp: MoeShape, hq, hs, w2p, w2sp, plan: Plan, ws, out=None, stream=None):
+def moe_w2_combine_grouped(shp: MoeShape, hq, hs, w2p, w2sp, plan: Plan, ws, out=None, stream=None, dead=None):
     out = torch.empty(shp.T, shp.H, dtype=torch.bfloat16, device=hq.device) if out is None else out
     _check(lib.moe_w2_combine_grouped(
         ctypes.byref(shp), _ptr(hq, torch.uint8), _ptr(hs, torch.uint8), _ptr(w2p, torch.uint8),
         _ptr(w2sp, torch.uint8), _ptr(plan.topk_w), _ptr(plan.expert_offsets), _ptr(plan.slot_of_row),
-        _ptr(plan.row_of_slot), _ptr(out, torch.bfloat16, shp.T * shp.H, "out"), _ptr(ws), ws.numel(),
-        _stream(stream)), "moe_w2_combine_grouped")
+        _ptr(plan.row_of_slot), _ptr(dead, torch.uint8, shp.T, "dead"),
+        _ptr(out, torch.bfloat16, shp.T * shp.H, "out"), _ptr(ws), ws.numel(), _stream(stream)),
+        "moe_w2_combine_grouped")
+    return out
+
+
+def moe_w2_grouped(shp: MoeShape, hq, hs, w2p, w2sp, plan: Plan, ws, y=None, stream=None):
+    """Down-projection GEMM alone: per-slot fp32 rows y [T*k, H] (rows of dead slots untouched)."""
+    S = shp.T * shp.k
+    y = torch.empty(max(S, 1), shp.H, dtype=torch.float32, device=hq.device) if y is None else y
+    _check(lib.moe_w2_grouped(
+        ctypes.byref(shp), _ptr(hq, torch.uint8), _ptr(hs, torch.uint8), _ptr(w2p, torch.uint8),
+        _ptr(w2sp, torch.uint8), _ptr(plan.topk_w), _ptr(plan.expert_offsets), _ptr(plan.slot_of_row),
+        _ptr(y, torch.float32, S * shp.H, "y"), _ptr(ws), ws.numel(), _stream(stream)), "moe_w2_grouped")
+    return y
+
+
+def moe_combine(shp: MoeShape, y, row_of_slot, ws, dead=None, out=None, stream=None):
+    """Fixed-order combine alone: out[t] = bf16(((y[t,0] + y[t,1]) + ...)), dead rows +0."""
+    out = torch.empty(shp.T, shp.H, dtype=torch.bfloat16, device=y.device) if out is None else out
+    _check(lib.moe_combine(
+        ctypes.byref(shp), _ptr(y, torch.float32, shp.T * shp.k * shp.H, "y"),
+        _ptr(row_of_slot, torch.int32, shp.T * shp.k, "row_of_slot"), _ptr(dead, torch.uint8, shp.T, "dead"),
+        _ptr(out, torch.bfloat16, shp.T * shp.H, "out"), _ptr(ws), ws.numel(), _stream(stream)), "moe_combine")
     return out
 
 
@@ -336,6 +363,16 @@ def moe_forward(shp: MoeShape, x, w_router, bias, dead, w13p, w13sp, w2p, w2sp, 
             ctypes.byref(im) if im is not None else None, _ptr(ws), ws.numel(), _stream(stream)),
             "moe_forward_anchored")
     return out
+
+
+def moe_probe_mma_rate(iters: int, ws, stream=None) -> tuple[int, int]:
+    """Launch the block-scaled MMA rate probe (time it with events on `stream`); returns
+    (CTAs, FLOPs of the launch)."""
+    ctas = _I32(0)
+    flops = ctypes.c_int64(0)
+    _check(lib.moe_probe_mma_rate(int(iters), ctypes.byref(ctas), ctypes.byref(flops), _ptr(ws), ws.numel(),
+                                  _stream(stream)), "moe_probe_mma_rate")
+    return int(ctas.value), int(flops.value)
 
 
 def moe_selftest_timeout(ws, limit_ns: int, stream=None) -> None:

@@ -4,6 +4,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 using namespace moe;
 
@@ -21,6 +22,7 @@ extern "C" const char* moe_status_string(int status) {
     case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_INPUT: return "invalid input found on the device (anchor, or a dead row holding slots)";
     default: return "unknown status";
   }
 }
@@ -49,25 +51,72 @@ extern "C" int moe_w13_swiglu_grouped(const moe_shape* s, const uint8_t* xq, con
                     ws_ptr<uint8_t>(ws, L.xqp), ws_ptr<uint8_t>(ws, L.xsp), false, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+// Argument checks of the down projection's GEMM, shared by the entry points that run it.
+int w2_args_ok(const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2_s, const float* topk_w,
+               const int32_t* expert_offsets, const int32_t* slot_of_row) {
+  if (!hq || !hs || !w2 || !w2_s || !topk_w || !expert_offsets || !slot_of_row) return MOE_ERR_INVALID_ARG;
+  if (!aligned(hq, 16) || !aligned(hs, 4) || !aligned(w2, 32) || !aligned(w2_s, 16) || !aligned(topk_w, 4))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// A workspace that only has to hold the status word.
+int status_ws_ok(void* ws, size_t ws_bytes) {
+  if (!ws || !aligned(ws, 256) || ws_bytes < 256) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+}  // namespace
+
 extern "C" int moe_w2_combine_grouped(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2,
                                       const uint8_t* w2_s, const float* topk_w, const int32_t* expert_offsets,
-                                      const int32_t* slot_of_row, const int32_t* row_of_slot, uint16_t* out,
-                                      void* ws, size_t ws_bytes, void* stream) {
+                                      const int32_t* slot_of_row, const int32_t* row_of_slot, const uint8_t* dead,
+                                      uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
   if (!s) return MOE_ERR_INVALID_ARG;
   if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
   int rc = ws_check(s, ws, ws_bytes);
   if (rc) return rc;
   if (s->T == 0) return MOE_OK;
-  if (!hq || !hs || !w2 || !w2_s || !topk_w || !expert_offsets || !slot_of_row || !row_of_slot || !out)
-    return MOE_ERR_INVALID_ARG;
-  if (!aligned(hq, 16) || !aligned(hs, 4) || !aligned(w2, 32) || !aligned(w2_s, 16) || !aligned(out, 16))
-    return MOE_ERR_INVALID_ARG;
+  rc = w2_args_ok(hq, hs, w2, w2_s, topk_w, expert_offsets, slot_of_row);
+  if (rc) return rc;
+  if (!row_of_slot || !out || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
   const Workspace L = workspace_layout(s);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* y = ws_ptr<float>(ws, L.y);
-  rc = launch_w2(s, hq, hs, w2, w2_s, topk_w, expert_offsets, slot_of_row, y, ws_ptr<uint32_t>(ws, L.status), st);
+  uint32_t* status = ws_ptr<uint32_t>(ws, L.status);
+  rc = launch_w2(s, hq, hs, w2, w2_s, topk_w, expert_offsets, slot_of_row, y, status, st);
   if (rc) return rc;
-  return launch_combine(s, y, row_of_slot, out, st);
+  return launch_combine(s, y, row_of_slot, out, st, nullptr, dead, status);
+}
+
+extern "C" int moe_w2_grouped(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2,
+                              const uint8_t* w2_s, const float* topk_w, const int32_t* expert_offsets,
+                              const int32_t* slot_of_row, float* y, void* ws, size_t ws_bytes, void* stream) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int rc = status_ws_ok(ws, ws_bytes);
+  if (rc) return rc;
+  if (s->T == 0) return MOE_OK;
+  rc = w2_args_ok(hq, hs, w2, w2_s, topk_w, expert_offsets, slot_of_row);
+  if (rc) return rc;
+  if (!y || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+  return launch_w2(s, hq, hs, w2, w2_s, topk_w, expert_offsets, slot_of_row, y, static_cast<uint32_t*>(ws),
+                   static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, const uint8_t* dead,
+                           uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int rc = status_ws_ok(ws, ws_bytes);
+  if (rc) return rc;
+  if (s->T == 0) return MOE_OK;
+  if (!y || !row_of_slot || !out || !aligned(y, 16) || !aligned(row_of_slot, 4) || !aligned(out, 16))
+    return MOE_ERR_INVALID_ARG;
+  return launch_combine(s, y, row_of_slot, out, static_cast<cudaStream_t>(stream), nullptr, dead,
+                        static_cast<uint32_t*>(ws));
 }
 
 extern "C" int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* bias,
@@ -222,7 +271,7 @@ int forward_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router
     cudaEventDestroy(ev_join);
   }
   if (rc) return rc;
-  return launch_combine(s, y, row_of_slot, out, st, y_shared);
+  return launch_combine(s, y, row_of_slot, out, st, y_shared, dead, status);
 }
 
 }  // namespace
@@ -262,7 +311,7 @@ extern "C" int moe_check_device_status(void* ws, void* stream) {
   if (h != 0) {
     if (cudaMemsetAsync(ws, 0, 4, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
       return MOE_ERR_CUDA;
-    return MOE_ERR_TIMEOUT;
+    return h == DEV_BAD_INPUT ? MOE_ERR_DEVICE_INPUT : MOE_ERR_TIMEOUT;
   }
   return MOE_OK;
 }

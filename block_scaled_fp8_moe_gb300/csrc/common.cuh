@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <map>
+#include <mutex>
 #include <utility>
 
 #include "../../include/moe.h"
@@ -92,33 +94,65 @@ inline int launch_status() {
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-inline int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
+constexpr int kMaxDevices = 64;
+
+inline int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  return dev;
 }
+
+// Per-device properties, read once per device (every GPU of a process gets its own entry).
+struct DeviceProps {
+  int sms = 0, smem_per_sm = 0, smem_reserved = 0;
+};
+
+inline const DeviceProps& device_props() {
+  static std::mutex mu;
+  static DeviceProps props[kMaxDevices];
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceProps& p = props[dev];
+  if (!p.sms) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    if (cudaDeviceGetAttribute(&p.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        p.smem_per_sm <= 0)
+      p.smem_per_sm = 228 * 1024;
+    if (cudaDeviceGetAttribute(&p.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+      p.smem_reserved = 1024;
+    p.sms = n;
+  }
+  return p;
+}
+
+inline int num_sms() { return device_props().sms; }
 
 // CTAs of `smem_bytes` dynamic shared memory that fit on one SM, capped at `cap` (the per-SM
 // shared-memory capacity minus the per-block reservation, as the device reports them).
 inline int ctas_per_sm_by_smem(size_t smem_bytes, int cap) {
-  static int per_sm = 0, reserved = 0;
-  if (!per_sm) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        per_sm <= 0)
-      per_sm = 228 * 1024;
-    if (cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
-      reserved = 1024;
-  }
-  int n = (int)((size_t)per_sm / (smem_bytes + (size_t)reserved));
+  const DeviceProps& p = device_props();
+  int n = (int)((size_t)p.smem_per_sm / (smem_bytes + (size_t)p.smem_reserved));
   if (n > cap) n = cap;
   return n < 1 ? 1 : n;
+}
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the current device. The
+// attribute belongs to the (kernel, device) pair, so each GPU a process uses is set up on its first
+// launch there; later calls only look the pair up.
+inline int ensure_smem_limit(const void* kern, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;
+  const std::pair<const void*, int> key(kern, current_device());
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find(key);
+  if (it != done.end() && it->second >= bytes) return MOE_OK;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  done[key] = bytes;
+  return MOE_OK;
 }
 
 // Launch with the programmatic-stream-serialization attribute: the kernel may begin while the
@@ -162,9 +196,10 @@ int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const u
 int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2s,
               const float* topk_w, const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
               cudaStream_t st, bool fp8_weights = false);
-// y_shared (nullable): a per-token row added after the routed slots (the shared expert)
+// y_shared (nullable): a per-token row added after the routed slots (the shared expert); dead
+// (nullable): rows forced to +0.0, a forced row that holds slots is recorded in *status
 int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, uint16_t* out, cudaStream_t st,
-                   const float* y_shared = nullptr);
+                   const float* y_shared, const uint8_t* dead, uint32_t* status);
 // Large-T router: certified tensor-core screen + exact recompute of the surviving experts; writes
 // the same score/key rows as the exact router for every expert that can be selected.
 bool router_screen_supported(const moe_shape* s);

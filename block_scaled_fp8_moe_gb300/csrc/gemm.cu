@@ -480,9 +480,11 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
         if (!ok) break;
         tc_commit(&acc_full[acc]);
       }
-      // every MMA this thread issued has completed before TMEM is released
+      // every MMA and scale copy this thread issued has completed before TMEM is released: the
+      // commit arrives once they finish, also after an abort, so this wait does not take the
+      // abort shortcut (it stays bounded by its own limit)
       tc_commit(drain);
-      mbar_wait(drain, 0, kWaitLimitNs, abort_flag, nullptr, 0);
+      mbar_wait(drain, 0, kWaitLimitNs, nullptr, p.status, DEV_TIMEOUT_DRAIN);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -621,7 +623,9 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
 
   __syncthreads();
   if (*abort_flag) {
-    // give copies still in flight time to land before the CTA's shared memory goes away
+    // after an expired wait, TMA copies the producers issued may still be landing in shared
+    // memory (their completion is only signalled on stage barriers whose other arrivals may never
+    // come): give them time to land before the CTA's shared memory goes away
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < 50000) {
     }
@@ -711,12 +715,7 @@ static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const G
   using L = Smem<BN>;
   auto kern = grouped_gemm_kernel<BN, W13>;
   const int smem = L::total(gp.E);
-  static int attr = 0;
-  if (attr < smem) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::total(kMaxE)) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr = L::total(kMaxE);
-  }
+  if (ensure_smem_limit((const void*)kern, L::total(kMaxE))) return MOE_ERR_CUDA;
   // persistent grid: as many CTAs as fit on the GPU at once (smem depends on E)
   const int occ = ctas_per_sm_by_smem((size_t)smem, L::kCtasPerSm);
   const long long grid = std::min<long long>(max_items, (long long)occ * num_sms());

@@ -14,8 +14,9 @@ enum : uint32_t {
   DEV_TIMEOUT_EMPTY = 2,     // producer waited too long for a free stage
   DEV_TIMEOUT_ACCUM = 3,     // epilogue waited too long for the accumulator
   DEV_TIMEOUT_DRAIN = 4,     // accumulator drain wait expired
-  DEV_BAD_PLAN = 5,          // plan arrays inconsistent with the shape
+  DEV_BAD_INPUT = 5,         // an input only the device can check was invalid (anchor, dead row with slots)
 };
+// Codes below DEV_BAD_INPUT are expired waits.
 
 // Programmatic dependent launch: every kernel of the layer is launched allowed to start while its
 // predecessor on the stream is still running. pdl_wait() blocks until the predecessor grid has
@@ -70,16 +71,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait. Returns false (after recording `code` in *err) once `limit_ns` has passed, or at
-// once if another thread of the CTA already gave up (*abort != 0).
+// once if another thread of the CTA already gave up (*abort != 0). With abort == nullptr the wait
+// ignores other threads' give-ups and ends only on completion or on its own limit (used to drain
+// asynchronous work that will complete whatever the rest of the CTA did).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
                                           volatile uint32_t* abort, uint32_t* err, uint32_t code) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
+    if (abort && *abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
-      *abort = 1;
+      if (abort) *abort = 1;
       if (err) atomicCAS(err, 0u, code);
       return false;
     }

@@ -354,7 +354,7 @@ __device__ __forceinline__ int anchor_of(const int32_t* __restrict__ anchor, int
   const int a = anchor[t];
   if (a < 0) return -1;
   if (a >= T || anchor[a] != -1) {
-    if (status) atomicCAS(status, 0u, (uint32_t)DEV_BAD_PLAN);
+    if (status) atomicCAS(status, 0u, (uint32_t)DEV_BAD_INPUT);
     return -1;
   }
   return a;
@@ -680,14 +680,9 @@ static int launch_topk_plan_ni(int nb, int E, size_t smem, cudaStream_t st, cons
                                const uint8_t* dead, int T, int k, int32_t* topk_idx, float* topk_w, int32_t* cnt,
                                int32_t* rank, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
                                int32_t* row_of_slot, const int32_t* anchor, uint32_t* status) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(topk_plan_single_kernel<NI>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(topk_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
-  }
+  if (ensure_smem_limit((const void*)topk_plan_single_kernel<NI>, 64 * 1024) ||
+      ensure_smem_limit((const void*)topk_plan_kernel, 64 * 1024))
+    return MOE_ERR_CUDA;
   if (nb == 1)
     return launch_pdl(topk_plan_single_kernel<NI>, dim3(1), dim3(512), plan_single_smem(E, k), st, score, key, dead, T,
                       E, k, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, anchor, status);
@@ -728,13 +723,7 @@ template <int NI>
 static int launch_topk_single_plain_ni(cudaStream_t st, const float* score, const float* key, const uint8_t* dead,
                                        int T, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* counts,
                                        int32_t* offsets, int32_t* slot_of_row, int32_t* row_of_slot) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(topk_plan_single_kernel<NI>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
-  }
+  if (ensure_smem_limit((const void*)topk_plan_single_kernel<NI>, 64 * 1024)) return MOE_ERR_CUDA;
   topk_plan_single_kernel<NI><<<1, 512, plan_single_smem(E, k), st>>>(score, key, dead, T, E, k, topk_idx, topk_w,
                                                                        counts, offsets, slot_of_row, row_of_slot,
                                                                        nullptr, nullptr);
@@ -775,13 +764,7 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
   const size_t dec_smem = router_decode_smem(T, H);
   int rc0 = MOE_OK;
   if (T <= kDecMaxT && kDecEpc * (H / kRouterChunk) <= 256 && dec_smem <= kDecodeSmemMax) {
-    static bool dec_attr = false;
-    if (!dec_attr) {
-      if (cudaFuncSetAttribute(router_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kDecodeSmemMax) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      dec_attr = true;
-    }
+    if (ensure_smem_limit((const void*)router_decode_kernel, (int)kDecodeSmemMax)) return MOE_ERR_CUDA;
     const bool fuse = xq && xs;
     uint8_t* fq = fuse ? xq : nullptr;
     uint8_t* fs = fuse ? xs : nullptr;
@@ -816,11 +799,13 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
 
 // ---------------------------------------------------------------------------------------------
 // Combine: out[t] = bf16_rne(((y[t,0] + y[t,1]) + ...) + y[t,k-1]) in fp32, slots in rank order,
-// then + y_shared[t] when a shared expert ran; rows without live slots get +0.0. 8 hidden elements
-// per thread.
+// then + y_shared[t] when a shared expert ran; rows without live slots, and rows the caller's dead
+// mask flags, get +0.0 (a flagged row that still holds slots is recorded in the status word). 8
+// hidden elements per thread.
 // ---------------------------------------------------------------------------------------------
 __global__ void combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_of_slot, int T, int H,
-                               int k, uint16_t* __restrict__ out, const float* __restrict__ y_shared) {
+                               int k, uint16_t* __restrict__ out, const float* __restrict__ y_shared,
+                               const uint8_t* __restrict__ dead, uint32_t* status) {
   pdl_trigger();
   pdl_wait();
   const int H8 = H / 8;
@@ -830,7 +815,10 @@ __global__ void combine_kernel(const float* __restrict__ y, const int32_t* __res
     float acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-    const bool live = row_of_slot[(size_t)t * k] >= 0;
+    const bool held = row_of_slot[(size_t)t * k] >= 0;
+    const bool flagged = dead != nullptr && dead[t] != 0;
+    if (flagged && held && h8 == 0 && status) atomicCAS(status, 0u, (uint32_t)DEV_BAD_INPUT);
+    const bool live = held && !flagged;
     if (live) {
       for (int j = 0; j < k; ++j) {
         const float4* yp = reinterpret_cast<const float4*>(y + ((size_t)t * k + j) * H) + 2 * h8;
@@ -859,11 +847,12 @@ __global__ void combine_kernel(const float* __restrict__ y, const int32_t* __res
 }
 
 int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, uint16_t* out, cudaStream_t st,
-                   const float* y_shared) {
+                   const float* y_shared, const uint8_t* dead, uint32_t* status) {
   const long long n = (long long)s->T * (s->H / 8);
   if (n == 0) return MOE_OK;
   const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);
-  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, st, y, row_of_slot, s->T, s->H, s->k, out, y_shared);
+  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, st, y, row_of_slot, s->T, s->H, s->k, out, y_shared,
+                    dead, status);
 }
 
 }  // namespace moe

@@ -170,7 +170,11 @@ __global__ void __launch_bounds__(kScrThreads, 1) router_screen_kernel(const __g
         tc_commit(&empty[stage]);
         if (++stage == kScrStages) { stage = 0; phase ^= 1; }
       }
-      if (ok) tc_commit(accb);
+      // the accumulator barrier is committed on every path: after an expired wait this thread
+      // itself waits on it (bounded, without the abort shortcut) so that no MMA it issued is still
+      // running when TMEM is released
+      tc_commit(accb);
+      if (!ok) mbar_wait(accb, 0, kScrWaitNs, nullptr, nullptr, 0);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -181,7 +185,8 @@ __global__ void __launch_bounds__(kScrThreads, 1) router_screen_kernel(const __g
     const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
     const int k = p.k;
     uint32_t okw = 1;
-    if (lane == 0) okw = mbar_wait(accb, 0, kScrWaitNs, abort_flag, p.status, DEV_TIMEOUT_ACCUM) ? 1u : 0u;
+    if (lane == 0)
+      okw = (mbar_wait(accb, 0, kScrWaitNs, abort_flag, p.status, DEV_TIMEOUT_ACCUM) && !*abort_flag) ? 1u : 0u;
     const bool ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
     tc_fence_after();
     // scratch (the stage ring is free now): lo[EP][128], lists[4][k][128], tau[128], count[128]
@@ -518,12 +523,7 @@ int launch_router_screen(const moe_shape* s, const uint16_t* x, const uint16_t* 
   rc = make_bf16_tmap(&tmw, wr, H, E, sp.EP);
   if (rc) return rc;
   const int smem = screen_smem_bytes(sp.EP, sp.k);
-  static int attr = 0;
-  if (attr < smem) {
-    if (cudaFuncSetAttribute(router_screen_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr = smem;
-  }
+  if (ensure_smem_limit((const void*)router_screen_kernel, smem)) return MOE_ERR_CUDA;
   rc = launch_pdl(router_screen_kernel, dim3(ceil_div(T, kScrRows)), dim3(kScrThreads), (size_t)smem, st, tmx, tmw,
                   sp);
   if (rc) return rc;
@@ -534,13 +534,7 @@ int launch_router_screen(const moe_shape* s, const uint16_t* x, const uint16_t* 
   rc = make_bf16_tmap(&tew, wr, kRouterChunk, E * NC, NC);
   if (rc) return rc;
   const size_t esmem = exact_smem_bytes(H);
-  static size_t eattr = 0;
-  if (eattr < esmem) {
-    if (cudaFuncSetAttribute(router_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)esmem) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-    eattr = esmem;
-  }
+  if (ensure_smem_limit((const void*)router_exact_kernel, (int)esmem)) return MOE_ERR_CUDA;
   const int eper_sm = ctas_per_sm_by_smem(esmem, 16);
   const int eg = (int)std::min<long long>(T, (long long)num_sms() * eper_sm);
   return launch_pdl(router_exact_kernel, dim3(eg), dim3(32), esmem, st, tex, tew, bias, cand, ncand, T, H, E, score,

@@ -29,9 +29,11 @@
  *  - Return value: MOE_OK or an moe_status code. Argument and shape checks happen on the host
  *    before any launch; on failure nothing is launched. Launch failures return MOE_ERR_CUDA.
  *  - Device-side waits are bounded (about one second); an expired wait records an error code in
- *    the first 4 bytes of the workspace, the kernel unwinds, and moe_check_device_status then
- *    returns MOE_ERR_TIMEOUT. Zero those 4 bytes once before first use (or call
- *    moe_check_device_status, which clears them).
+ *    the first 4 bytes of the workspace (the status word), the kernel unwinds, and
+ *    moe_check_device_status then returns MOE_ERR_TIMEOUT. Inputs that only the device can check
+ *    (an invalid anchor, a dead row that holds slots in the plan it was given) are recorded in the
+ *    same word and reported as MOE_ERR_DEVICE_INPUT. Zero those 4 bytes once before first use (or
+ *    call moe_check_device_status, which clears them).
  *  - bf16 tensors travel as uint16_t bit patterns.
  *  - Alignment (checked, MOE_ERR_INVALID_ARG otherwise): x, w_router, xq, hq, out, swiglu_debug
  *    16 bytes; xs, hs, topk_idx, topk_w 4 bytes; packed codes 32 bytes, packed scales 16 bytes.
@@ -94,7 +96,9 @@ typedef enum moe_status {
   MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* shape outside the supported set above               */
   MOE_ERR_WORKSPACE = 3,          /* workspace pointer null/misaligned or too small       */
   MOE_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed                    */
-  MOE_ERR_TIMEOUT = 5             /* a bounded device-side wait expired                  */
+  MOE_ERR_TIMEOUT = 5,            /* a bounded device-side wait expired                  */
+  MOE_ERR_DEVICE_INPUT = 6        /* an input checked on the device was invalid (anchor,  */
+                                  /* or a dead row holding slots in the plan)             */
 } moe_status;
 
 typedef struct moe_intermediates {
@@ -173,12 +177,33 @@ MOE_API int moe_w13_swiglu_grouped(const moe_shape* shape, const uint8_t* xq, co
 
 /* Down grouped GEMM and fixed-order weighted combine (TP4 profile README, "Experts" row):
  *   y[slot] = topk_w[slot] * (W2[e] h^[slot]) in fp32 (per-slot buffer in the workspace),
- *   out[t] = bf16_rne( ((y[t,0] + y[t,1]) + ...) ); rows with no live slot (dead) get +0.0.
- * w2 / w2_s are PACKED weights. */
+ *   out[t] = bf16_rne( ((y[t,0] + y[t,1]) + ...) ); dead rows get +0.0.
+ * w2 / w2_s are PACKED weights. dead (u8 [T] or NULL) is the mask the plan was made with: a row
+ * with dead[t] != 0 gets +0.0 whatever the plan says, and if the plan still gives it slots (a plan
+ * made without that mask) the status word records it (moe_check_device_status ->
+ * MOE_ERR_DEVICE_INPUT). With dead = NULL a row is dead when row_of_slot[t*k] == -1. This call is
+ * moe_w2_grouped followed by moe_combine on the workspace's per-slot buffer. */
 MOE_API int moe_w2_combine_grouped(const moe_shape* shape, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2,
                            const uint8_t* w2_s, const float* topk_w, const int32_t* expert_offsets,
-                           const int32_t* slot_of_row, const int32_t* row_of_slot, uint16_t* out, void* ws,
-                           size_t ws_bytes, void* stream);
+                           const int32_t* slot_of_row, const int32_t* row_of_slot, const uint8_t* dead,
+                           uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+/* The down-projection GEMM alone (the first half of moe_w2_combine_grouped), into a per-slot buffer
+ * the caller owns: y fp32 [T*k, H], 16-byte aligned; row t*k + j = topk_w[t, j] * (W2[e] h^) for
+ * every live slot (t, j), e = topk_idx[t, j]; rows of dead slots are not written. ws: a workspace
+ * of at least 256 bytes (its first 4 bytes are the status word; moe_workspace_bytes is not needed). */
+MOE_API int moe_w2_grouped(const moe_shape* shape, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2,
+                           const uint8_t* w2_s, const float* topk_w, const int32_t* expert_offsets,
+                           const int32_t* slot_of_row, float* y, void* ws, size_t ws_bytes, void* stream);
+
+/* The fixed-order combine alone (TP4 profile README, "Experts" row): out[t] = bf16_rne(((y[t*k] +
+ * y[t*k+1]) + ...) + y[t*k+k-1]) in fp32, slots in rank order, for each row t with
+ * row_of_slot[t*k] >= 0 and (dead == NULL or dead[t] == 0); every other row gets +0.0. y fp32
+ * [T*k, H] (16-byte aligned), row_of_slot i32 [T*k] (the router's), dead u8 [T] or NULL, out bf16
+ * [T, H]. A dead row that holds slots is recorded as for moe_w2_combine_grouped. ws: at least 256
+ * bytes, as for moe_w2_grouped. */
+MOE_API int moe_combine(const moe_shape* shape, const float* y, const int32_t* row_of_slot, const uint8_t* dead,
+                        uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
 /* The whole layer: route -> quant -> W13+SwiGLU+requant -> W2 -> combine, on one stream, no host
  * synchronisation and no allocation (capturable in a CUDA graph for a fixed shape).
@@ -195,8 +220,8 @@ MOE_API int moe_forward(const moe_shape* shape, const uint16_t* x, const uint16_
  *           experts (in a's rank order) and weights them with its own scores,
  *           w_j = score[t, e_j] / ((score[t, e_0] + score[t, e_1]) + ...). Row a must route itself.
  * An anchor outside [0, T) or pointing at an anchored row is ignored (that row routes itself) and
- * recorded in the workspace status word (moe_check_device_status then returns MOE_ERR_TIMEOUT, the
- * generic device-side error). Otherwise identical to moe_route_topk / moe_forward, which are these
+ * recorded in the workspace status word (moe_check_device_status then returns
+ * MOE_ERR_DEVICE_INPUT). Otherwise identical to moe_route_topk / moe_forward, which are these
  * calls with anchor = NULL. anchor must be 4-byte aligned. */
 MOE_API int moe_route_topk_anchored(const moe_shape* shape, const uint16_t* x, const uint16_t* w_router,
                                     const float* bias, const uint8_t* dead, const int32_t* anchor,
@@ -252,6 +277,16 @@ MOE_API int moe_forward_shared(const moe_shape* shape, const uint16_t* x, const 
  * hang, the context stays usable. Not part of the layer. */
 MOE_API int moe_selftest_timeout(void* ws, uint64_t limit_ns, void* stream);
 
+/* Rate probe of the block-scaled tensor-core instruction the grouped GEMMs use (tcgen05.mma
+ * kind::mxf8f6f4, E2M1 x E4M3 with UE8M0 scales per 32; "New Deepseek 4.1 flash recipe", post 6
+ * "How it works" item 1): one CTA per SM issues `iters` back-to-back M = 128, N = 256, K = 32 MMAs
+ * from operands resident in shared memory, with nothing else to do. The caller times the call with
+ * CUDA events on `stream`; *flops receives the multiply-add work (2 * 128 * 256 * 32 * iters *
+ * CTAs) and *ctas the grid. It is the denominator of the prefill GEMMs' tensor utilisation, not part
+ * of the layer. iters in [1, 2^24]; ws: at least 256 bytes, its first 4 bytes the status word. */
+MOE_API int moe_probe_mma_rate(int32_t iters, int32_t* ctas, int64_t* flops, void* ws, size_t ws_bytes,
+                               void* stream);
+
 /* Allocation-free variant of moe_route_topk, for callers that cannot allocate device memory:
  * engines that reserved all of HBM for their own pool at start-up, or code running inside a host
  * framework's callback where allocation is not allowed. It takes no workspace; its scratch lives in
@@ -268,7 +303,9 @@ MOE_API int moe_route_topk_noalloc(const moe_shape* shape, const uint16_t* x, co
                                    int32_t* row_of_slot, void* stream);
 
 /* Test/debug helper: synchronises `stream`, reads and clears the device status word at the start
- * of `ws`, and returns MOE_OK or MOE_ERR_TIMEOUT (MOE_ERR_CUDA if the stream itself failed). */
+ * of `ws`, and returns MOE_OK, MOE_ERR_TIMEOUT (an expired device-side wait) or
+ * MOE_ERR_DEVICE_INPUT (an input the device found invalid); MOE_ERR_CUDA if the stream itself
+ * failed. */
 MOE_API int moe_check_device_status(void* ws, void* stream);
 
 #ifdef __cplusplus

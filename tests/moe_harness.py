@@ -65,7 +65,7 @@ class GpuLayer:
         S = cfg.T * cfg.k
         dbg = torch.full((max(S, 1), cfg.I), float("nan"), dtype=torch.float32, device=self.x.device)
         hq, hs = B.moe_w13_swiglu_grouped(shp, xq, xs, self.layer.w13p, self.layer.w13sp, plan, ws, debug=dbg)
-        out = B.moe_w2_combine_grouped(shp, hq, hs, self.layer.w2p, self.layer.w2sp, plan, ws)
+        out = B.moe_w2_combine_grouped(shp, hq, hs, self.layer.w2p, self.layer.w2sp, plan, ws, dead=dead)
         B.moe_check_device_status(ws)
         return dict(plan=plan, xq=xq, xs=xs, hq=hq, hs=hs, dbg=dbg, out=out)
 

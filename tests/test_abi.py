@@ -40,8 +40,8 @@ def test_library_exports_every_declared_symbol(B):
 
 
 def test_status_strings(B):
-    for c in range(6):
-        assert B.lib.moe_status_string(c)
+    for c in range(7):
+        assert B.lib.moe_status_string(c) != b"unknown status"
     assert B.lib.moe_status_string(99) == b"unknown status"
 
 
@@ -69,7 +69,11 @@ def test_workspace_checks_on_host(B):
     assert B.lib.moe_w13_swiglu_grouped(ctypes.byref(shp), *([n] * 9), n, need, n) == B.MOE_ERR_WORKSPACE
     # misaligned / too small workspace (never dereferenced: checks precede any launch)
     fake = ctypes.c_void_p(0x1000 + 8)
-    assert B.lib.moe_w2_combine_grouped(ctypes.byref(shp), *([n] * 9), fake, need, n) == B.MOE_ERR_WORKSPACE
+    assert B.lib.moe_w2_combine_grouped(ctypes.byref(shp), *([n] * 10), fake, need, n) == B.MOE_ERR_WORKSPACE
+    # the split down projection / combine only need the status word, but it must be there
+    assert B.lib.moe_w2_grouped(ctypes.byref(shp), *([n] * 8), n, 256, n) == B.MOE_ERR_WORKSPACE
+    assert B.lib.moe_combine(ctypes.byref(shp), *([n] * 4), ctypes.c_void_p(0x1000), 128, n) == B.MOE_ERR_WORKSPACE
+    assert B.lib.moe_combine(ctypes.byref(shp), *([n] * 4), ctypes.c_void_p(0x1000), 256, n) == B.MOE_ERR_INVALID_ARG
     fake = ctypes.c_void_p(0x1000)
     assert B.lib.moe_forward(ctypes.byref(shp), *([n] * 9), None, fake, need - 256, n) == B.MOE_ERR_WORKSPACE
 

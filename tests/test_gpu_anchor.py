@@ -84,8 +84,10 @@ def test_invalid_anchors_are_ignored_and_reported():
     ws = B.alloc_workspace(shp)
     plan = B.moe_route_topk(shp, x.cuda(), wr.cuda(), torch.from_numpy(bias).cuda(), None, ws,
                             anchor=torch.from_numpy(anchor).cuda())
-    with pytest.raises(B.MoeError):
+    with pytest.raises(B.MoeError) as ei:
         B.moe_check_device_status(ws)
+    assert ei.value.code == B.MOE_ERR_DEVICE_INPUT      # an input error, not an expired wait
+    B.moe_check_device_status(ws)                      # the word was cleared
     fixed = anchor.copy()
     fixed[[3, 5]] = -1
     ref = M.route(x.float().numpy(), wr.float().numpy(), bias, k, None, fixed)

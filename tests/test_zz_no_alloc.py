@@ -38,9 +38,12 @@ def _same(a, b, S, Tk):
 @pytest.mark.gpu
 def test_noalloc_router_matches_workspace_router_on_consecutive_calls():
     from block_scaled_fp8_moe_gb300 import binding as B
-    # a larger call first, then a smaller one with dead rows: the second must not see the first's
-    # leftovers in the shared scratch
-    for (T, H, E, k, seed, dead_frac) in ((200, 512, 256, 8, 1, 0.0), (6, 4096, 256, 8, 2, 0.3)):
+    # a larger call first, then smaller ones with dead rows: a later call must not see an earlier
+    # one's leftovers in the shared scratch. The three sizes cover each pair of router kernels the
+    # two entry points pick (workspace / no-allocation): T = 200 screen + exact recompute / tiled,
+    # T = 6 decode / small, T = 40 decode / tiled.
+    for (T, H, E, k, seed, dead_frac) in ((200, 512, 256, 8, 1, 0.0), (6, 4096, 256, 8, 2, 0.3),
+                                          (40, 4096, 256, 8, 3, 0.2)):
         x, wr, bias, dead = _inputs(T, H, E, seed, dead_frac)
         shp = B.shape(T, H, E, k, 64)
         ws = B.alloc_workspace(shp)

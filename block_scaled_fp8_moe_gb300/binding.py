@@ -27,8 +27,11 @@ EXPORTED = [
     "moe_route_topk_noalloc", "moe_selftest_timeout", "moe_route_topk_anchored", "moe_forward_anchored",
     "moe_packed_shared_w13_bytes", "moe_packed_shared_w2_bytes", "moe_pack_shared_w13", "moe_pack_shared_w2",
     "moe_shared_workspace_bytes", "moe_forward_shared", "moe_dead_from_survival", "moe_w2_grouped", "moe_combine",
-    "moe_probe_mma_rate",
+    "moe_probe_mma_rate", "moe_quant_mxfp8_plan",
 ]
+
+MOE_FLAG_SWIGLU_DEBUG = 1
+MOE_FLAG_X_PLAN_ORDER = 2
 
 
 class MoeShape(ctypes.Structure):
@@ -62,6 +65,7 @@ lib.moe_packed_w2_bytes.restype = _SZ
 lib.moe_packed_w2_bytes.argtypes = [_SHP, ctypes.POINTER(_SZ)]
 lib.moe_quant_mxfp4.argtypes = [_I32, _I32, _P, _P, _P, _P]
 lib.moe_quant_mxfp8.argtypes = [_I32, _I32, _P, _P, _P, _P]
+lib.moe_quant_mxfp8_plan.argtypes = [_SHP] + [_P] * 6 + [_P]
 lib.moe_dead_from_survival.argtypes = [_I32, _P, ctypes.c_float, _P, _P]
 lib.moe_pack_w13.argtypes = [_SHP, _P, _P, _P, _P, _P]
 lib.moe_pack_w2.argtypes = [_SHP, _P, _P, _P, _P, _P]
@@ -174,6 +178,20 @@ def moe_quant_mxfp8(x: torch.Tensor, q: torch.Tensor | None = None, s: torch.Ten
     return q, s
 
 
+def moe_quant_mxfp8_plan(shp: MoeShape, x, plan: "Plan", xq_plan=None, xs_plan=None, xq=None, xs=None,
+                         stream=None):
+    """MXFP8 codes/scales written to plan rows ([T*k, H] / [T*k, H/32]); token order too if given."""
+    S = shp.T * shp.k
+    xq_plan = torch.empty(max(S, 1), shp.H, dtype=torch.uint8, device=x.device) if xq_plan is None else xq_plan
+    xs_plan = torch.empty(max(S, 1), shp.H // 32, dtype=torch.uint8, device=x.device) if xs_plan is None else xs_plan
+    _check(lib.moe_quant_mxfp8_plan(
+        ctypes.byref(shp), _ptr(x, torch.bfloat16, shp.T * shp.H, "x"), _ptr(plan.row_of_slot, torch.int32, S),
+        _ptr(xq_plan, torch.uint8, S * shp.H), _ptr(xs_plan, torch.uint8, S * shp.H // 32),
+        _ptr(xq, torch.uint8, shp.T * shp.H), _ptr(xs, torch.uint8, shp.T * shp.H // 32), _stream(stream)),
+        "moe_quant_mxfp8_plan")
+    return xq_plan, xs_plan
+
+
 SURVIVAL_THRESHOLD = 0.2
 
 
@@ -250,12 +268,14 @@ def moe_route_topk_noalloc(shp: MoeShape, x, w_router, bias, dead, plan: Plan | 
 
 def moe_w13_swiglu_grouped(shp: MoeShape, xq, xs, w13p, w13sp, plan: Plan, ws, hq=None, hs=None, debug=None,
                            stream=None):
+    """xq/xs in token order, or in plan order when shp.flags has MOE_FLAG_X_PLAN_ORDER."""
     S = shp.T * shp.k
     dev = xq.device
+    rows = S if shp.flags & MOE_FLAG_X_PLAN_ORDER else shp.T
     hq = torch.empty(max(S, 1), shp.I, dtype=torch.uint8, device=dev) if hq is None else hq
     hs = torch.empty(max(S, 1), hs_pitch(shp.I), dtype=torch.uint8, device=dev) if hs is None else hs
     _check(lib.moe_w13_swiglu_grouped(
-        ctypes.byref(shp), _ptr(xq, torch.uint8, shp.T * shp.H), _ptr(xs, torch.uint8, shp.T * shp.H // 32),
+        ctypes.byref(shp), _ptr(xq, torch.uint8, rows * shp.H), _ptr(xs, torch.uint8, rows * shp.H // 32),
         _ptr(w13p, torch.uint8), _ptr(w13sp, torch.uint8), _ptr(plan.expert_offsets), _ptr(plan.slot_of_row),
         _ptr(hq, torch.uint8, S * shp.I), _ptr(hs, torch.uint8, S * hs_pitch(shp.I)),
         _ptr(debug, torch.float32, S * shp.I), _ptr(ws), ws.numel(), _stream(stream)), "moe_w13_swiglu_grouped")

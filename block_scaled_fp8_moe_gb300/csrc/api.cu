@@ -46,9 +46,12 @@ extern "C" int moe_w13_swiglu_grouped(const moe_shape* s, const uint8_t* xq, con
       !aligned(swiglu_debug, 16))
     return MOE_ERR_INVALID_ARG;
   const Workspace L = workspace_layout(s);
+  const bool plan_order = (s->flags & MOE_FLAG_X_PLAN_ORDER) != 0;
+  uint8_t* xq_rows = plan_order ? const_cast<uint8_t*>(xq) : ws_ptr<uint8_t>(ws, L.xqp);
+  uint8_t* xs_rows = plan_order ? const_cast<uint8_t*>(xs) : ws_ptr<uint8_t>(ws, L.xsp);
   return launch_w13(s, xq, xs, w13, w13_s, expert_offsets, slot_of_row, hq, hs,
-                    (s->flags & 1) ? swiglu_debug : nullptr, ws_ptr<uint32_t>(ws, L.status),
-                    ws_ptr<uint8_t>(ws, L.xqp), ws_ptr<uint8_t>(ws, L.xsp), false, static_cast<cudaStream_t>(stream));
+                    (s->flags & MOE_FLAG_SWIGLU_DEBUG) ? swiglu_debug : nullptr, ws_ptr<uint32_t>(ws, L.status),
+                    xq_rows, xs_rows, plan_order, static_cast<cudaStream_t>(stream));
 }
 
 namespace {

@@ -70,6 +70,7 @@ struct GemmParams {
   // B side (activations)
   const uint8_t* bq;        // W13: xq [T, H];  W2: hq [S, I]
   const uint8_t* bs;        // W13: xs [T, H/32]; W2: hs [S, HS_PITCH]
+  int b_plan_rows;          // W13: 1 if bq/bs rows are plan rows (row p feeds plan row p), 0 if token rows
   int b_row_bytes;          // K in bytes (= elements)
   int b_scale_pitch;        // bytes per scale row
   // A side (packed weights)
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
         long long r = -1;
         if (c < nrows) {
           const int prow = row0 + c;
-          r = W13 ? (long long)(p.slot_of_row[prow] / p.k) : (long long)prow;
+          r = (W13 && !p.b_plan_rows) ? (long long)(p.slot_of_row[prow] / p.k) : (long long)prow;
         }
         s_rows[c] = r;
       }
@@ -790,9 +791,12 @@ int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const u
   gp.a_fp8 = fp8_weights ? 1 : 0;
   gp.bq = xq;
   gp.bs = xs;
-  if (pick_bn(s) >= 128 && plan_rows_ready) {
+  if (plan_rows_ready) {
+    // the activation rows already sit in plan order (wide tiles read them with TMA boxes, narrow
+    // tiles gather plan row p for column p)
     gp.bq = xq_plan;
     gp.bs = xs_plan;
+    gp.b_plan_rows = 1;
   } else if (pick_bn(s) >= 128) {
     // wide tiles read the token operand in plan order with TMA boxes: gather it once
     const long long n = (long long)s->T * s->k * (s->H / 16 + s->H / 128);
@@ -802,6 +806,7 @@ int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const u
     if (rc) return rc;
     gp.bq = xq_plan;
     gp.bs = xs_plan;
+    gp.b_plan_rows = 1;
   }
   gp.b_row_bytes = s->H;
   gp.b_scale_pitch = s->H / 32;

@@ -204,6 +204,19 @@ int launch_quant_mxfp8(int rows, int cols, const uint16_t* x, uint8_t* q, uint8_
 
 using namespace moe;
 
+extern "C" int moe_quant_mxfp8_plan(const moe_shape* sh, const uint16_t* x, const int32_t* row_of_slot,
+                                    uint8_t* xq_plan, uint8_t* xs_plan, uint8_t* xq, uint8_t* xs, void* stream) {
+  if (!sh) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(sh)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (sh->T == 0) return MOE_OK;
+  if (!x || !row_of_slot || !xq_plan || !xs_plan || (!xq) != (!xs)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(xq_plan) & 7) ||
+      (reinterpret_cast<uintptr_t>(xq) & 7) || (reinterpret_cast<uintptr_t>(row_of_slot) & 3))
+    return MOE_ERR_INVALID_ARG;
+  return launch_quant_mxfp8_plan(sh->T, sh->H, sh->k, x, xq, xs, row_of_slot, xq_plan, xs_plan,
+                                 static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int moe_quant_mxfp8(int32_t rows, int32_t cols, const uint16_t* x, uint8_t* q, uint8_t* s,
                                void* stream) {
   if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;

@@ -87,8 +87,13 @@ typedef struct moe_shape {
   int32_t E;      /* experts                                          */
   int32_t k;      /* experts per row                                  */
   int32_t I;      /* expert intermediate size                         */
-  int32_t flags;  /* bit 0: W13 writes the fp32 SwiGLU debug output   */
+  int32_t flags;  /* MOE_FLAG_* bits, read by moe_w13_swiglu_grouped  */
 } moe_shape;
+
+/* moe_shape.flags */
+#define MOE_FLAG_SWIGLU_DEBUG 1   /* W13 writes the fp32 SwiGLU values to swiglu_debug              */
+#define MOE_FLAG_X_PLAN_ORDER 2   /* xq / xs given to W13 hold plan rows ([T*k, H] / [T*k, H/32]:
+                                     row p = the token of plan row p), as moe_quant_mxfp8_plan writes */
 
 typedef enum moe_status {
   MOE_OK = 0,
@@ -165,11 +170,22 @@ MOE_API int moe_dead_from_survival(int32_t T, const float* p_survive, float thre
  *   code = E4M3 round-to-nearest-even of x * 2^-s (never saturates). cols % 32 == 0. */
 MOE_API int moe_quant_mxfp8(int32_t rows, int32_t cols, const uint16_t* x, uint8_t* q, uint8_t* s, void* stream);
 
+/* The same quantisation written in plan order, the form the wide-tile W13 reads (and what
+ * moe_forward runs for large batches): the codes and scale bytes of token t go to plan rows
+ * row_of_slot[t*k + j] of xq_plan u8 [T*k, H] / xs_plan u8 [T*k, H/32] (slots with -1 are skipped;
+ * rows past the live slots are left untouched), and also to xq / xs in token order when those are
+ * non-NULL (both or neither). row_of_slot as written by moe_route_topk. x 16-byte aligned, xq_plan
+ * and xq 8-byte aligned. */
+MOE_API int moe_quant_mxfp8_plan(const moe_shape* shape, const uint16_t* x, const int32_t* row_of_slot,
+                                 uint8_t* xq_plan, uint8_t* xs_plan, uint8_t* xq, uint8_t* xs, void* stream);
+
 /* Gate/up grouped GEMM fused with SwiGLU and MXFP8 requantisation, for every live slot:
  *   g = Wg[e] x^, u = Wu[e] x^ (block-scaled FP8 x FP4 tensor-core MMA, fp32 accumulate),
  *   a = g * sigmoid(g) * u (fp32), then per 32 along I: the MXFP8 rule of moe_quant_mxfp8.
- * Writes hq/hs rows in plan order (row p = slot slot_of_row[p]); swiglu_debug (nullable) gets a.
- * expert_offsets / slot_of_row as produced by moe_route_topk. w13 / w13_s are PACKED weights. */
+ * Writes hq/hs rows in plan order (row p = slot slot_of_row[p]); swiglu_debug (nullable, written
+ * when shape->flags has MOE_FLAG_SWIGLU_DEBUG) gets a. xq / xs are token rows [T, H] / [T, H/32],
+ * or plan rows [T*k, H] / [T*k, H/32] with MOE_FLAG_X_PLAN_ORDER. expert_offsets / slot_of_row as
+ * produced by moe_route_topk. w13 / w13_s are PACKED weights. */
 MOE_API int moe_w13_swiglu_grouped(const moe_shape* shape, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13,
                            const uint8_t* w13_s, const int32_t* expert_offsets, const int32_t* slot_of_row,
                            uint8_t* hq, uint8_t* hs, float* swiglu_debug, void* ws, size_t ws_bytes,

@@ -57,7 +57,7 @@ class GpuLayer:
         """Route -> quant -> W13 (debug on) -> W2+combine through the four step entry points."""
         B = self.B
         cfg = self.cfg
-        shp = self.shape(flags=1)
+        shp = self.shape(flags=B.MOE_FLAG_SWIGLU_DEBUG)
         ws = B.alloc_workspace(shp)
         dead = self.dead if use_dead else None
         plan = B.moe_route_topk(shp, self.x, self.wr, self.bias, dead, ws)

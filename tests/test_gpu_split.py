@@ -55,3 +55,29 @@ def test_dead_mask_on_a_plan_made_without_it():
     assert int(flagged.sum()) == 6
     assert torch.all(masked[flagged] == 0) and not torch.any(torch.signbit(masked[flagged].float()))
     assert torch.equal(masked[~flagged], plain[~flagged])
+
+
+@pytest.mark.parametrize("name,T,Hd,E,k,I", [("p37", 37, 512, 16, 4, 192), ("p640", 640, 256, 4, 2, 1024)])
+def test_w13_on_plan_order_rows_equals_token_order(name, T, Hd, E, k, I):
+    """moe_quant_mxfp8_plan + MOE_FLAG_X_PLAN_ORDER (what moe_forward runs for wide tiles) against
+    token-order codes: plan rows are copies of their tokens' codes, and W13 gives the same bits."""
+    from block_scaled_fp8_moe_gb300 import binding as B
+    inp = synth.make_inputs_cpu(synth.custom(name, T, Hd, E, k, I, seed=T + 11, dead_frac=0.2))
+    g = H.GpuLayer(inp)
+    shp = g.shape()
+    ws = B.alloc_workspace(shp)
+    plan = B.moe_route_topk(shp, g.x, g.wr, g.bias, g.dead, ws)
+    xq, xs = B.moe_quant_mxfp8(g.x)
+    xq2 = torch.empty_like(xq)
+    xs2 = torch.empty_like(xs)
+    xqp, xsp = B.moe_quant_mxfp8_plan(shp, g.x, plan, xq=xq2, xs=xs2)
+    S = int(plan.expert_offsets[-1].item())
+    tok = (plan.slot_of_row[:S] // k).long()
+    assert torch.equal(xq2, xq) and torch.equal(xs2, xs)
+    assert torch.equal(xqp[:S], xq[tok]) and torch.equal(xsp[:S], xs[tok])
+    hq, hs = B.moe_w13_swiglu_grouped(shp, xq, xs, g.layer.w13p, g.layer.w13sp, plan, ws)
+    shp_p = g.shape(flags=B.MOE_FLAG_X_PLAN_ORDER)
+    hq2, hs2 = B.moe_w13_swiglu_grouped(shp_p, xqp, xsp, g.layer.w13p, g.layer.w13sp, plan, ws)
+    B.moe_check_device_status(ws)
+    assert torch.equal(hq[:S], hq2[:S])
+    assert torch.equal(hs[:S, : I // 32], hs2[:S, : I // 32])

@@ -584,7 +584,7 @@ def measure(cfg, args, gpu, world, headline: bool, peak_info=None):
         ev["w2"][i][1].record(stream)
         gpu.flush_l2(float(i) + 0.75)
         ev["combine"][i][0].record(stream)
-        B.moe_combine(shp, y, plan.row_of_slot, ws, dead=dead, out=out)
+        B.moe_combine(shp, y, plan, ws, dead=dead, out=out)
         ev["combine"][i][1].record(stream)
     torch.cuda.synchronize()
     B.moe_check_device_status(ws)
@@ -647,7 +647,7 @@ def measure(cfg, args, gpu, world, headline: bool, peak_info=None):
         rec["w2_roofline"] = {"bound": "tensor", "achieved": round(a2, 1), "peak": pk["tflops"], "unit": "TFLOP/s",
                               "frac": round(a2 / pk["tflops"], 4), "alg_flops_per_launch": f2,
                               "launch_ms": round(kms["w2"], 5)}
-        ystep = 2 * 4 * live_slots * cfg.H + 2 * cfg.T * cfg.H
+        ystep = 4 * live_slots * cfg.H + 2 * cfg.T * cfg.H + 8 * live_slots
         rec["combine_hbm"] = {"bytes_per_launch": ystep,
                               "achieved_gbs": round(ystep / (kms["combine"] * 1e-3) / 1e9, 1)}
         lf = (f13 + f2) / (ms_per_step * 1e-3) / 1e12

@@ -72,8 +72,8 @@ lib.moe_pack_w2.argtypes = [_SHP, _P, _P, _P, _P, _P]
 lib.moe_route_topk.argtypes = [_SHP] + [_P] * 10 + [_P, _SZ, _P]
 lib.moe_w13_swiglu_grouped.argtypes = [_SHP] + [_P] * 9 + [_P, _SZ, _P]
 lib.moe_w2_combine_grouped.argtypes = [_SHP] + [_P] * 10 + [_P, _SZ, _P]
-lib.moe_w2_grouped.argtypes = [_SHP] + [_P] * 8 + [_P, _SZ, _P]
-lib.moe_combine.argtypes = [_SHP] + [_P] * 4 + [_P, _SZ, _P]
+lib.moe_w2_grouped.argtypes = [_SHP] + [_P] * 7 + [_P, _SZ, _P]
+lib.moe_combine.argtypes = [_SHP] + [_P] * 5 + [_P, _SZ, _P]
 lib.moe_probe_mma_rate.argtypes = [_I32, ctypes.POINTER(_I32), ctypes.POINTER(ctypes.c_int64), _P, _SZ, _P]
 lib.moe_forward.argtypes = [_SHP] + [_P] * 9 + [ctypes.POINTER(MoeIntermediates), _P, _SZ, _P]
 lib.moe_check_device_status.argtypes = [_P, _P]
@@ -294,22 +294,23 @@ def moe_w2_combine_grouped(shp: MoeShape, hq, hs, w2p, w2sp, plan: Plan, ws, out
 
 
 def moe_w2_grouped(shp: MoeShape, hq, hs, w2p, w2sp, plan: Plan, ws, y=None, stream=None):
-    """Down-projection GEMM alone: per-slot fp32 rows y [T*k, H] (rows of dead slots untouched)."""
+    """Down-projection GEMM alone: fp32 rows y [T*k, H] in plan order, before the routing weight."""
     S = shp.T * shp.k
     y = torch.empty(max(S, 1), shp.H, dtype=torch.float32, device=hq.device) if y is None else y
     _check(lib.moe_w2_grouped(
         ctypes.byref(shp), _ptr(hq, torch.uint8), _ptr(hs, torch.uint8), _ptr(w2p, torch.uint8),
-        _ptr(w2sp, torch.uint8), _ptr(plan.topk_w), _ptr(plan.expert_offsets), _ptr(plan.slot_of_row),
+        _ptr(w2sp, torch.uint8), _ptr(plan.expert_offsets), _ptr(plan.slot_of_row),
         _ptr(y, torch.float32, S * shp.H, "y"), _ptr(ws), ws.numel(), _stream(stream)), "moe_w2_grouped")
     return y
 
 
-def moe_combine(shp: MoeShape, y, row_of_slot, ws, dead=None, out=None, stream=None):
-    """Fixed-order combine alone: out[t] = bf16(((y[t,0] + y[t,1]) + ...)), dead rows +0."""
+def moe_combine(shp: MoeShape, y, plan: Plan, ws, dead=None, out=None, stream=None):
+    """Fixed-order combine alone: out[t] = bf16(((w_0 y[r_0] + w_1 y[r_1]) + ...)), dead rows +0."""
     out = torch.empty(shp.T, shp.H, dtype=torch.bfloat16, device=y.device) if out is None else out
     _check(lib.moe_combine(
         ctypes.byref(shp), _ptr(y, torch.float32, shp.T * shp.k * shp.H, "y"),
-        _ptr(row_of_slot, torch.int32, shp.T * shp.k, "row_of_slot"), _ptr(dead, torch.uint8, shp.T, "dead"),
+        _ptr(plan.topk_w, torch.float32, shp.T * shp.k, "topk_w"),
+        _ptr(plan.row_of_slot, torch.int32, shp.T * shp.k, "row_of_slot"), _ptr(dead, torch.uint8, shp.T, "dead"),
         _ptr(out, torch.bfloat16, shp.T * shp.H, "out"), _ptr(ws), ws.numel(), _stream(stream)), "moe_combine")
     return out
 

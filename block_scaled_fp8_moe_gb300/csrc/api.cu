@@ -57,11 +57,10 @@ extern "C" int moe_w13_swiglu_grouped(const moe_shape* s, const uint8_t* xq, con
 namespace {
 
 // Argument checks of the down projection's GEMM, shared by the entry points that run it.
-int w2_args_ok(const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2_s, const float* topk_w,
+int w2_args_ok(const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2_s,
                const int32_t* expert_offsets, const int32_t* slot_of_row) {
-  if (!hq || !hs || !w2 || !w2_s || !topk_w || !expert_offsets || !slot_of_row) return MOE_ERR_INVALID_ARG;
-  if (!aligned(hq, 16) || !aligned(hs, 4) || !aligned(w2, 32) || !aligned(w2_s, 16) || !aligned(topk_w, 4))
-    return MOE_ERR_INVALID_ARG;
+  if (!hq || !hs || !w2 || !w2_s || !expert_offsets || !slot_of_row) return MOE_ERR_INVALID_ARG;
+  if (!aligned(hq, 16) || !aligned(hs, 4) || !aligned(w2, 32) || !aligned(w2_s, 16)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -82,43 +81,44 @@ extern "C" int moe_w2_combine_grouped(const moe_shape* s, const uint8_t* hq, con
   int rc = ws_check(s, ws, ws_bytes);
   if (rc) return rc;
   if (s->T == 0) return MOE_OK;
-  rc = w2_args_ok(hq, hs, w2, w2_s, topk_w, expert_offsets, slot_of_row);
+  rc = w2_args_ok(hq, hs, w2, w2_s, expert_offsets, slot_of_row);
   if (rc) return rc;
-  if (!row_of_slot || !out || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  if (!topk_w || !row_of_slot || !out || !aligned(topk_w, 4) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
   const Workspace L = workspace_layout(s);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* y = ws_ptr<float>(ws, L.y);
   uint32_t* status = ws_ptr<uint32_t>(ws, L.status);
-  rc = launch_w2(s, hq, hs, w2, w2_s, topk_w, expert_offsets, slot_of_row, y, status, st);
+  rc = launch_w2(s, hq, hs, w2, w2_s, expert_offsets, slot_of_row, y, status, st);
   if (rc) return rc;
-  return launch_combine(s, y, row_of_slot, out, st, nullptr, dead, status);
+  return launch_combine(s, y, topk_w, row_of_slot, out, st, nullptr, dead, status);
 }
 
 extern "C" int moe_w2_grouped(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2,
-                              const uint8_t* w2_s, const float* topk_w, const int32_t* expert_offsets,
-                              const int32_t* slot_of_row, float* y, void* ws, size_t ws_bytes, void* stream) {
+                              const uint8_t* w2_s, const int32_t* expert_offsets, const int32_t* slot_of_row,
+                              float* y, void* ws, size_t ws_bytes, void* stream) {
   if (!s) return MOE_ERR_INVALID_ARG;
   if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
   int rc = status_ws_ok(ws, ws_bytes);
   if (rc) return rc;
   if (s->T == 0) return MOE_OK;
-  rc = w2_args_ok(hq, hs, w2, w2_s, topk_w, expert_offsets, slot_of_row);
+  rc = w2_args_ok(hq, hs, w2, w2_s, expert_offsets, slot_of_row);
   if (rc) return rc;
   if (!y || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
-  return launch_w2(s, hq, hs, w2, w2_s, topk_w, expert_offsets, slot_of_row, y, static_cast<uint32_t*>(ws),
+  return launch_w2(s, hq, hs, w2, w2_s, expert_offsets, slot_of_row, y, static_cast<uint32_t*>(ws),
                    static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int moe_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, const uint8_t* dead,
-                           uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+extern "C" int moe_combine(const moe_shape* s, const float* y, const float* topk_w, const int32_t* row_of_slot,
+                           const uint8_t* dead, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
   if (!s) return MOE_ERR_INVALID_ARG;
   if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
   int rc = status_ws_ok(ws, ws_bytes);
   if (rc) return rc;
   if (s->T == 0) return MOE_OK;
-  if (!y || !row_of_slot || !out || !aligned(y, 16) || !aligned(row_of_slot, 4) || !aligned(out, 16))
+  if (!y || !topk_w || !row_of_slot || !out || !aligned(y, 16) || !aligned(topk_w, 4) || !aligned(row_of_slot, 4) ||
+      !aligned(out, 16))
     return MOE_ERR_INVALID_ARG;
-  return launch_combine(s, y, row_of_slot, out, static_cast<cudaStream_t>(stream), nullptr, dead,
+  return launch_combine(s, y, topk_w, row_of_slot, out, static_cast<cudaStream_t>(stream), nullptr, dead,
                         static_cast<uint32_t*>(ws));
 }
 
@@ -132,10 +132,10 @@ extern "C" int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t
 
 namespace {
 
-// Shared-expert scratch: identity plan (one expert, row t = token t, weight 1) and the expert's
-// intermediates. Every piece 256-byte aligned.
+// Shared-expert scratch: identity plan (one expert, row t = token t) and the expert's
+// intermediates; its rows enter the combine with weight 1. Every piece 256-byte aligned.
 struct SharedWs {
-  size_t offsets, slot, ones, hq, hs, y, total;
+  size_t offsets, slot, hq, hs, y, total;
 };
 
 SharedWs shared_layout(int T, int H, int Is) {
@@ -144,7 +144,6 @@ SharedWs shared_layout(int T, int H, int Is) {
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + (bytes ? bytes : 1), 256); return o; };
   w.offsets = take(2 * 4);
   w.slot = take((size_t)T * 4);
-  w.ones = take((size_t)T * 4);
   w.hq = take((size_t)T * Is);
   w.hs = take((size_t)T * hs_pitch(Is));
   w.y = take((size_t)T * H * 4);
@@ -152,12 +151,8 @@ SharedWs shared_layout(int T, int H, int Is) {
   return w;
 }
 
-__global__ void shared_plan_kernel(int T, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
-                                   float* __restrict__ ones) {
-  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
-    slot[t] = t;
-    ones[t] = 1.0f;
-  }
+__global__ void shared_plan_kernel(int T, int32_t* __restrict__ offsets, int32_t* __restrict__ slot) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) slot[t] = t;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     offsets[0] = 0;
     offsets[1] = T;
@@ -246,18 +241,17 @@ int forward_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router
     }
     int32_t* s_off = ws_ptr<int32_t>(shared->ws, SL.offsets);
     int32_t* s_slot = ws_ptr<int32_t>(shared->ws, SL.slot);
-    float* s_ones = ws_ptr<float>(shared->ws, SL.ones);
     uint8_t* s_hq = ws_ptr<uint8_t>(shared->ws, SL.hq);
     uint8_t* s_hs = ws_ptr<uint8_t>(shared->ws, SL.hs);
     y_shared = ws_ptr<float>(shared->ws, SL.y);
     const int blocks = (int)std::min<long long>((s->T + 255) / 256, (long long)num_sms() * 4);
-    shared_plan_kernel<<<blocks, 256, 0, side>>>(s->T, s_off, s_slot, s_ones);
+    shared_plan_kernel<<<blocks, 256, 0, side>>>(s->T, s_off, s_slot);
     rc = launch_status();
     if (rc) return rc;
     rc = launch_w13(&ss, xq, xs, shared->w13, shared->w13_s, s_off, s_slot, s_hq, s_hs, nullptr, status, xq, xs,
                     true, side, true);
     if (rc) return rc;
-    rc = launch_w2(&ss, s_hq, s_hs, shared->w2, shared->w2_s, s_ones, s_off, s_slot, y_shared, status, side, true);
+    rc = launch_w2(&ss, s_hq, s_hs, shared->w2, shared->w2_s, s_off, s_slot, y_shared, status, side, true);
     if (rc) return rc;
     if (side != st) {
       if (cudaEventCreateWithFlags(&ev_join, cudaEventDisableTiming) != cudaSuccess) return MOE_ERR_CUDA;
@@ -268,13 +262,13 @@ int forward_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router
     }
   }
   rc = launch_w13(s, xq, xs, w13, w13_s, offsets, slot_of_row, hq, hs, im.swiglu, status, xqp, xsp, plan_rows, st);
-  if (!rc) rc = launch_w2(s, hq, hs, w2, w2_s, topk_w, offsets, slot_of_row, y, status, st);
+  if (!rc) rc = launch_w2(s, hq, hs, w2, w2_s, offsets, slot_of_row, y, status, st);
   if (ev_join) {
     if (!rc && cudaStreamWaitEvent(st, ev_join, 0) != cudaSuccess) rc = MOE_ERR_CUDA;
     cudaEventDestroy(ev_join);
   }
   if (rc) return rc;
-  return launch_combine(s, y, row_of_slot, out, st, y_shared, dead, status);
+  return launch_combine(s, y, topk_w, row_of_slot, out, st, y_shared, dead, status);
 }
 
 }  // namespace

@@ -193,13 +193,15 @@ int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const u
                const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
                uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, bool plan_rows_ready, cudaStream_t st,
                bool fp8_weights = false);
+// y: plan-order rows W2[e] h^ (fp32, before the routing weight)
 int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2s,
-              const float* topk_w, const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
-              cudaStream_t st, bool fp8_weights = false);
+              const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status, cudaStream_t st,
+              bool fp8_weights = false);
+// out[t] = bf16(((w_0 y[r_0] + w_1 y[r_1]) + ...)), r_j = row_of_slot[t k + j], w_j = topk_w[t k + j];
 // y_shared (nullable): a per-token row added after the routed slots (the shared expert); dead
 // (nullable): rows forced to +0.0, a forced row that holds slots is recorded in *status
-int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, uint16_t* out, cudaStream_t st,
-                   const float* y_shared, const uint8_t* dead, uint32_t* status);
+int launch_combine(const moe_shape* s, const float* y, const float* topk_w, const int32_t* row_of_slot,
+                   uint16_t* out, cudaStream_t st, const float* y_shared, const uint8_t* dead, uint32_t* status);
 // Large-T router: certified tensor-core screen + exact recompute of the surviving experts; writes
 // the same score/key rows as the exact router for every expert that can be selected.
 bool router_screen_supported(const moe_shape* s);

@@ -87,8 +87,7 @@ struct GemmParams {
   uint8_t* hs;
   int hs_pitch;
   float* dbg;
-  // W2 outputs
-  const float* topk_w;
+  // W2 output: per-slot rows in plan order, before the routing weight
   float* y;
   uint32_t* status;
 };
@@ -505,19 +504,6 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
       decode(w, e, m, nt, row0, nrows, tw);
       const int acc = (NACC == 2) ? (it & 1) : 0;
       const int use = (NACC == 2) ? (it >> 1) : it;
-      // W2: the slot and routing weight of every column of this tile, one coalesced load per lane
-      // (issued before the accumulator wait so its latency hides behind it)
-      int w2_slot[(BN + 31) / 32];
-      float w2_wgt[(BN + 31) / 32];
-      if constexpr (!W13) {
-#pragma unroll
-        for (int i = 0; i < (BN + 31) / 32; ++i) {
-          const int col = lane + 32 * i;
-          w2_slot[i] = col < nrows ? p.slot_of_row[row0 + col] : 0;
-        }
-#pragma unroll
-        for (int i = 0; i < (BN + 31) / 32; ++i) w2_wgt[i] = (lane + 32 * i) < nrows ? p.topk_w[w2_slot[i]] : 0.f;
-      }
       if (ok) ok = warp_wait(&acc_full[acc], use & 1, abort_flag, p.status, DEV_TIMEOUT_ACCUM);
       tc_fence_after();
       const uint32_t d_tmem = tmem + (uint32_t)(acc * L::kAccStride);
@@ -594,24 +580,13 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
             named_bar_sync(bar_id, 128);
           } else {
             if (ok) {
+              // plan row row0 + c of the per-slot buffer, features 128 m + 32 q + lane: each store
+              // instruction writes 128 contiguous bytes (the routing weight is applied by the combine)
               const int feat = 128 * m + 32 * q + lane;
-              // this chunk's 16 columns lie in one 32-column group (c0 is a multiple of 16)
-              int g_slot = 0;
-              float g_wgt = 0.f;
+              float* yrow = p.y + (size_t)(row0 + c0) * p.H + feat;
 #pragma unroll
-              for (int i = 0; i < (BN + 31) / 32; ++i)
-                if (i == (c0 >> 5)) {
-                  g_slot = w2_slot[i];
-                  g_wgt = w2_wgt[i];
-                }
-#pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const int col = c0 + c;
-                // slot and routing weight of column col, loaded once per tile by lane col % 32
-                const int slot = __shfl_sync(0xffffffffu, g_slot, col & 31);
-                const float wgt = __shfl_sync(0xffffffffu, g_wgt, col & 31);
-                if (col < nrows) p.y[(size_t)slot * p.H + feat] = __fmul_rn(wgt, __uint_as_float(r[c]));
-              }
+              for (int c = 0; c < 16; ++c)
+                if (c0 + c < nrows) yrow[(size_t)c * p.H] = __uint_as_float(r[c]);
             }
           }
         }
@@ -830,7 +805,7 @@ int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const u
 }
 
 int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2s,
-              const float* topk_w, const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
+              const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
               cudaStream_t st, bool fp8_weights) {
   if (s->T == 0) return MOE_OK;
   GemmParams gp{};
@@ -850,7 +825,6 @@ int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const ui
   gp.MT = s->H / 128;
   gp.I = s->I;
   gp.H = s->H;
-  gp.topk_w = topk_w;
   gp.y = y;
   gp.status = status;
   return launch_gemm<false>(s, w2, gp, st);

@@ -798,13 +798,15 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
 }
 
 // ---------------------------------------------------------------------------------------------
-// Combine: out[t] = bf16_rne(((y[t,0] + y[t,1]) + ...) + y[t,k-1]) in fp32, slots in rank order,
-// then + y_shared[t] when a shared expert ran; rows without live slots, and rows the caller's dead
-// mask flags, get +0.0 (a flagged row that still holds slots is recorded in the status word). 8
-// hidden elements per thread.
+// Combine: out[t] = bf16_rne(((y_0 + y_1) + ...) + y_{k-1}) in fp32, slots in rank order, where
+// y_j = topk_w[t, j] * y[row_of_slot[t k + j]] (one fp32 rounding: the down projection's plan-order
+// rows arrive before their routing weight); then + y_shared[t] when a shared expert ran. Rows
+// without live slots, and rows the caller's dead mask flags, get +0.0 (a flagged row that still
+// holds slots is recorded in the status word). 8 hidden elements per thread.
 // ---------------------------------------------------------------------------------------------
-__global__ void combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ row_of_slot, int T, int H,
-                               int k, uint16_t* __restrict__ out, const float* __restrict__ y_shared,
+__global__ void combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
+                               const int32_t* __restrict__ row_of_slot, int T, int H, int k,
+                               uint16_t* __restrict__ out, const float* __restrict__ y_shared,
                                const uint8_t* __restrict__ dead, uint32_t* status) {
   pdl_trigger();
   pdl_wait();
@@ -821,11 +823,16 @@ __global__ void combine_kernel(const float* __restrict__ y, const int32_t* __res
     const bool live = held && !flagged;
     if (live) {
       for (int j = 0; j < k; ++j) {
-        const float4* yp = reinterpret_cast<const float4*>(y + ((size_t)t * k + j) * H) + 2 * h8;
+        const int r = __ldg(row_of_slot + (size_t)t * k + j);
+        const float w = __ldg(topk_w + (size_t)t * k + j);
+        const float4* yp = reinterpret_cast<const float4*>(y + (size_t)r * H) + 2 * h8;
         const float4 a = __ldg(yp), b = __ldg(yp + 1);
         const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = (j == 0) ? v[q] : __fadd_rn(acc[q], v[q]);
+        for (int q = 0; q < 8; ++q) {
+          const float wv = __fmul_rn(w, v[q]);
+          acc[q] = (j == 0) ? wv : __fadd_rn(acc[q], wv);
+        }
       }
       if (y_shared) {
         const float4* yp = reinterpret_cast<const float4*>(y_shared + (size_t)t * H) + 2 * h8;
@@ -846,13 +853,13 @@ __global__ void combine_kernel(const float* __restrict__ y, const int32_t* __res
   }
 }
 
-int launch_combine(const moe_shape* s, const float* y, const int32_t* row_of_slot, uint16_t* out, cudaStream_t st,
-                   const float* y_shared, const uint8_t* dead, uint32_t* status) {
+int launch_combine(const moe_shape* s, const float* y, const float* topk_w, const int32_t* row_of_slot,
+                   uint16_t* out, cudaStream_t st, const float* y_shared, const uint8_t* dead, uint32_t* status) {
   const long long n = (long long)s->T * (s->H / 8);
   if (n == 0) return MOE_OK;
   const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);
-  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, st, y, row_of_slot, s->T, s->H, s->k, out, y_shared,
-                    dead, status);
+  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, st, y, topk_w, row_of_slot, s->T, s->H, s->k, out,
+                    y_shared, dead, status);
 }
 
 }  // namespace moe

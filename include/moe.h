@@ -192,8 +192,9 @@ MOE_API int moe_w13_swiglu_grouped(const moe_shape* shape, const uint8_t* xq, co
                            void* stream);
 
 /* Down grouped GEMM and fixed-order weighted combine (TP4 profile README, "Experts" row):
- *   y[slot] = topk_w[slot] * (W2[e] h^[slot]) in fp32 (per-slot buffer in the workspace),
- *   out[t] = bf16_rne( ((y[t,0] + y[t,1]) + ...) ); dead rows get +0.0.
+ *   per slot (t, j) with plan row p: y_j = topk_w[t, j] * (W2[e] h^[p]) in fp32 (the product
+ *   W2[e] h^[p] sits in a per-slot buffer in the workspace, one fp32 multiply by the weight),
+ *   out[t] = bf16_rne( ((y_0 + y_1) + ...) ), slots in rank order; dead rows get +0.0.
  * w2 / w2_s are PACKED weights. dead (u8 [T] or NULL) is the mask the plan was made with: a row
  * with dead[t] != 0 gets +0.0 whatever the plan says, and if the plan still gives it slots (a plan
  * made without that mask) the status word records it (moe_check_device_status ->
@@ -205,21 +206,23 @@ MOE_API int moe_w2_combine_grouped(const moe_shape* shape, const uint8_t* hq, co
                            uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
 /* The down-projection GEMM alone (the first half of moe_w2_combine_grouped), into a per-slot buffer
- * the caller owns: y fp32 [T*k, H], 16-byte aligned; row t*k + j = topk_w[t, j] * (W2[e] h^) for
- * every live slot (t, j), e = topk_idx[t, j]; rows of dead slots are not written. ws: a workspace
- * of at least 256 bytes (its first 4 bytes are the status word; moe_workspace_bytes is not needed). */
+ * the caller owns, in plan order and before the routing weight: y fp32 [T*k, H], 16-byte aligned;
+ * row p (p < live slots) = W2[e] h^[p], e the expert of plan row p; rows past the live slots are
+ * not written. ws: a workspace of at least 256 bytes (its first 4 bytes are the status word;
+ * moe_workspace_bytes is not needed). */
 MOE_API int moe_w2_grouped(const moe_shape* shape, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2,
-                           const uint8_t* w2_s, const float* topk_w, const int32_t* expert_offsets,
-                           const int32_t* slot_of_row, float* y, void* ws, size_t ws_bytes, void* stream);
+                           const uint8_t* w2_s, const int32_t* expert_offsets, const int32_t* slot_of_row,
+                           float* y, void* ws, size_t ws_bytes, void* stream);
 
-/* The fixed-order combine alone (TP4 profile README, "Experts" row): out[t] = bf16_rne(((y[t*k] +
- * y[t*k+1]) + ...) + y[t*k+k-1]) in fp32, slots in rank order, for each row t with
- * row_of_slot[t*k] >= 0 and (dead == NULL or dead[t] == 0); every other row gets +0.0. y fp32
- * [T*k, H] (16-byte aligned), row_of_slot i32 [T*k] (the router's), dead u8 [T] or NULL, out bf16
- * [T, H]. A dead row that holds slots is recorded as for moe_w2_combine_grouped. ws: at least 256
- * bytes, as for moe_w2_grouped. */
-MOE_API int moe_combine(const moe_shape* shape, const float* y, const int32_t* row_of_slot, const uint8_t* dead,
-                        uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+/* The fixed-order combine alone (TP4 profile README, "Experts" row): with r_j = row_of_slot[t*k+j]
+ * and y_j = topk_w[t, j] * y[r_j] (fp32, one rounding), out[t] = bf16_rne(((y_0 + y_1) + ...) +
+ * y_{k-1}) in fp32, slots in rank order, for each row t with row_of_slot[t*k] >= 0 and (dead ==
+ * NULL or dead[t] == 0); every other row gets +0.0. y fp32 [T*k, H] as moe_w2_grouped writes it
+ * (16-byte aligned), topk_w f32 [T, k] and row_of_slot i32 [T*k] as the router writes them, dead
+ * u8 [T] or NULL, out bf16 [T, H]. A dead row that holds slots is recorded as for
+ * moe_w2_combine_grouped. ws: at least 256 bytes, as for moe_w2_grouped. */
+MOE_API int moe_combine(const moe_shape* shape, const float* y, const float* topk_w, const int32_t* row_of_slot,
+                        const uint8_t* dead, uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
 /* The whole layer: route -> quant -> W13+SwiGLU+requant -> W2 -> combine, on one stream, no host
  * synchronisation and no allocation (capturable in a CUDA graph for a fixed shape).

@@ -71,9 +71,9 @@ def test_workspace_checks_on_host(B):
     fake = ctypes.c_void_p(0x1000 + 8)
     assert B.lib.moe_w2_combine_grouped(ctypes.byref(shp), *([n] * 10), fake, need, n) == B.MOE_ERR_WORKSPACE
     # the split down projection / combine only need the status word, but it must be there
-    assert B.lib.moe_w2_grouped(ctypes.byref(shp), *([n] * 8), n, 256, n) == B.MOE_ERR_WORKSPACE
-    assert B.lib.moe_combine(ctypes.byref(shp), *([n] * 4), ctypes.c_void_p(0x1000), 128, n) == B.MOE_ERR_WORKSPACE
-    assert B.lib.moe_combine(ctypes.byref(shp), *([n] * 4), ctypes.c_void_p(0x1000), 256, n) == B.MOE_ERR_INVALID_ARG
+    assert B.lib.moe_w2_grouped(ctypes.byref(shp), *([n] * 7), n, 256, n) == B.MOE_ERR_WORKSPACE
+    assert B.lib.moe_combine(ctypes.byref(shp), *([n] * 5), ctypes.c_void_p(0x1000), 128, n) == B.MOE_ERR_WORKSPACE
+    assert B.lib.moe_combine(ctypes.byref(shp), *([n] * 5), ctypes.c_void_p(0x1000), 256, n) == B.MOE_ERR_INVALID_ARG
     fake = ctypes.c_void_p(0x1000)
     assert B.lib.moe_forward(ctypes.byref(shp), *([n] * 9), None, fake, need - 256, n) == B.MOE_ERR_WORKSPACE
 

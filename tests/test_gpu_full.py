@@ -87,8 +87,8 @@ def _tile_width(cfg, cnt, w13: bool):
 
 
 def _tile_rows(cfg, offsets, e):
-    """Plan rows at the first/last row of the first, middle and last token tile of expert e, for the
-    tile widths of both GEMMs."""
+    """Plan rows at the first, middle and last column of the first, middle and last token tile of
+    expert e, for the tile widths of both GEMMs."""
     lo, hi = int(offsets[e]), int(offsets[e + 1])
     cnt = hi - lo
     rows = set()
@@ -96,8 +96,8 @@ def _tile_rows(cfg, offsets, e):
         tw = _tile_width(cfg, cnt, w13)
         starts = list(range(0, cnt, tw))
         for s in {starts[0], starts[len(starts) // 2], starts[-1]}:
-            rows.add(lo + s)
-            rows.add(lo + min(s + tw, cnt) - 1)
+            end = min(s + tw, cnt)
+            rows.update((lo + s, lo + (s + end - 1) // 2, lo + end - 1))
     return sorted(rows)
 
 

@@ -27,7 +27,7 @@ def test_split_w2_and_combine_equal_fused(name, T, Hd, E, k, I, dead_frac):
     hq, hs = B.moe_w13_swiglu_grouped(shp, xq, xs, g.layer.w13p, g.layer.w13sp, plan, ws)
     fused = B.moe_w2_combine_grouped(shp, hq, hs, g.layer.w2p, g.layer.w2sp, plan, ws, dead=dead).clone()
     y = B.moe_w2_grouped(shp, hq, hs, g.layer.w2p, g.layer.w2sp, plan, ws)
-    split = B.moe_combine(shp, y, plan.row_of_slot, ws, dead=dead)
+    split = B.moe_combine(shp, y, plan, ws, dead=dead)
     B.moe_check_device_status(ws)
     assert torch.equal(split, fused)
     # and the whole layer agrees with both

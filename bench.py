@@ -97,7 +97,7 @@ def median_ci(values, level=0.95, resamples=2000, seed=0):
             "mean": round(float(v.mean()), 5), "n": int(v.size)}
 
 
-GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "mx.cuh", "common.cuh")
+GEMM_SOURCES = ("gemm.cu", "gemm.cuh", "gemm2sm.cu", "ptx.cuh", "mx.cuh", "common.cuh")
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 

@@ -29,7 +29,10 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 #include "common.cuh"
+#include "gemm.cuh"
 #include "mx.cuh"
 #include "ptx.cuh"
 
@@ -64,34 +67,6 @@ struct Threads {
   static constexpr int kEpiWarps = ((BN == 128 && MOE_N128_CTAS == 1) || (BN > 128 && MOE_WIDE_CTAS == 1)) ? 8 : 4;
   static constexpr int kCount = 128 + 32 * kEpiWarps;
 };
-constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
-
-struct GemmParams {
-  // B side (activations)
-  const uint8_t* bq;        // W13: xq [T, H];  W2: hq [S, I]
-  const uint8_t* bs;        // W13: xs [T, H/32]; W2: hs [S, HS_PITCH]
-  int b_plan_rows;          // W13: 1 if bq/bs rows are plan rows (row p feeds plan row p), 0 if token rows
-  int b_row_bytes;          // K in bytes (= elements)
-  int b_scale_pitch;        // bytes per scale row
-  // A side (packed weights)
-  const uint8_t* a_codes;   // packed tiles (the tensor map's memory), for L2 prefetch
-  const uint8_t* a_scales;  // packed 512-byte scale blocks
-  int a_fp8;                // 0: E2M1 codes (8 KB packed tiles, unpacked by the TMA); 1: E4M3 (16 KB tiles)
-  // plan
-  const int32_t* offsets;   // [E + 1]
-  const int32_t* slot_of_row;
-  int E, k, K, KC, MT;      // MT = weight panels (of 128 packed rows) per expert
-  int I, H;
-  // W13 outputs
-  uint8_t* hq;
-  uint8_t* hs;
-  int hs_pitch;
-  float* dbg;
-  // W2 output: per-slot rows in plan order, before the routing weight
-  float* y;
-  uint32_t* status;
-};
-
 #ifndef MOE_DEC_KT
 #define MOE_DEC_KT 1                // K-chunks per stage, decode tiles (16 / 32 token rows)
 #endif
@@ -156,28 +131,6 @@ struct Smem {
   // + (E + 1) * 8 bytes of plan tables, sized per launch
   static int total(int E) { return kFixed + (int)align_up((size_t)(E + 1) * 8, 16); }
 };
-
-// One lane waits (bounded), the whole warp learns the outcome.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort, uint32_t* err,
-                                          uint32_t code) {
-  uint32_t ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, kWaitLimitNs, abort, err, code) ? 1u : 0u;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-__device__ __forceinline__ int find_expert(const int* cum, int E, int w) {
-  // largest e with cum[e] <= w (cum non-decreasing, cum[E] > w)
-  int lo = 0, hi = E;           // invariant: cum[lo] <= w < cum[hi]
-  while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
-    if (cum[mid] <= w) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
 
 template <int BN, bool W13>
 __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -524,71 +477,11 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
           const int c0 = cg + 16 * h;
           if (c0 >= tw) break;
           const uint32_t(&r)[16] = rg[h];
-          if constexpr (W13) {
-            // q 0,1 hold gate features 64m + 32q + lane, q 2,3 the matching up features. The chunk
-            // goes to shared memory as [column][feature]; then thread t owns column t / 8 and the
-            // eight features 8 (t % 8) .. +7: SwiGLU, a four-thread amax per 32-block, and one
-            // 8-byte store of codes.
-            // Feature f of a column sits at f ^ (4 * (f / 32 % 2)): the second 32-feature half has
-            // its float4 slots swapped in pairs, so the eight 16-byte reads of a quarter-warp
-            // (features 8 j and 8 j + 4 of one column) fall on distinct banks.
-            float* gs = xchg + half * 2 * 16 * 64;   // [16][64] gate
-            float* us = gs + 16 * 64;                 // [16][64] up
-            if (ok) {
-              float* dst = (q < 2) ? gs : us;
-              const int fsw = (32 * (q & 1) + lane) ^ (4 * (q & 1));
-#pragma unroll
-              for (int c = 0; c < 16; ++c) dst[c * 64 + fsw] = __uint_as_float(r[c]);
-            }
-            named_bar_sync(bar_id, 128);
-            if (ok) {
-              const int t = threadIdx.x - 128 - 128 * half;
-              const int cc = t >> 3, f0 = (t & 7) * 8;
-              const int col = c0 + cc;
-              const int s0 = f0 ^ (4 * (f0 >> 5)), s1 = (f0 + 4) ^ (4 * (f0 >> 5));
-              const float4 g0 = *reinterpret_cast<const float4*>(gs + cc * 64 + s0);
-              const float4 g1 = *reinterpret_cast<const float4*>(gs + cc * 64 + s1);
-              const float4 u0 = *reinterpret_cast<const float4*>(us + cc * 64 + s0);
-              const float4 u1 = *reinterpret_cast<const float4*>(us + cc * 64 + s1);
-              const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-              const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-              float a[8];
-              float am = 0.f;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                a[i] = silu_mul(gv[i], uv[i]);
-                am = fmaxf(am, fabsf(a[i]));
-              }
-              am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-              am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-              const int se = e4m3_scale_exp(am);
-              const float sc = __uint_as_float((uint32_t)(127 - se) << 23);
-              const uint32_t lo = e4m3x2(a[0] * sc, a[1] * sc) | (e4m3x2(a[2] * sc, a[3] * sc) << 16);
-              const uint32_t hi = e4m3x2(a[4] * sc, a[5] * sc) | (e4m3x2(a[6] * sc, a[7] * sc) << 16);
-              if (col < nrows) {
-                const size_t prow = (size_t)(row0 + col);
-                const int feat = 64 * m + f0;
-                *reinterpret_cast<uint2*>(p.hq + prow * p.I + feat) = make_uint2(lo, hi);
-                if ((t & 3) == 0) p.hs[prow * p.hs_pitch + (feat >> 5)] = (uint8_t)(se + 127);
-                if (p.dbg) {
-                  float4* d = reinterpret_cast<float4*>(p.dbg + prow * p.I + feat);
-                  d[0] = make_float4(a[0], a[1], a[2], a[3]);
-                  d[1] = make_float4(a[4], a[5], a[6], a[7]);
-                }
-              }
-            }
-            named_bar_sync(bar_id, 128);
-          } else {
-            if (ok) {
-              // plan row row0 + c of the per-slot buffer, features 128 m + 32 q + lane: each store
-              // instruction writes 128 contiguous bytes (the routing weight is applied by the combine)
-              const int feat = 128 * m + 32 * q + lane;
-              float* yrow = p.y + (size_t)(row0 + c0) * p.H + feat;
-#pragma unroll
-              for (int c = 0; c < 16; ++c)
-                if (c0 + c < nrows) yrow[(size_t)c * p.H] = __uint_as_float(r[c]);
-            }
-          }
+          if constexpr (W13)
+            epi_w13_chunk(r, xchg + half * 2 * 16 * 64, q, lane, threadIdx.x - 128 - 128 * half, bar_id, ok, true,
+                          c0, m, row0, nrows, p);
+          else if (ok)
+            epi_w2_chunk(r, q, lane, c0, m, row0, nrows, p);
         }
       }
       tc_fence_before();
@@ -613,67 +506,6 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
 // ---------------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn get_encode() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
-// Packed weight codes viewed as [tiles * 128 rows, 128 FP4 elements], 64 bytes per row; one box
-// covers `box_tiles` consecutive tiles.
-static int make_weight_tmap(CUtensorMap* m, const uint8_t* codes, long long tiles, int box_tiles) {
-  EncodeTiledFn enc = get_encode();
-  if (!enc) return MOE_ERR_CUDA;
-  cuuint64_t gdim[2] = {128, (cuuint64_t)tiles * 128};
-  cuuint64_t gstride[1] = {64};
-  cuuint32_t box[2] = {128, (cuuint32_t)(128 * box_tiles)};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t*>(codes), gdim, gstride, box,
-                   estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
-}
-
-// Packed E4M3 weight codes viewed as [tiles * 128 rows, 128 bytes]; one box covers `box_tiles`
-// consecutive tiles (the same 128-byte swizzled shared layout as the unpacked FP4 tiles).
-static int make_weight_tmap_fp8(CUtensorMap* m, const uint8_t* codes, long long tiles, int box_tiles) {
-  EncodeTiledFn enc = get_encode();
-  if (!enc) return MOE_ERR_CUDA;
-  cuuint64_t gdim[2] = {128, (cuuint64_t)tiles * 128};
-  cuuint64_t gstride[1] = {128};
-  cuuint32_t box[2] = {128, (cuuint32_t)(128 * box_tiles)};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), gdim, gstride, box, estride,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
-}
-
-// Activation codes viewed as [rows, row_bytes] bytes, 128-byte swizzled boxes of box_rows rows.
-static int make_act_tmap(CUtensorMap* m, const uint8_t* base, int row_bytes, long long rows, int box_rows) {
-  EncodeTiledFn enc = get_encode();
-  if (!enc) return MOE_ERR_CUDA;
-  cuuint64_t gdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-  cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
-  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), gdim, gstride, box, estride,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
-}
-
 // Token-tile width from the mean rows per expert. Wide tiles (MMA N up to MOE_WIDE_BN) are sized
 // per expert inside the kernel: an N = 128 block-scaled MMA with its scale copies occupies the
 // tensor core about as long as an N = 256 one, so fewer, wider tiles raise the math rate.
@@ -699,12 +531,24 @@ static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const G
   return launch_pdl(kern, dim3((unsigned)grid), dim3(Threads<BN>::kCount), (size_t)smem, st, tm, tmb, gp);
 }
 
+// Which wide-tile GEMMs run on CTA pairs: 0 none, 1 W13 only, 2 W13 and W2 (MOE_PAIR in the
+// environment, read once; default 0).
+static int pair_mode() {
+  static int mode = -1;
+  if (mode < 0) {
+    const char* v = getenv("MOE_PAIR");
+    mode = (v && v[0] >= '0' && v[0] <= '2') ? v[0] - '0' : 0;
+  }
+  return mode;
+}
+
 template <bool W13>
 static int launch_gemm(const moe_shape* s, const uint8_t* codes, const GemmParams& gp, cudaStream_t st) {
   const long long slots = (long long)s->T * s->k;
   // TMA row coordinates of the packed weights are 32-bit: 128 rows per tile
   if ((long long)s->E * gp.MT * gp.KC * 128 >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
   int bn = pick_bn(s);
+  if (bn >= 128 && pair_mode() >= (W13 ? 1 : 2)) return launch_gemm_pair(s, codes, gp, W13, st);
   // a down projection with a short K (fewer than 8 chunks) is bound by its epilogue's per-slot
   // stores, not by the MMA rate: it keeps 128-row token tiles
   if (!W13 && bn > 128 && gp.KC < 8) bn = 128;

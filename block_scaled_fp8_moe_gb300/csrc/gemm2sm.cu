@@ -30,6 +30,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "gemm.cuh"
@@ -38,44 +39,46 @@
 
 namespace moe {
 
-#ifndef MOE_PAIR_BN
-#define MOE_PAIR_BN 224             // widest token tile of a pair (MMA N)
-#endif
-#ifndef MOE_PAIR_STAGES
-#define MOE_PAIR_STAGES 5
-#endif
-
-struct Pair {
-  static constexpr int BN = MOE_PAIR_BN;
+// Tile configurations of the pair kernel: token-tile width BN (MMA N across the pair), pipeline
+// stages, and pairs resident per SM pair (1: two accumulator slots, 8 epilogue warps; 2: one
+// accumulator slot per CTA, 4 epilogue warps, the other pair's MMAs covering each epilogue).
+template <int BN_, int STAGES, int CTAS>
+struct PairCfg {
+  static constexpr int BN = BN_;
   static constexpr int kHalfRows = BN / 2;                 // token rows each CTA stages
-  static constexpr int kStages = MOE_PAIR_STAGES;
-  static constexpr int kEpiWarps = 8;
+  static constexpr int kStages = STAGES;
+  static constexpr int kCtasPerSm = CTAS;
+  static constexpr int kAcc = CTAS == 1 ? 2 : 1;
+  static constexpr int kEpiWarps = CTAS == 1 ? 8 : 4;
+  static constexpr int kSets = kEpiWarps / 4;              // epilogue sets of four warps
   static constexpr int kThreads = 128 + 32 * kEpiWarps;
   static constexpr int kTileA = 16384;                     // one 128 x 128 weight tile in 8-bit containers
-  static constexpr int kTileB = kHalfRows * 128;           // tw/2 token rows x 128 FP8
+  static constexpr int kTileB = kHalfRows * 128;           // BN/2 token rows x 128 FP8
   static constexpr int kSfbAtoms = (BN + 127) / 128;       // B scale atoms (128 token columns each)
   static constexpr int kSfChunk = 512 + 512 * kSfbAtoms;
   static constexpr int kStageBytes = (kTileA + kTileB + kSfChunk + 1023) / 1024 * 1024;
   static constexpr int kTiles = kStages * kStageBytes;
-  static constexpr int kXchg = 2 * 2 * 16 * 64 * 4;        // two epilogue sets x (gate + up) [16][64] fp32
+  static constexpr int kXchg = kSets * 2 * 16 * 64 * 4;    // per set: (gate + up) [16][64] fp32
   static constexpr int kMisc = 1024;
   static constexpr int kFixed = 1024 + kTiles + kXchg + kMisc;
   static int total(int E) { return kFixed + (int)align_up((size_t)(E + 1) * 8, 16); }
-  // TMEM (same columns in both CTAs): two accumulator slots of BN columns, then one scale slot per
+  // TMEM (same columns in both CTAs): kAcc accumulator slots of BN columns, then one scale slot per
   // stage (4 columns of A scales, 4 per B atom)
   static constexpr int kAccStride = BN;
-  static constexpr int kSfCol = 2 * BN;
+  static constexpr int kSfCol = kAcc * BN;
   static constexpr int kSfSlot = 4 + 4 * kSfbAtoms;
-  static constexpr int kTmemCols = 512;
+  static constexpr int kTmemCols = 512 / CTAS;
   static_assert(kSfCol + kStages * kSfSlot <= kTmemCols, "TMEM columns");
   static_assert(BN % 32 == 0 && BN <= 256, "pair tile width");
+  static_assert(CTAS == 1 || CTAS == 2, "pairs per SM pair");
 };
 
-template <bool W13>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, 1)
+template <bool W13, class Pair>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, Pair::kCtasPerSm)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                              const GemmParams p) {
   constexpr int S = Pair::kStages;
+  constexpr int NACC = Pair::kAcc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = base;
@@ -106,7 +109,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, 1)
       mbar_init(&full[s], 1 + 32 + (rank == 0 ? 1 : 0));
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NACC; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], 2 * Pair::kEpiWarps);
     }
@@ -235,8 +238,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, 1)
         int e, mp, row0, nrows, tw;
         decode(w, e, mp, row0, nrows, tw);
         const uint32_t idesc_base = idesc_mxf8f6f4(p.a_fp8 ? 0 : 5 /*weights E4M3 or E2M1*/, 0 /*E4M3*/, 256, tw, 0, 0);
-        const int acc = it & 1;
-        const int use = it >> 1;
+        const int acc = (NACC == 2) ? (it & 1) : 0;
+        const int use = (NACC == 2) ? (it >> 1) : it;
         if (use > 0 && !mbar_wait_cluster(&acc_empty[acc], (use - 1) & 1, kWaitLimitNs, abort_flag, p.status,
                                           DEV_TIMEOUT_DRAIN)) {
           ok = false;
@@ -299,8 +302,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ===================== epilogue (warp w -> TMEM lanes 32 (w % 4)) =====================
-    // Warps 4-7 take the even 16 kGrp-column groups of a tile, warps 8-11 the odd ones, each set
-    // with its own exchange buffer and named barrier.
+    // With two sets, warps 4-7 take the even 16 kGrp-column groups of a tile and warps 8-11 the odd
+    // ones, each set with its own exchange buffer and named barrier.
     const int q = (warp - 4) & 3;
     const int half = (warp - 4) >> 2;
     const uint32_t bar_id = 1 + 2 * half;
@@ -313,13 +316,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, 1)
       decode(w, e, mp, row0, nrows, tw);
       const int m = 2 * mp + (int)rank;
       const bool store = m < p.MT;
-      const int acc = it & 1;
-      const int use = it >> 1;
+      const int acc = (NACC == 2) ? (it & 1) : 0;
+      const int use = (NACC == 2) ? (it >> 1) : it;
       if (ok) ok = warp_wait(&acc_full[acc], use & 1, abort_flag, p.status, DEV_TIMEOUT_ACCUM);
       tc_fence_after();
       const uint32_t d_tmem = tmem + (uint32_t)(acc * Pair::kAccStride);
       constexpr int kGrp = W13 ? 2 : 4;
-      for (int cg = 16 * kGrp * half; cg < tw; cg += 16 * kGrp * 2) {
+      for (int cg = 16 * kGrp * half; cg < tw; cg += 16 * kGrp * Pair::kSets) {
         uint32_t rg[kGrp][16];
         if (ok) {
 #pragma unroll
@@ -369,7 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, 1)
 // ---------------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------------
-template <bool W13>
+template <bool W13, class Pair>
 static int launch_pair_t(const moe_shape* s, const uint8_t* codes, const GemmParams& gp, cudaStream_t st) {
   const long long slots = (long long)s->T * s->k;
   if ((long long)s->E * gp.MT * gp.KC * 128 >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -379,18 +382,39 @@ static int launch_pair_t(const moe_shape* s, const uint8_t* codes, const GemmPar
   if (rc) return rc;
   rc = make_act_tmap(&tmb, gp.bq, gp.b_row_bytes, slots, Pair::kHalfRows);
   if (rc) return rc;
-  auto kern = grouped_gemm_pair_kernel<W13>;
+  auto kern = grouped_gemm_pair_kernel<W13, Pair>;
   if (ensure_smem_limit((const void*)kern, Pair::total(kMaxE))) return MOE_ERR_CUDA;
   const int MP = (gp.MT + 1) / 2;
   const long long max_items = (long long)MP * ((slots + Pair::BN - 1) / Pair::BN + std::min<long long>(s->E, slots));
-  const long long pairs = std::min<long long>(max_items, num_sms() / 2);
+  const int occ = ctas_per_sm_by_smem((size_t)Pair::total(gp.E), Pair::kCtasPerSm);
+  const long long pairs = std::min<long long>(max_items, (long long)occ * (num_sms() / 2));
   if (pairs <= 0) return MOE_OK;
   return launch_pdl(kern, dim3((unsigned)(2 * pairs)), dim3(Pair::kThreads), (size_t)Pair::total(gp.E), st, tm, tmb,
                     gp);
 }
 
+// Pair tile configuration (MOE_PAIR_CFG in the environment, read once): 0 = 224 columns, 5 stages,
+// one pair per SM pair; 1 = 192 columns, 6 stages; 2 = 192 columns, 3 stages, two pairs per SM pair.
+static int pair_cfg() {
+  static int c = -1;
+  if (c < 0) {
+    const char* v = getenv("MOE_PAIR_CFG");
+    c = (v && v[0] >= '0' && v[0] <= '2') ? v[0] - '0' : 0;
+  }
+  return c;
+}
+
+template <bool W13>
+static int launch_pair_w(const moe_shape* s, const uint8_t* codes, const GemmParams& gp, cudaStream_t st) {
+  switch (pair_cfg()) {
+    case 1: return launch_pair_t<W13, PairCfg<192, 6, 1>>(s, codes, gp, st);
+    case 2: return launch_pair_t<W13, PairCfg<192, 3, 2>>(s, codes, gp, st);
+    default: return launch_pair_t<W13, PairCfg<224, 5, 1>>(s, codes, gp, st);
+  }
+}
+
 int launch_gemm_pair(const moe_shape* s, const uint8_t* codes, const GemmParams& gp, bool w13, cudaStream_t st) {
-  return w13 ? launch_pair_t<true>(s, codes, gp, st) : launch_pair_t<false>(s, codes, gp, st);
+  return w13 ? launch_pair_w<true>(s, codes, gp, st) : launch_pair_w<false>(s, codes, gp, st);
 }
 
 }  // namespace moe

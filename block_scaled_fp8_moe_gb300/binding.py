@@ -27,7 +27,7 @@ EXPORTED = [
     "moe_route_topk_noalloc", "moe_selftest_timeout", "moe_route_topk_anchored", "moe_forward_anchored",
     "moe_packed_shared_w13_bytes", "moe_packed_shared_w2_bytes", "moe_pack_shared_w13", "moe_pack_shared_w2",
     "moe_shared_workspace_bytes", "moe_forward_shared", "moe_dead_from_survival", "moe_w2_grouped", "moe_combine",
-    "moe_probe_mma_rate", "moe_quant_mxfp8_plan",
+    "moe_probe_mma_rate", "moe_quant_mxfp8_plan", "moe_experts_grouped",
 ]
 
 MOE_FLAG_SWIGLU_DEBUG = 1
@@ -66,6 +66,7 @@ lib.moe_packed_w2_bytes.argtypes = [_SHP, ctypes.POINTER(_SZ)]
 lib.moe_quant_mxfp4.argtypes = [_I32, _I32, _P, _P, _P, _P]
 lib.moe_quant_mxfp8.argtypes = [_I32, _I32, _P, _P, _P, _P]
 lib.moe_quant_mxfp8_plan.argtypes = [_SHP] + [_P] * 6 + [_P]
+lib.moe_experts_grouped.argtypes = [_SHP] + [_P] * 13 + [_P, _SZ, _P]
 lib.moe_dead_from_survival.argtypes = [_I32, _P, ctypes.c_float, _P, _P]
 lib.moe_pack_w13.argtypes = [_SHP, _P, _P, _P, _P, _P]
 lib.moe_pack_w2.argtypes = [_SHP, _P, _P, _P, _P, _P]
@@ -313,6 +314,24 @@ def moe_combine(shp: MoeShape, y, plan: Plan, ws, dead=None, out=None, stream=No
         _ptr(plan.row_of_slot, torch.int32, shp.T * shp.k, "row_of_slot"), _ptr(dead, torch.uint8, shp.T, "dead"),
         _ptr(out, torch.bfloat16, shp.T * shp.H, "out"), _ptr(ws), ws.numel(), _stream(stream)), "moe_combine")
     return out
+
+
+def moe_experts_grouped(shp: MoeShape, xq, xs, w13p, w13sp, w2p, w2sp, plan: Plan, ws, hq=None, hs=None, y=None,
+                        debug=None, stream=None):
+    """Both expert GEMMs (one launch for decode-sized batches): hq / hs and plan-order fp32 y."""
+    S = shp.T * shp.k
+    dev = xq.device
+    rows = S if shp.flags & MOE_FLAG_X_PLAN_ORDER else shp.T
+    hq = torch.empty(max(S, 1), shp.I, dtype=torch.uint8, device=dev) if hq is None else hq
+    hs = torch.empty(max(S, 1), hs_pitch(shp.I), dtype=torch.uint8, device=dev) if hs is None else hs
+    y = torch.empty(max(S, 1), shp.H, dtype=torch.float32, device=dev) if y is None else y
+    _check(lib.moe_experts_grouped(
+        ctypes.byref(shp), _ptr(xq, torch.uint8, rows * shp.H), _ptr(xs, torch.uint8, rows * shp.H // 32),
+        _ptr(w13p, torch.uint8), _ptr(w13sp, torch.uint8), _ptr(w2p, torch.uint8), _ptr(w2sp, torch.uint8),
+        _ptr(plan.expert_offsets), _ptr(plan.slot_of_row), _ptr(hq, torch.uint8, S * shp.I),
+        _ptr(hs, torch.uint8, S * hs_pitch(shp.I)), _ptr(debug, torch.float32, S * shp.I),
+        _ptr(y, torch.float32, S * shp.H, "y"), _ptr(ws), ws.numel(), _stream(stream)), "moe_experts_grouped")
+    return hq, hs, y
 
 
 class SharedExpert:

@@ -2,6 +2,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -11,6 +12,17 @@ using namespace moe;
 namespace {
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// W13 + W2 as one launch for decode-sized tiles (MOE_FUSED=1 in the environment, read once; off by
+// default while it is measured against the two launches).
+bool fused_gemms_enabled() {
+  static int on = -1;
+  if (on < 0) {
+    const char* v = getenv("MOE_FUSED");
+    on = (v && v[0] == '1') ? 1 : 0;
+  }
+  return on == 1;
+}
 
 }  // namespace
 
@@ -122,6 +134,41 @@ extern "C" int moe_combine(const moe_shape* s, const float* y, const float* topk
                         static_cast<uint32_t*>(ws));
 }
 
+extern "C" int moe_experts_grouped(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13,
+                                   const uint8_t* w13_s, const uint8_t* w2, const uint8_t* w2_s,
+                                   const int32_t* expert_offsets, const int32_t* slot_of_row, uint8_t* hq,
+                                   uint8_t* hs, float* swiglu_debug, float* y, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int rc = ws_check(s, ws, ws_bytes);
+  if (rc) return rc;
+  if (s->T == 0) return MOE_OK;
+  if (!xq || !xs || !w13 || !w13_s || !hq || !hs || !y) return MOE_ERR_INVALID_ARG;
+  rc = w2_args_ok(hq, hs, w2, w2_s, expert_offsets, slot_of_row);
+  if (rc) return rc;
+  if (!aligned(xq, 16) || !aligned(xs, 4) || !aligned(w13, 32) || !aligned(w13_s, 16) || !aligned(y, 16) ||
+      !aligned(swiglu_debug, 16))
+    return MOE_ERR_INVALID_ARG;
+  const Workspace L = workspace_layout(s);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* status = ws_ptr<uint32_t>(ws, L.status);
+  float* dbg = (s->flags & MOE_FLAG_SWIGLU_DEBUG) ? swiglu_debug : nullptr;
+  const bool plan_order = (s->flags & MOE_FLAG_X_PLAN_ORDER) != 0;
+  if (fused_gemms_enabled() && fused_gemms_supported(s) && !plan_order) {
+    uint32_t* ready = ws_ptr<uint32_t>(ws, L.ready);
+    if (cudaMemsetAsync(ready, 0, sizeof(uint32_t) * s->E, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return launch_w13_w2_fused(s, xq, xs, w13, w13_s, w2, w2_s, expert_offsets, slot_of_row, hq, hs, dbg, y, status,
+                               ready, st);
+  }
+  uint8_t* xq_rows = plan_order ? const_cast<uint8_t*>(xq) : ws_ptr<uint8_t>(ws, L.xqp);
+  uint8_t* xs_rows = plan_order ? const_cast<uint8_t*>(xs) : ws_ptr<uint8_t>(ws, L.xsp);
+  rc = launch_w13(s, xq, xs, w13, w13_s, expert_offsets, slot_of_row, hq, hs, dbg, status, xq_rows, xs_rows,
+                  plan_order, st);
+  if (rc) return rc;
+  return launch_w2(s, hq, hs, w2, w2_s, expert_offsets, slot_of_row, y, status, st);
+}
+
 extern "C" int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* bias,
                            const uint8_t* dead, const uint8_t* w13, const uint8_t* w13_s, const uint8_t* w2,
                            const uint8_t* w2_s, uint16_t* out, const moe_intermediates* inter, void* ws,
@@ -207,9 +254,13 @@ int forward_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router
   uint32_t* status = ws_ptr<uint32_t>(ws, L.status);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
+  // decode-sized tiles run W13 and W2 as one persistent launch (its per-expert counters are zeroed
+  // by this call's plan kernel)
+  uint32_t* ready = ws_ptr<uint32_t>(ws, L.ready);
+  const bool fuse_gemms = fused_gemms_enabled() && fused_gemms_supported(s);
   bool quant_done = false;
   rc = launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, ws, st,
-                    xq, xs, &quant_done, anchor);
+                    xq, xs, &quant_done, anchor, fuse_gemms ? ready : nullptr);
   if (rc) return rc;
   uint8_t* xqp = ws_ptr<uint8_t>(ws, L.xqp);
   uint8_t* xsp = ws_ptr<uint8_t>(ws, L.xsp);
@@ -261,8 +312,13 @@ int forward_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router
       }
     }
   }
-  rc = launch_w13(s, xq, xs, w13, w13_s, offsets, slot_of_row, hq, hs, im.swiglu, status, xqp, xsp, plan_rows, st);
-  if (!rc) rc = launch_w2(s, hq, hs, w2, w2_s, offsets, slot_of_row, y, status, st);
+  if (fuse_gemms) {
+    rc = launch_w13_w2_fused(s, xq, xs, w13, w13_s, w2, w2_s, offsets, slot_of_row, hq, hs, im.swiglu, y, status,
+                             ready, st);
+  } else {
+    rc = launch_w13(s, xq, xs, w13, w13_s, offsets, slot_of_row, hq, hs, im.swiglu, status, xqp, xsp, plan_rows, st);
+    if (!rc) rc = launch_w2(s, hq, hs, w2, w2_s, offsets, slot_of_row, y, status, st);
+  }
   if (ev_join) {
     if (!rc && cudaStreamWaitEvent(st, ev_join, 0) != cudaSuccess) rc = MOE_ERR_CUDA;
     cudaEventDestroy(ev_join);

@@ -128,15 +128,25 @@ struct Smem {
   static constexpr int kMisc = 1024;                            // barriers, flags
   static constexpr int kRows = 128 * 8;                         // gather row table
   static constexpr int kFixed = 1024 + kTiles + kXchg + kMisc + kRows;
-  // + (E + 1) * 8 bytes of plan tables, sized per launch
-  static int total(int E) { return kFixed + (int)align_up((size_t)(E + 1) * 8, 16); }
+  // + (E + 1) * 12 bytes of plan tables, sized per launch
+  static int total(int E) { return kFixed + (int)align_up((size_t)(E + 1) * 12, 16); }
 };
 
-template <int BN, bool W13>
-__global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                                                                    const __grid_constant__ CUtensorMap tmap_b,
-                                                                    const GemmParams p) {
+// MODE 0: the down projection (W2); 1: gate/up with SwiGLU and requant (W13); 2: W13 then W2 in
+// one persistent launch (decode tiles): every CTA works through its W13 items, then its W2 items.
+// A W2 item's weight tiles stream as soon as the CTA reaches it; its token rows (h) are gathered
+// once the W13 epilogues have counted every W13 tile of that expert (GemmParams::ready). All CTAs
+// are resident (the grid is sized to the GPU), and each CTA finishes its W13 items before its W2
+// ones, so every counted tile is produced by a CTA that is running. In mode 2, p describes W13 and
+// p2 / tmap_a2 the down projection; otherwise p2 and tmap_a2 repeat p and tmap_a.
+template <int BN, int MODE>
+__global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                        const __grid_constant__ CUtensorMap tmap_a2, const __grid_constant__ GemmParams p,
+                        const __grid_constant__ GemmParams p2) {
   using L = Smem<BN>;
+  constexpr bool kFused = MODE == 2;
+  constexpr bool kW13Only = MODE == 1;
   constexpr int S = L::kStages;
   constexpr int NACC = L::kAcc;                    // accumulator slots in TMEM
   constexpr bool kTmaB = L::kTmaB;
@@ -155,6 +165,7 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
   long long* s_rows = reinterpret_cast<long long*>(misc + L::kMisc);   // [BN] gather row or -1
   int* s_off = reinterpret_cast<int*>(misc + L::kMisc + L::kRows);      // expert offsets [E+1]
   int* s_cum = s_off + (p.E + 1);                                       // MT * tile starts [E+1]
+  int* s_cum2 = s_cum + (p.E + 1);                                      // the same for p2.MT (mode 2)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
@@ -200,28 +211,38 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
     int run = incl - local;
     for (int e = e0; e < min(E, e0 + per); ++e) {
       s_cum[e] = run * p.MT;
+      if (kFused) s_cum2[e] = run * p2.MT;
       run += (s_off[e + 1] - s_off[e] + BN - 1) / BN;
     }
-    if (lane == 31) s_cum[E] = incl * p.MT;
+    if (lane == 31) {
+      s_cum[E] = incl * p.MT;
+      if (kFused) s_cum2[E] = incl * p2.MT;
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = s_cum[E];
+  const int total1 = s_cum[E];                        // items of the first (or only) GEMM
+  const int total = total1 + (kFused ? s_cum2[E] : 0);
 
-  // decode work item w -> (e, m, nt); tw = the expert's tile width (columns per token tile): BN
-  // for narrow tiles, else its rows spread evenly over ceil(count / BN) tiles, rounded up to 16
-  auto decode = [&](int w, int& e, int& m, int& nt, int& row0, int& nrows, int& tw) {
-    e = find_expert(s_cum, E, w);
+  // decode work item w -> (GEMM, e, m, nt); first = the item belongs to p (W13 in mode 2); tw = the
+  // expert's tile width (columns per token tile): BN for narrow tiles, else its rows spread evenly
+  // over ceil(count / BN) tiles, rounded up to 16
+  auto decode = [&](int w, bool& first, int& e, int& m, int& nt, int& row0, int& nrows, int& tw) {
+    first = !kFused || w < total1;
+    const int* cum = first ? s_cum : s_cum2;
+    const int MT = first ? p.MT : p2.MT;
+    const int ww = first ? w : w - total1;
+    e = find_expert(cum, E, ww);
     const int cnt = s_off[e + 1] - s_off[e];
     const int ntiles = (cnt + BN - 1) / BN;
     tw = BN;
     if (kTmaB) tw = min(BN, ((cnt + ntiles - 1) / ntiles + 15) / 16 * 16);
-    const int local = w - s_cum[e];
+    const int local = ww - cum[e];
     if (MOE_PANEL_FAST) {
-      nt = local / p.MT;
-      m = local - nt * p.MT;
+      nt = local / MT;
+      m = local - nt * MT;
     } else {
       m = local / ntiles;
       nt = local - m * ntiles;
@@ -229,6 +250,8 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
     row0 = s_off[e] + nt * tw;
     nrows = min(tw, cnt - nt * tw);
   };
+  // the gate/up GEMM (SwiGLU epilogue) or the down projection, for an item of GEMM `first`
+  auto is_w13 = [&](bool first) { return kFused ? first : kW13Only; };
 
   if (warp == 0) {
     // ===================== TMA producer: weights =====================
@@ -236,7 +259,6 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      const int KC = p.KC;
       const uint32_t tile_bytes = p.a_fp8 ? 2 * kTileCodeBytes : kTileCodeBytes;
       // L2 prefetch cursor: walks this CTA's (item, K-chunk) sequence kPrefetch chunks ahead of
       // the loads. It starts kPrefetch chunks in without prefetching: the first chunks are loaded
@@ -245,17 +267,20 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
       long long pf_tile0 = -1;
       auto pf_step = [&](bool issue) {
         if (pf_w >= total) return;
+        const bool pf_first = !kFused || pf_w < total1;
+        const GemmParams& pq = pf_first ? p : p2;
         if (issue) {
           if (pf_tile0 < 0) {
             int e, m, nt, row0, nrows, tw;
-            decode(pf_w, e, m, nt, row0, nrows, tw);
-            pf_tile0 = (long long)(e * p.MT + m) * KC;
+            bool first;
+            decode(pf_w, first, e, m, nt, row0, nrows, tw);
+            pf_tile0 = (long long)(e * pq.MT + m) * pq.KC;
           }
           const long long g = pf_tile0 + pf_kc;
-          prefetch_l2_bulk(p.a_codes + g * tile_bytes, tile_bytes);
-          prefetch_l2_bulk(p.a_scales + g * kTileScaleBytes, kTileScaleBytes);
+          prefetch_l2_bulk(pq.a_codes + g * tile_bytes, tile_bytes);
+          prefetch_l2_bulk(pq.a_scales + g * kTileScaleBytes, kTileScaleBytes);
         }
-        if (++pf_kc == KC) {
+        if (++pf_kc == pq.KC) {
           pf_kc = 0;
           pf_w += gridDim.x;
           pf_tile0 = -1;
@@ -264,8 +289,12 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
       for (int i = 0; i < L::kPrefetch; ++i) pf_step(false);
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         int e, m, nt, row0, nrows, tw;
-        decode(w, e, m, nt, row0, nrows, tw);
-        const int tile0 = (e * p.MT + m) * KC;
+        bool first;
+        decode(w, first, e, m, nt, row0, nrows, tw);
+        const GemmParams& q = first ? p : p2;
+        const CUtensorMap* ta = first ? &tmap_a : &tmap_a2;
+        const int KC = q.KC;
+        const int tile0 = (e * q.MT + m) * KC;
         for (int kc0 = 0; kc0 < KC; kc0 += L::KT) {
           if (!mbar_wait(&empty[stage], phase ^ 1, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_EMPTY)) {
             ok = false;
@@ -278,8 +307,8 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
           // the scale copy stops at the panel's end
           mbar_arrive_expect_tx(&full[stage], L::KT * (p.a_fp8 ? 2 * kTileCodeBytes : kTileCodeBytes) + nv * kTileScaleBytes +
                                                   (kTmaB ? L::kStageB : 0));
-          tma_load_2d(sA, &tmap_a, 0, (tile0 + kc0) * 128, &full[stage]);
-          bulk_load(sSFA, p.a_scales + (size_t)(tile0 + kc0) * kTileScaleBytes, nv * kTileScaleBytes, &full[stage]);
+          tma_load_2d(sA, ta, 0, (tile0 + kc0) * 128, &full[stage]);
+          bulk_load(sSFA, q.a_scales + (size_t)(tile0 + kc0) * kTileScaleBytes, nv * kTileScaleBytes, &full[stage]);
           if (L::kPrefetch > 0)
             for (int j = 0; j < nv; ++j) pf_step(true);
           if (++stage == S) { stage = 0; phase ^= 1; }
@@ -297,7 +326,8 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
     bool ok = true;
     for (int w = blockIdx.x; w < total; w += gridDim.x) {
       int e, m, nt, row0, nrows, tw;
-      decode(w, e, m, nt, row0, nrows, tw);
+      bool first;
+      decode(w, first, e, m, nt, row0, nrows, tw);
       for (int kc0 = 0; kc0 < p.KC; kc0 += L::KT) {
         if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
         if (ok) {
@@ -336,21 +366,31 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
     bool ok = true;
     for (int w = blockIdx.x; w < total; w += gridDim.x) {
       int e, m, nt, row0, nrows, tw;
-      decode(w, e, m, nt, row0, nrows, tw);
+      bool first;
+      decode(w, first, e, m, nt, row0, nrows, tw);
+      const GemmParams& q = first ? p : p2;
       named_bar_sync(2, 64);                          // previous item's table no longer in use
       for (int c = pb; c < BN; c += 64) {
         long long r = -1;
         if (c < nrows) {
           const int prow = row0 + c;
-          r = (W13 && !p.b_plan_rows) ? (long long)(p.slot_of_row[prow] / p.k) : (long long)prow;
+          r = (is_w13(first) && !q.b_plan_rows) ? (long long)(q.slot_of_row[prow] / q.k) : (long long)prow;
         }
         s_rows[c] = r;
       }
       named_bar_sync(2, 64);
-      for (int kc0 = 0; kc0 < p.KC; kc0 += L::KT) {
+      if (kFused && !first && ok) {
+        // the expert's h rows exist once every W13 tile of the expert has been counted
+        const uint32_t need = (uint32_t)((s_cum[e + 1] - s_cum[e]) * Threads<BN>::kEpiWarps);
+        uint32_t got = 1;
+        if (lane == 0) got = wait_count_at_least(q.ready + e, need, kWaitLimitNs, abort_flag, q.status) ? 1u : 0u;
+        ok = __shfl_sync(0xffffffffu, got, 0) != 0;
+        __syncwarp();                                 // the lanes' gathers follow lane 0's acquire
+      }
+      for (int kc0 = 0; kc0 < q.KC; kc0 += L::KT) {
         if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
         if (ok) {
-          const int nv = min(L::KT, p.KC - kc0);
+          const int nv = min(L::KT, q.KC - kc0);
           uint8_t* sB0 = tiles + stage * L::kStageBytes + L::kStageA;
           uint8_t* sSFB0 = sB0 + L::kStageB + L::KT * 512;
           for (int j2 = 0; j2 < nv; ++j2) {
@@ -361,14 +401,14 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
               const int c = i >> 3, j = i & 7;
               const long long r = s_rows[c];
               const int kbyte = kc * 128 + j * 16;
-              const bool valid = (r >= 0) && (kbyte < p.b_row_bytes);
-              const uint8_t* src = valid ? p.bq + r * p.b_row_bytes + kbyte : p.bq;
+              const bool valid = (r >= 0) && (kbyte < q.b_row_bytes);
+              const uint8_t* src = valid ? q.bq + r * q.b_row_bytes + kbyte : q.bq;
               cp_async_16(sB + c * 128 + ((j ^ (c & 7)) << 4), src, valid ? 16u : 0u);
             }
             for (int c = pb; c < BN; c += 64) {
               const long long r = s_rows[c];
               const bool valid = r >= 0;
-              const uint8_t* src = valid ? p.bs + r * p.b_scale_pitch + kc * 4 : p.bs;
+              const uint8_t* src = valid ? q.bs + r * q.b_scale_pitch + kc * 4 : q.bs;
               cp_async_4(sSFB + (c & 31) * 16 + (c >> 5) * 4, src, valid ? 4u : 0u);
             }
           }
@@ -387,7 +427,9 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it) {
         int e, m, nt, row0, nrows, tw;
-        decode(w, e, m, nt, row0, nrows, tw);
+        bool first;
+        decode(w, first, e, m, nt, row0, nrows, tw);
+        const GemmParams& q = first ? p : p2;
         const uint32_t idesc_base = idesc_mxf8f6f4(p.a_fp8 ? 0 : 5 /*weights E4M3 or E2M1*/, 0 /*E4M3*/, 128, tw, 0, 0);
         const int acc = (NACC == 2) ? (it & 1) : 0;
         const int use = (NACC == 2) ? (it >> 1) : it;       // how many times this slot was used before
@@ -398,14 +440,14 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(acc * L::kAccStride);
-        for (int kc0 = 0; kc0 < p.KC; kc0 += L::KT) {
+        for (int kc0 = 0; kc0 < q.KC; kc0 += L::KT) {
           if (!mbar_wait(&full[stage], phase, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_FULL)) {
             ok = false;
             break;
           }
           fence_async_smem();
           tc_fence_after();
-          const int nv = min(L::KT, p.KC - kc0);
+          const int nv = min(L::KT, q.KC - kc0);
           uint8_t* sA0 = tiles + stage * L::kStageBytes;
           uint8_t* sB0 = sA0 + L::kStageA;
           uint8_t* sSFA0 = sB0 + L::kStageB;
@@ -416,10 +458,10 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
             const uint32_t tsfb = tsfa + 4;
             tc_cp_32x128b_warpx4(tsfa, smem_desc(smem_u32(sSFA0 + j * 512), 16, 128, 0));
             // B scales: one 512-byte atom per 128 token rows, atom q at TMEM column tsfb + 4 q
-            for (int q = 0; q * 128 < tw; ++q)
-              tc_cp_32x128b_warpx4(tsfb + 4 * q, smem_desc(smem_u32(sSFB0 + j * L::kSfbChunk + q * 512), 16, 128, 0));
+            for (int a = 0; a * 128 < tw; ++a)
+              tc_cp_32x128b_warpx4(tsfb + 4 * a, smem_desc(smem_u32(sSFB0 + j * L::kSfbChunk + a * 512), 16, 128, 0));
             const uint32_t a0 = smem_u32(sA0 + j * L::kTileA), b0 = smem_u32(sB0 + j * L::kTileB);
-            const int nk = min(4, (p.K - kc * 128) / 32);
+            const int nk = min(4, (q.K - kc * 128) / 32);
             for (int kb = 0; kb < nk; ++kb) {
               const uint64_t ad = smem_desc(a0 + kb * 32, 16, 1024, 2);
               const uint64_t bd = smem_desc(b0 + kb * 32, 16, 1024, 2);
@@ -446,22 +488,26 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
     // odd ones, each set with its own exchange buffer and named barrier. As above, an expired wait
     // turns the remaining iterations into no-ops that still meet at the named barriers.
     constexpr int kHalves = Threads<BN>::kEpiWarps / 4;
-    const int q = (warp - 4) & 3;
+    const int qd = (warp - 4) & 3;                    // TMEM lane quarter of this warp
     const int half = (warp - 4) >> 2;
     const uint32_t bar_id = 1 + 2 * half;
-    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
     int it = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total; w += gridDim.x, ++it) {
       int e, m, nt, row0, nrows, tw;
-      decode(w, e, m, nt, row0, nrows, tw);
+      bool first;
+      decode(w, first, e, m, nt, row0, nrows, tw);
+      const GemmParams& q = first ? p : p2;
+      const bool w13_item = is_w13(first);
       const int acc = (NACC == 2) ? (it & 1) : 0;
       const int use = (NACC == 2) ? (it >> 1) : it;
       if (ok) ok = warp_wait(&acc_full[acc], use & 1, abort_flag, p.status, DEV_TIMEOUT_ACCUM);
       tc_fence_after();
       const uint32_t d_tmem = tmem + (uint32_t)(acc * L::kAccStride);
       // TMEM is read kGrp 16-column chunks per round trip (one wait for several loads)
-      constexpr int kGrp = W13 ? (BN <= 32 ? 1 : 2) : (BN >= 64 ? (L::kAcc == 1 ? 2 : 4) : BN / 16);
+      constexpr int kGrp = kFused ? 1
+                                  : (kW13Only ? (BN <= 32 ? 1 : 2) : (BN >= 64 ? (L::kAcc == 1 ? 2 : 4) : BN / 16));
       for (int cg = 16 * kGrp * half; cg < tw; cg += 16 * kGrp * kHalves) {
         uint32_t rg[kGrp][16];
         if (ok) {
@@ -477,16 +523,21 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm) gro
           const int c0 = cg + 16 * h;
           if (c0 >= tw) break;
           const uint32_t(&r)[16] = rg[h];
-          if constexpr (W13)
-            epi_w13_chunk(r, xchg + half * 2 * 16 * 64, q, lane, threadIdx.x - 128 - 128 * half, bar_id, ok, true,
-                          c0, m, row0, nrows, p);
+          if (w13_item)
+            epi_w13_chunk(r, xchg + half * 2 * 16 * 64, qd, lane, threadIdx.x - 128 - 128 * half, bar_id, ok, true,
+                          c0, m, row0, nrows, q);
           else if (ok)
-            epi_w2_chunk(r, q, lane, c0, m, row0, nrows, p);
+            epi_w2_chunk(r, qd, lane, c0, m, row0, nrows, q);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && ok) mbar_arrive(&acc_empty[acc]);
+      if (kFused && w13_item && lane == 0 && ok) {
+        // this warp's stores of the tile are done (the set's named barrier ordered them): publish
+        __threadfence();
+        atomicAdd(q.ready + e, 1u);
+      }
     }
   }
 
@@ -517,29 +568,41 @@ static int pick_bn(const moe_shape* s) {
   return MOE_WIDE_BN;
 }
 
-template <int BN, bool W13>
-static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const GemmParams& gp, long long max_items,
-                          cudaStream_t st) {
+template <int BN, int MODE>
+static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const CUtensorMap& tm2, const GemmParams& gp,
+                          const GemmParams& gp2, long long max_items, cudaStream_t st) {
   using L = Smem<BN>;
-  auto kern = grouped_gemm_kernel<BN, W13>;
+  auto kern = grouped_gemm_kernel<BN, MODE>;
   const int smem = L::total(gp.E);
   if (ensure_smem_limit((const void*)kern, L::total(kMaxE))) return MOE_ERR_CUDA;
-  // persistent grid: as many CTAs as fit on the GPU at once (smem depends on E)
+  // persistent grid: as many CTAs as fit on the GPU at once (smem depends on E); the one-launch
+  // W13 + W2 mode relies on every CTA being resident
   const int occ = ctas_per_sm_by_smem((size_t)smem, L::kCtasPerSm);
   const long long grid = std::min<long long>(max_items, (long long)occ * num_sms());
   if (grid <= 0) return MOE_OK;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(Threads<BN>::kCount), (size_t)smem, st, tm, tmb, gp);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(Threads<BN>::kCount), (size_t)smem, st, tm, tmb, tm2, gp, gp2);
 }
 
-// Which wide-tile GEMMs run on CTA pairs: 0 none, 1 W13 only, 2 W13 and W2 (MOE_PAIR in the
-// environment, read once; default 0).
+// Which wide-tile GEMMs run on CTA pairs: 0 none, 1 W13 only, 2 W13 and W2, 3 (default) only a
+// down projection with a short K (fewer than 8 K-chunks), where the pairs measured faster (MOE_PAIR
+// in the environment, read once, for measurements).
 static int pair_mode() {
   static int mode = -1;
   if (mode < 0) {
     const char* v = getenv("MOE_PAIR");
-    mode = (v && v[0] >= '0' && v[0] <= '2') ? v[0] - '0' : 0;
+    mode = (v && v[0] >= '0' && v[0] <= '3') ? v[0] - '0' : 3;
   }
   return mode;
+}
+
+static bool use_pairs(bool w13, int KC) {
+  const int m = pair_mode();
+  return m == 3 ? (!w13 && KC < 8) : m >= (w13 ? 1 : 2);
+}
+
+static int weight_tmap(CUtensorMap* tm, const moe_shape* s, const uint8_t* codes, const GemmParams& gp, int box_tiles) {
+  const long long tiles = (long long)s->E * gp.MT * gp.KC;
+  return gp.a_fp8 ? make_weight_tmap_fp8(tm, codes, tiles, box_tiles) : make_weight_tmap(tm, codes, tiles, box_tiles);
 }
 
 template <bool W13>
@@ -548,14 +611,13 @@ static int launch_gemm(const moe_shape* s, const uint8_t* codes, const GemmParam
   // TMA row coordinates of the packed weights are 32-bit: 128 rows per tile
   if ((long long)s->E * gp.MT * gp.KC * 128 >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
   int bn = pick_bn(s);
-  if (bn >= 128 && pair_mode() >= (W13 ? 1 : 2)) return launch_gemm_pair(s, codes, gp, W13, st);
+  if (bn >= 128 && use_pairs(W13, gp.KC)) return launch_gemm_pair(s, codes, gp, W13, st);
   // a down projection with a short K (fewer than 8 chunks) is bound by its epilogue's per-slot
   // stores, not by the MMA rate: it keeps 128-row token tiles
   if (!W13 && bn > 128 && gp.KC < 8) bn = 128;
   CUtensorMap tm;
   const int box_tiles = (bn <= 32) ? Smem<16>::KT : (bn <= 64 ? Smem<64>::KT : (bn == 128 ? Smem<128>::KT : Smem<MOE_WIDE_BN>::KT));
-  int rc0 = gp.a_fp8 ? make_weight_tmap_fp8(&tm, codes, (long long)s->E * gp.MT * gp.KC, box_tiles)
-                     : make_weight_tmap(&tm, codes, (long long)s->E * gp.MT * gp.KC, box_tiles);
+  int rc0 = weight_tmap(&tm, s, codes, gp, box_tiles);
   if (rc0) return rc0;
   // activation operand of the wide token tile as a TMA tensor: [T*k plan rows, K] bytes, boxes of
   // bn plan rows (W13: the plan-order copy of xq; W2: hq)
@@ -565,12 +627,13 @@ static int launch_gemm(const moe_shape* s, const uint8_t* codes, const GemmParam
     const int rc = make_act_tmap(&tmb, gp.bq, gp.b_row_bytes, slots, bn);
     if (rc) return rc;
   }
+  constexpr int M = W13 ? 1 : 0;
   switch (bn) {
-    case 16: return launch_gemm_bn<16, W13>(tm, tmb, gp, max_items, st);
-    case 32: return launch_gemm_bn<32, W13>(tm, tmb, gp, max_items, st);
-    case 64: return launch_gemm_bn<64, W13>(tm, tmb, gp, max_items, st);
-    case 128: return launch_gemm_bn<128, W13>(tm, tmb, gp, max_items, st);
-    default: return launch_gemm_bn<MOE_WIDE_BN, W13>(tm, tmb, gp, max_items, st);
+    case 16: return launch_gemm_bn<16, M>(tm, tmb, tm, gp, gp, max_items, st);
+    case 32: return launch_gemm_bn<32, M>(tm, tmb, tm, gp, gp, max_items, st);
+    case 64: return launch_gemm_bn<64, M>(tm, tmb, tm, gp, gp, max_items, st);
+    case 128: return launch_gemm_bn<128, M>(tm, tmb, tm, gp, gp, max_items, st);
+    default: return launch_gemm_bn<MOE_WIDE_BN, M>(tm, tmb, tm, gp, gp, max_items, st);
   }
 }
 
@@ -601,32 +664,16 @@ __global__ void gather_plan_rows_kernel(const uint8_t* __restrict__ xq, const ui
 
 bool w13_wants_plan_rows(const moe_shape* s) { return pick_bn(s) >= 128; }
 
-int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
-               const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
-               uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, bool plan_rows_ready, cudaStream_t st,
-               bool fp8_weights) {
-  if (s->T == 0) return MOE_OK;
+// Parameters of the gate/up GEMM reading xq / xs (token rows, or plan rows with plan_rows).
+static GemmParams w13_params(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, bool plan_rows,
+                             const uint8_t* w13, const uint8_t* w13s, const int32_t* offsets,
+                             const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg, uint32_t* status,
+                             bool fp8_weights) {
   GemmParams gp{};
   gp.a_fp8 = fp8_weights ? 1 : 0;
   gp.bq = xq;
   gp.bs = xs;
-  if (plan_rows_ready) {
-    // the activation rows already sit in plan order (wide tiles read them with TMA boxes, narrow
-    // tiles gather plan row p for column p)
-    gp.bq = xq_plan;
-    gp.bs = xs_plan;
-    gp.b_plan_rows = 1;
-  } else if (pick_bn(s) >= 128) {
-    // wide tiles read the token operand in plan order with TMA boxes: gather it once
-    const long long n = (long long)s->T * s->k * (s->H / 16 + s->H / 128);
-    const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);
-    const int rc = launch_pdl(gather_plan_rows_kernel, dim3(blocks), dim3(256), 0, st, xq, xs, s->H, slot_of_row,
-                              offsets, s->E, s->k, s->T * s->k, xq_plan, xs_plan);
-    if (rc) return rc;
-    gp.bq = xq_plan;
-    gp.bs = xs_plan;
-    gp.b_plan_rows = 1;
-  }
+  gp.b_plan_rows = plan_rows ? 1 : 0;
   gp.b_row_bytes = s->H;
   gp.b_scale_pitch = s->H / 32;
   gp.a_codes = w13;
@@ -645,13 +692,13 @@ int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const u
   gp.hs_pitch = hs_pitch(s->I);
   gp.dbg = dbg;
   gp.status = status;
-  return launch_gemm<true>(s, w13, gp, st);
+  return gp;
 }
 
-int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2s,
-              const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
-              cudaStream_t st, bool fp8_weights) {
-  if (s->T == 0) return MOE_OK;
+// Parameters of the down projection reading hq / hs (plan rows) into plan-order y.
+static GemmParams w2_params(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2,
+                            const uint8_t* w2s, const int32_t* offsets, const int32_t* slot_of_row, float* y,
+                            uint32_t* status, bool fp8_weights) {
   GemmParams gp{};
   gp.a_fp8 = fp8_weights ? 1 : 0;
   gp.bq = hq;
@@ -671,7 +718,67 @@ int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const ui
   gp.H = s->H;
   gp.y = y;
   gp.status = status;
+  return gp;
+}
+
+int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
+               const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
+               uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, bool plan_rows_ready, cudaStream_t st,
+               bool fp8_weights) {
+  if (s->T == 0) return MOE_OK;
+  bool plan_rows = false;
+  if (plan_rows_ready) {
+    // the activation rows already sit in plan order (wide tiles read them with TMA boxes, narrow
+    // tiles gather plan row p for column p)
+    xq = xq_plan;
+    xs = xs_plan;
+    plan_rows = true;
+  } else if (pick_bn(s) >= 128) {
+    // wide tiles read the token operand in plan order with TMA boxes: gather it once
+    const long long n = (long long)s->T * s->k * (s->H / 16 + s->H / 128);
+    const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 8);
+    const int rc = launch_pdl(gather_plan_rows_kernel, dim3(blocks), dim3(256), 0, st, xq, xs, s->H, slot_of_row,
+                              offsets, s->E, s->k, s->T * s->k, xq_plan, xs_plan);
+    if (rc) return rc;
+    xq = xq_plan;
+    xs = xs_plan;
+    plan_rows = true;
+  }
+  const GemmParams gp = w13_params(s, xq, xs, plan_rows, w13, w13s, offsets, slot_of_row, hq, hs, dbg, status,
+                                   fp8_weights);
+  return launch_gemm<true>(s, w13, gp, st);
+}
+
+int launch_w2(const moe_shape* s, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2, const uint8_t* w2s,
+              const int32_t* offsets, const int32_t* slot_of_row, float* y, uint32_t* status,
+              cudaStream_t st, bool fp8_weights) {
+  if (s->T == 0) return MOE_OK;
+  const GemmParams gp = w2_params(s, hq, hs, w2, w2s, offsets, slot_of_row, y, status, fp8_weights);
   return launch_gemm<false>(s, w2, gp, st);
+}
+
+bool fused_gemms_supported(const moe_shape* s) { return pick_bn(s) <= 32; }
+
+int launch_w13_w2_fused(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13,
+                        const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, const int32_t* offsets,
+                        const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg, float* y, uint32_t* status,
+                        uint32_t* ready, cudaStream_t st) {
+  if (s->T == 0) return MOE_OK;
+  const int bn = pick_bn(s);
+  if (bn > 32 || !ready) return MOE_ERR_UNSUPPORTED_SHAPE;
+  GemmParams g13 = w13_params(s, xq, xs, false, w13, w13s, offsets, slot_of_row, hq, hs, dbg, status, false);
+  GemmParams g2 = w2_params(s, hq, hs, w2, w2s, offsets, slot_of_row, y, status, false);
+  g13.ready = ready;
+  g2.ready = ready;
+  if ((long long)s->E * std::max(g13.MT * g13.KC, g2.MT * g2.KC) * 128 >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  CUtensorMap t13, t2;
+  int rc = weight_tmap(&t13, s, w13, g13, Smem<16>::KT);
+  if (!rc) rc = weight_tmap(&t2, s, w2, g2, Smem<16>::KT);
+  if (rc) return rc;
+  const long long slots = (long long)s->T * s->k;
+  const long long max_items = (long long)(g13.MT + g2.MT) * ((slots + bn - 1) / bn + std::min<long long>(s->E, slots));
+  return bn == 16 ? launch_gemm_bn<16, 2>(t13, t13, t2, g13, g2, max_items, st)
+                  : launch_gemm_bn<32, 2>(t13, t13, t2, g13, g2, max_items, st);
 }
 
 }  // namespace moe

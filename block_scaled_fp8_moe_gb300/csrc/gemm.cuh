@@ -38,6 +38,10 @@ struct GemmParams {
   // W2 output: per-slot rows in plan order, before the routing weight
   float* y;
   uint32_t* status;
+  // W13 then W2 in one launch: W13 epilogue warps count finished tiles per expert here (after their
+  // stores), and a W2 tile gathers its expert's rows only once every W13 tile of that expert has
+  // been counted. Zeroed by the plan kernel before each layer call.
+  uint32_t* ready;
 };
 
 
@@ -61,6 +65,30 @@ __device__ __forceinline__ int find_expert(const int* cum, int E, int w) {
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+// Bounded wait (one thread) until a counter in global memory reaches `need` (acquire: the writes
+// published before each increment are visible afterwards). On expiry it records DEV_TIMEOUT_FULL
+// in *err, sets *abort and returns false; it returns false at once if *abort is already set.
+__device__ __forceinline__ bool wait_count_at_least(const uint32_t* counter, uint32_t need, uint64_t limit_ns,
+                                                    volatile uint32_t* abort, uint32_t* err) {
+  auto load = [&]() {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    return v;
+  };
+  if (load() >= need) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (load() >= need) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      atomicCAS(err, 0u, (uint32_t)DEV_TIMEOUT_FULL);
+      return false;
+    }
+    __nanosleep(64);
+  }
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -393,13 +393,15 @@ static int launch_pair_t(const moe_shape* s, const uint8_t* codes, const GemmPar
                     gp);
 }
 
-// Pair tile configuration (MOE_PAIR_CFG in the environment, read once): 0 = 224 columns, 5 stages,
-// one pair per SM pair; 1 = 192 columns, 6 stages; 2 = 192 columns, 3 stages, two pairs per SM pair.
+// Pair tile configuration (MOE_PAIR_CFG in the environment, read once, for measurements): 0 = 224
+// columns, 5 stages, one pair per SM pair; 1 = 192 columns, 6 stages; 2 (default) = 192 columns,
+// 3 stages, two pairs per SM pair (fastest measured: the second pair keeps the SMs busy while the
+// first waits on its stages).
 static int pair_cfg() {
   static int c = -1;
   if (c < 0) {
     const char* v = getenv("MOE_PAIR_CFG");
-    c = (v && v[0] >= '0' && v[0] <= '2') ? v[0] - '0' : 0;
+    c = (v && v[0] >= '0' && v[0] <= '2') ? v[0] - '0' : 2;
   }
   return c;
 }

@@ -558,9 +558,13 @@ __global__ void __launch_bounds__(512) topk_plan_single_kernel(const float* __re
                                                                int32_t* __restrict__ offsets,
                                                                int32_t* __restrict__ slot_of_row,
                                                                int32_t* __restrict__ row_of_slot,
-                                                               const int32_t* __restrict__ anchor, uint32_t* status) {
+                                                               const int32_t* __restrict__ anchor, uint32_t* status,
+                                                               uint32_t* __restrict__ ready) {
   pdl_trigger();
   pdl_wait();
+  // per-expert tile counters of the one-launch W13 + W2 GEMM (nullable): zero before it runs
+  if (ready)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) ready[e] = 0;
   extern __shared__ __align__(16) uint8_t psm[];
   uint32_t* mask = reinterpret_cast<uint32_t*>(psm);
   int16_t* sidx = reinterpret_cast<int16_t*>(psm + align_up((size_t)E * 8 * 4, 16));
@@ -618,9 +622,11 @@ __global__ void __launch_bounds__(512) topk_plan_kernel(const uint8_t* __restric
 // Multi-block plan, step 2 (one CTA): per-expert totals, offsets, and each block's base row.
 __global__ void __launch_bounds__(512) plan_scan_kernel(const int32_t* __restrict__ cnt, int nb, int E,
                                                         int32_t* __restrict__ base, int32_t* __restrict__ counts,
-                                                        int32_t* __restrict__ offsets) {
+                                                        int32_t* __restrict__ offsets, uint32_t* __restrict__ ready) {
   pdl_trigger();
   pdl_wait();
+  if (ready)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) ready[e] = 0;
   __shared__ int tot[kMaxE];
   __shared__ int total_s;
   constexpr int U = 8;                            // block counts loaded per step (all in flight)
@@ -679,13 +685,13 @@ template <int NI>
 static int launch_topk_plan_ni(int nb, int E, size_t smem, cudaStream_t st, const float* score, const float* key,
                                const uint8_t* dead, int T, int k, int32_t* topk_idx, float* topk_w, int32_t* cnt,
                                int32_t* rank, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
-                               int32_t* row_of_slot, const int32_t* anchor, uint32_t* status) {
+                               int32_t* row_of_slot, const int32_t* anchor, uint32_t* status, uint32_t* ready) {
   if (ensure_smem_limit((const void*)topk_plan_single_kernel<NI>, 64 * 1024) ||
       ensure_smem_limit((const void*)topk_plan_kernel, 64 * 1024))
     return MOE_ERR_CUDA;
   if (nb == 1)
     return launch_pdl(topk_plan_single_kernel<NI>, dim3(1), dim3(512), plan_single_smem(E, k), st, score, key, dead, T,
-                      E, k, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, anchor, status);
+                      E, k, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, anchor, status, ready);
   // many blocks: selection spread over the whole GPU (anchored rows next), then the per-block plan
   const int sel_blocks = (int)std::min<long long>(((long long)T + 7) / 8, (long long)num_sms() * 8);
   int rc = launch_pdl(topk_select_kernel<NI>, dim3(sel_blocks), dim3(256), 0, st, score, key, T, E, k, topk_idx,
@@ -703,11 +709,11 @@ static int launch_topk_plan_ni(int nb, int E, size_t smem, cudaStream_t st, cons
 static int launch_topk_plan(int nb, int E, size_t smem, cudaStream_t st, const float* score, const float* key,
                             const uint8_t* dead, int T, int k, int32_t* topk_idx, float* topk_w, int32_t* cnt,
                             int32_t* rank, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
-                            int32_t* row_of_slot, const int32_t* anchor, uint32_t* status) {
+                            int32_t* row_of_slot, const int32_t* anchor, uint32_t* status, uint32_t* ready) {
 #define MOE_TOPK_CASE(N)                                                                                        \
   if (E <= 32 * N)                                                                                              \
     return launch_topk_plan_ni<N>(nb, E, smem, st, score, key, dead, T, k, topk_idx, topk_w, cnt, rank, counts, \
-                                  offsets, slot_of_row, row_of_slot, anchor, status);
+                                  offsets, slot_of_row, row_of_slot, anchor, status, ready);
   MOE_TOPK_CASE(1)
   MOE_TOPK_CASE(2)
   MOE_TOPK_CASE(4)
@@ -726,7 +732,7 @@ static int launch_topk_single_plain_ni(cudaStream_t st, const float* score, cons
   if (ensure_smem_limit((const void*)topk_plan_single_kernel<NI>, 64 * 1024)) return MOE_ERR_CUDA;
   topk_plan_single_kernel<NI><<<1, 512, plan_single_smem(E, k), st>>>(score, key, dead, T, E, k, topk_idx, topk_w,
                                                                        counts, offsets, slot_of_row, row_of_slot,
-                                                                       nullptr, nullptr);
+                                                                       nullptr, nullptr, nullptr);
   return launch_status();
 }
 
@@ -750,7 +756,7 @@ static int launch_topk_single_plain(int E, cudaStream_t st, const float* score, 
 int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, const uint8_t* dead,
                  int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
                  int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done,
-                 const int32_t* anchor) {
+                 const int32_t* anchor, uint32_t* ready) {
   if (quant_done) *quant_done = false;
   const Workspace L = workspace_layout(s);
   const int T = s->T, E = s->E, k = s->k, H = s->H;
@@ -787,9 +793,9 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
   int32_t* base = ws_ptr<int32_t>(ws, L.base);
   int32_t* rank = ws_ptr<int32_t>(ws, L.rank);
   rc = launch_topk_plan(nb, E, smem, st, score, key, dead, T, k, topk_idx, topk_w, cnt, rank, counts, offsets,
-                        slot_of_row, row_of_slot, anchor, ws_ptr<uint32_t>(ws, L.status));
+                        slot_of_row, row_of_slot, anchor, ws_ptr<uint32_t>(ws, L.status), ready);
   if (rc || nb == 1) return rc;
-  rc = launch_pdl(plan_scan_kernel, dim3(1), dim3(512), 0, st, cnt, nb, E, base, counts, offsets);
+  rc = launch_pdl(plan_scan_kernel, dim3(1), dim3(512), 0, st, cnt, nb, E, base, counts, offsets, ready);
   if (rc) return rc;
   const long long n = (long long)T * k;
   const int blocks = (int)std::min<long long>((n + 255) / 256, (long long)num_sms() * 4);
@@ -890,7 +896,7 @@ extern "C" int moe_route_topk_anchored(const moe_shape* s, const uint16_t* x, co
   int rc = ws_check(s, ws, ws_bytes);
   if (rc) return rc;
   return launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, expert_counts, expert_offsets, slot_of_row,
-                      row_of_slot, ws, static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, anchor);
+                      row_of_slot, ws, static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, anchor, nullptr);
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -224,6 +224,18 @@ MOE_API int moe_w2_grouped(const moe_shape* shape, const uint8_t* hq, const uint
 MOE_API int moe_combine(const moe_shape* shape, const float* y, const float* topk_w, const int32_t* row_of_slot,
                         const uint8_t* dead, uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
+/* Both expert GEMMs on a plan: moe_w13_swiglu_grouped (hq / hs, and swiglu_debug when flags ask for
+ * it) followed by moe_w2_grouped (y, plan order, before the routing weight), with the same
+ * arguments and results as those two calls. For decode-sized batches (at most 32 plan rows per
+ * expert on average) they run as ONE persistent launch: each CTA streams its down-projection weight
+ * tiles as soon as it has finished its gate/up tiles, and gathers an expert's h rows once every
+ * gate/up tile of that expert is stored (per-expert counters in the workspace, zeroed by this call
+ * before the launch). ws: workspace of moe_workspace_bytes(shape). */
+MOE_API int moe_experts_grouped(const moe_shape* shape, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13,
+                                const uint8_t* w13_s, const uint8_t* w2, const uint8_t* w2_s,
+                                const int32_t* expert_offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs,
+                                float* swiglu_debug, float* y, void* ws, size_t ws_bytes, void* stream);
+
 /* The whole layer: route -> quant -> W13+SwiGLU+requant -> W2 -> combine, on one stream, no host
  * synchronisation and no allocation (capturable in a CUDA graph for a fixed shape).
  * `inter` (nullable) receives the intermediates the caller wants to keep. */

@@ -66,7 +66,7 @@ lib.moe_packed_w2_bytes.argtypes = [_SHP, ctypes.POINTER(_SZ)]
 lib.moe_quant_mxfp4.argtypes = [_I32, _I32, _P, _P, _P, _P]
 lib.moe_quant_mxfp8.argtypes = [_I32, _I32, _P, _P, _P, _P]
 lib.moe_quant_mxfp8_plan.argtypes = [_SHP] + [_P] * 6 + [_P]
-lib.moe_experts_grouped.argtypes = [_SHP] + [_P] * 13 + [_P, _SZ, _P]
+lib.moe_experts_grouped.argtypes = [_SHP] + [_P] * 12 + [_P, _SZ, _P]
 lib.moe_dead_from_survival.argtypes = [_I32, _P, ctypes.c_float, _P, _P]
 lib.moe_pack_w13.argtypes = [_SHP, _P, _P, _P, _P, _P]
 lib.moe_pack_w2.argtypes = [_SHP, _P, _P, _P, _P, _P]

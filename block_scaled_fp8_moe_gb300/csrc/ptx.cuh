@@ -70,6 +70,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+#ifndef MOE_WAIT_HINT_NS
+#define MOE_WAIT_HINT_NS 1000000    // how long a waiting thread may stay suspended per try (it wakes
+                                    // as soon as the phase completes)
+#endif
+
+// try_wait with a suspend-time hint: the thread sleeps until the phase completes or the hint
+// expires, instead of returning at once, so waiting threads do not keep polling shared memory.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"((uint32_t)MOE_WAIT_HINT_NS)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait. Returns false (after recording `code` in *err) once `limit_ns` has passed, or at
 // once if another thread of the CTA already gave up (*abort != 0). With abort == nullptr the wait
 // ignores other threads' give-ups and ends only on completion or on its own limit (used to drain
@@ -79,7 +98,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (MOE_WAIT_HINT_NS > 0 ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (abort && *abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       if (abort) *abort = 1;

@@ -105,3 +105,22 @@ def test_dead_from_survival_host_checks(B):
     assert B.lib.moe_dead_from_survival(4, n, float("nan"), n, n) == B.MOE_ERR_INVALID_ARG
     odd = ctypes.c_void_p(0x1002)                                               # not 4-byte aligned
     assert B.lib.moe_dead_from_survival(4, odd, 0.2, ctypes.c_void_p(0x2000), n) == B.MOE_ERR_INVALID_ARG
+
+
+def _prototypes():
+    """name -> number of parameters, from the declarations in include/moe.h."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(([^)]*)\)\s*;", text):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_the_header(B):
+    protos = _prototypes()
+    assert set(protos) == set(B.EXPORTED)
+    for name, n in protos.items():
+        fn = getattr(B.lib, name)
+        assert fn.argtypes is not None and len(fn.argtypes) == n, (name, n, fn.argtypes)

@@ -2,7 +2,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <cstdlib>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -13,16 +12,6 @@ namespace {
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// W13 + W2 as one launch for decode-sized tiles (MOE_FUSED=1 in the environment, read once; off by
-// default while it is measured against the two launches).
-bool fused_gemms_enabled() {
-  static int on = -1;
-  if (on < 0) {
-    const char* v = getenv("MOE_FUSED");
-    on = (v && v[0] == '1') ? 1 : 0;
-  }
-  return on == 1;
-}
 
 }  // namespace
 
@@ -155,7 +144,7 @@ extern "C" int moe_experts_grouped(const moe_shape* s, const uint8_t* xq, const 
   uint32_t* status = ws_ptr<uint32_t>(ws, L.status);
   float* dbg = (s->flags & MOE_FLAG_SWIGLU_DEBUG) ? swiglu_debug : nullptr;
   const bool plan_order = (s->flags & MOE_FLAG_X_PLAN_ORDER) != 0;
-  if (fused_gemms_enabled() && fused_gemms_supported(s) && !plan_order) {
+  if (fused_gemms_supported(s) && !plan_order) {
     uint32_t* ready = ws_ptr<uint32_t>(ws, L.ready);
     if (cudaMemsetAsync(ready, 0, sizeof(uint32_t) * s->E, st) != cudaSuccess) return MOE_ERR_CUDA;
     return launch_w13_w2_fused(s, xq, xs, w13, w13_s, w2, w2_s, expert_offsets, slot_of_row, hq, hs, dbg, y, status,
@@ -257,7 +246,7 @@ int forward_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router
   // decode-sized tiles run W13 and W2 as one persistent launch (its per-expert counters are zeroed
   // by this call's plan kernel)
   uint32_t* ready = ws_ptr<uint32_t>(ws, L.ready);
-  const bool fuse_gemms = fused_gemms_enabled() && fused_gemms_supported(s);
+  const bool fuse_gemms = fused_gemms_supported(s);
   bool quant_done = false;
   rc = launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, ws, st,
                     xq, xs, &quant_done, anchor, fuse_gemms ? ready : nullptr);

@@ -237,7 +237,8 @@ MOE_API int moe_experts_grouped(const moe_shape* shape, const uint8_t* xq, const
                                 float* swiglu_debug, float* y, void* ws, size_t ws_bytes, void* stream);
 
 /* The whole layer: route -> quant -> W13+SwiGLU+requant -> W2 -> combine, on one stream, no host
- * synchronisation and no allocation (capturable in a CUDA graph for a fixed shape).
+ * synchronisation and no allocation (capturable in a CUDA graph for a fixed shape). For
+ * decode-sized batches W13 and W2 run as one launch, as in moe_experts_grouped.
  * `inter` (nullable) receives the intermediates the caller wants to keep. */
 MOE_API int moe_forward(const moe_shape* shape, const uint16_t* x, const uint16_t* w_router, const float* bias,
                 const uint8_t* dead, const uint8_t* w13, const uint8_t* w13_s, const uint8_t* w2,

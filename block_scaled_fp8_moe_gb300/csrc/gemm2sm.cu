@@ -14,12 +14,14 @@
 // token-operand traffic per SM against one-CTA tiles. A row's result is the same as on any other
 // tile kind: same K order, same fp32 accumulation per column, the same epilogue code (gemm.cuh).
 //
-// Roles (384 threads per CTA, one CTA per SM, both CTAs of a pair run the same code):
+// Roles (both CTAs of a pair run the same code; 384 threads with one pair per SM pair, 256 with
+// two):
 //   warp 0      weight TMA (FP4 tile unpacked to 8-bit containers) and its 512-byte scale block
 //   warp 1      token TMA (one box of tw/2 plan rows) and the scale bytes of all tw columns
+//               (the weight and token boxes of both CTAs complete on the even CTA's stage barrier)
 //   warp 2      even CTA: tcgen05.cp of the scale blocks and the pair's MMAs, commits multicast to
-//               both CTAs' stage and accumulator barriers; odd CTA: relays "stage full" to the even
-//               CTA once its own stage has landed. Both: the pair's TMEM allocation.
+//               both CTAs' stage and accumulator barriers; odd CTA: tells the even CTA when its
+//               scale bytes for a stage have landed. Both: the pair's TMEM allocation.
 //   warps 4-11  epilogue of the CTA's 128 accumulator rows (two sets of four warps, alternating
 //               column groups): SwiGLU + MXFP8 requant (W13) or plan-order fp32 rows (W2); each set
 //               tells the even CTA when an accumulator slot is free again.
@@ -174,6 +176,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, Pair
       uint32_t phase = 0;
       bool ok = true;
       const uint32_t tile_bytes = p.a_fp8 ? 2 * kTileCodeBytes : kTileCodeBytes;
+      // the weight and token boxes of BOTH CTAs complete on the even CTA's stage barrier: its
+      // producer announces all of them; the odd CTA's own barrier only counts its scale copies
+      const uint32_t leader_full = mapa_shared(&full[0], 0);
+      const uint32_t expect = rank == 0 ? 2 * (tile_bytes + Pair::kTileB) + kTileScaleBytes : kTileScaleBytes;
       for (int w = pair; w < total && ok; w += npairs) {
         int e, mp, row0, nrows, tw;
         decode(w, e, mp, row0, nrows, tw);
@@ -188,8 +194,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, Pair
           }
           uint8_t* sA = tiles + stage * Pair::kStageBytes;
           uint8_t* sSFA = sA + Pair::kTileA + Pair::kTileB;
-          mbar_arrive_expect_tx(&full[stage], tile_bytes + kTileScaleBytes + Pair::kTileB);
-          tma_load_2d(sA, &tmap_a, 0, (tile0 + kc) * 128, &full[stage]);
+          mbar_arrive_expect_tx(&full[stage], expect);
+          tma_load_2d_pair(sA, &tmap_a, 0, (tile0 + kc) * 128, leader_full + (uint32_t)(stage * 8));
           bulk_load(sSFA, p.a_scales + (size_t)(tile0 + kc) * kTileScaleBytes, kTileScaleBytes, &full[stage]);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
@@ -204,6 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, Pair
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    const uint32_t leader_full = mapa_shared(&full[0], 0);
     for (int w = pair; w < total; w += npairs) {
       int e, mp, row0, nrows, tw;
       decode(w, e, mp, row0, nrows, tw);
@@ -213,7 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, Pair
         if (ok) {
           uint8_t* sB = tiles + stage * Pair::kStageBytes + Pair::kTileA;
           uint8_t* sSFB = sB + Pair::kTileB + 512;
-          if (lane == 0) tma_load_2d(sB, &tmap_b, kc * 128, brow, &full[stage]);
+          if (lane == 0) tma_load_2d_pair(sB, &tmap_b, kc * 128, brow, leader_full + (uint32_t)(stage * 8));
 #pragma unroll
           for (int i = 0; i < (Pair::BN + 31) / 32; ++i) {
             const int c = lane + 32 * i;
@@ -282,7 +289,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, Pair
       tc_commit_pair_mc(drain, 0x1);
       mbar_wait(drain, 0, kWaitLimitNs, nullptr, p.status, DEV_TIMEOUT_DRAIN);
     } else if (lane == 0) {
-      // ===================== relay (odd CTA): "my half of this stage has landed" =====================
+      // ===================== relay (odd CTA): "my scale bytes for this stage have landed" =====================
+      // (its weight and token boxes complete on the even CTA's barrier directly; only the small
+      // scale copies, which complete on this CTA's barrier, are relayed)
       const uint32_t leader_full = mapa_shared(&full[0], 0);
       int stage = 0;
       uint32_t phase = 0;

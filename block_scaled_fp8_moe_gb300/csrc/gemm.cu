@@ -29,8 +29,6 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <cstdlib>
-
 #include "common.cuh"
 #include "gemm.cuh"
 #include "mx.cuh"
@@ -128,8 +126,12 @@ struct Smem {
   static constexpr int kMisc = 1024;                            // barriers, flags
   static constexpr int kRows = 128 * 8;                         // gather row table
   static constexpr int kFixed = 1024 + kTiles + kXchg + kMisc + kRows;
-  // + (E + 1) * 12 bytes of plan tables, sized per launch
-  static int total(int E) { return kFixed + (int)align_up((size_t)(E + 1) * 12, 16); }
+  // + plan tables sized per launch: (E + 1) x (offsets, tile starts) ints, and a second table of
+  // tile starts when one launch runs both GEMMs
+  static int total(int E, bool two_gemms) {
+    return kFixed + (int)align_up((size_t)(E + 1) * (two_gemms ? 12 : 8), 16);
+  }
+  static_assert(kFixed + (kMaxE + 1) * 8 + 16 <= 227 * 1024, "shared memory per CTA at the largest E");
 };
 
 // MODE 0: the down projection (W2); 1: gate/up with SwiGLU and requant (W13); 2: W13 then W2 in
@@ -573,31 +575,14 @@ static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const C
                           const GemmParams& gp2, long long max_items, cudaStream_t st) {
   using L = Smem<BN>;
   auto kern = grouped_gemm_kernel<BN, MODE>;
-  const int smem = L::total(gp.E);
-  if (ensure_smem_limit((const void*)kern, L::total(kMaxE))) return MOE_ERR_CUDA;
+  const int smem = L::total(gp.E, MODE == 2);
+  if (ensure_smem_limit((const void*)kern, L::total(kMaxE, MODE == 2))) return MOE_ERR_CUDA;
   // persistent grid: as many CTAs as fit on the GPU at once (smem depends on E); the one-launch
   // W13 + W2 mode relies on every CTA being resident
   const int occ = ctas_per_sm_by_smem((size_t)smem, L::kCtasPerSm);
   const long long grid = std::min<long long>(max_items, (long long)occ * num_sms());
   if (grid <= 0) return MOE_OK;
   return launch_pdl(kern, dim3((unsigned)grid), dim3(Threads<BN>::kCount), (size_t)smem, st, tm, tmb, tm2, gp, gp2);
-}
-
-// Which wide-tile GEMMs run on CTA pairs: 0 none, 1 W13 only, 2 W13 and W2, 3 (default) only a
-// down projection with a short K (fewer than 8 K-chunks), where the pairs measured faster (MOE_PAIR
-// in the environment, read once, for measurements).
-static int pair_mode() {
-  static int mode = -1;
-  if (mode < 0) {
-    const char* v = getenv("MOE_PAIR");
-    mode = (v && v[0] >= '0' && v[0] <= '3') ? v[0] - '0' : 3;
-  }
-  return mode;
-}
-
-static bool use_pairs(bool w13, int KC) {
-  const int m = pair_mode();
-  return m == 3 ? (!w13 && KC < 8) : m >= (w13 ? 1 : 2);
 }
 
 static int weight_tmap(CUtensorMap* tm, const moe_shape* s, const uint8_t* codes, const GemmParams& gp, int box_tiles) {
@@ -610,13 +595,14 @@ static int launch_gemm(const moe_shape* s, const uint8_t* codes, const GemmParam
   const long long slots = (long long)s->T * s->k;
   // TMA row coordinates of the packed weights are 32-bit: 128 rows per tile
   if ((long long)s->E * gp.MT * gp.KC * 128 >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  int bn = pick_bn(s);
-  if (bn >= 128 && use_pairs(W13, gp.KC)) return launch_gemm_pair(s, codes, gp, W13, st);
-  // a down projection with a short K (fewer than 8 chunks) is bound by its epilogue's per-slot
-  // stores, not by the MMA rate: it keeps 128-row token tiles
-  if (!W13 && bn > 128 && gp.KC < 8) bn = 128;
+  const int bn = pick_bn(s);
+  // a wide down projection with a short K (fewer than 8 K-chunks of 128) runs on CTA pairs: each of
+  // its tiles is short work with a long epilogue of per-slot stores, and the pairs' extra pipelines
+  // per SM keep the tensor cores fed through it (measured faster than one-CTA tiles; with a long K,
+  // and for the gate/up GEMM, the one-CTA wide tiles measured faster)
+  if (!W13 && bn > 64 && gp.KC < 8) return launch_gemm_pair(s, codes, gp, false, st);
   CUtensorMap tm;
-  const int box_tiles = (bn <= 32) ? Smem<16>::KT : (bn <= 64 ? Smem<64>::KT : (bn == 128 ? Smem<128>::KT : Smem<MOE_WIDE_BN>::KT));
+  const int box_tiles = (bn <= 32) ? Smem<16>::KT : (bn <= 64 ? Smem<64>::KT : Smem<MOE_WIDE_BN>::KT);
   int rc0 = weight_tmap(&tm, s, codes, gp, box_tiles);
   if (rc0) return rc0;
   // activation operand of the wide token tile as a TMA tensor: [T*k plan rows, K] bytes, boxes of
@@ -632,7 +618,6 @@ static int launch_gemm(const moe_shape* s, const uint8_t* codes, const GemmParam
     case 16: return launch_gemm_bn<16, M>(tm, tmb, tm, gp, gp, max_items, st);
     case 32: return launch_gemm_bn<32, M>(tm, tmb, tm, gp, gp, max_items, st);
     case 64: return launch_gemm_bn<64, M>(tm, tmb, tm, gp, gp, max_items, st);
-    case 128: return launch_gemm_bn<128, M>(tm, tmb, tm, gp, gp, max_items, st);
     default: return launch_gemm_bn<MOE_WIDE_BN, M>(tm, tmb, tm, gp, gp, max_items, st);
   }
 }

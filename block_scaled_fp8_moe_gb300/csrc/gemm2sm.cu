@@ -32,7 +32,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <cstdlib>
 
 #include "common.cuh"
 #include "gemm.cuh"
@@ -73,6 +72,8 @@ struct PairCfg {
   static_assert(kSfCol + kStages * kSfSlot <= kTmemCols, "TMEM columns");
   static_assert(BN % 32 == 0 && BN <= 256, "pair tile width");
   static_assert(CTAS == 1 || CTAS == 2, "pairs per SM pair");
+  static_assert(kFixed + (kMaxE + 1) * 8 + 16 <= (CTAS == 1 ? 227 * 1024 : 113 * 1024),
+                "shared memory per CTA at the largest E");
 };
 
 template <bool W13, class Pair>
@@ -402,30 +403,13 @@ static int launch_pair_t(const moe_shape* s, const uint8_t* codes, const GemmPar
                     gp);
 }
 
-// Pair tile configuration (MOE_PAIR_CFG in the environment, read once, for measurements): 0 = 224
-// columns, 5 stages, one pair per SM pair; 1 = 192 columns, 6 stages; 2 (default) = 192 columns,
-// 3 stages, two pairs per SM pair (fastest measured: the second pair keeps the SMs busy while the
-// first waits on its stages).
-static int pair_cfg() {
-  static int c = -1;
-  if (c < 0) {
-    const char* v = getenv("MOE_PAIR_CFG");
-    c = (v && v[0] >= '0' && v[0] <= '2') ? v[0] - '0' : 2;
-  }
-  return c;
-}
-
-template <bool W13>
-static int launch_pair_w(const moe_shape* s, const uint8_t* codes, const GemmParams& gp, cudaStream_t st) {
-  switch (pair_cfg()) {
-    case 1: return launch_pair_t<W13, PairCfg<192, 6, 1>>(s, codes, gp, st);
-    case 2: return launch_pair_t<W13, PairCfg<192, 3, 2>>(s, codes, gp, st);
-    default: return launch_pair_t<W13, PairCfg<224, 5, 1>>(s, codes, gp, st);
-  }
-}
+// The configuration in use: tiles of up to 192 columns, 3 stages, two pairs per SM pair (measured
+// fastest of {224 columns, 5 stages, one pair}, {192, 6, one pair}, {192, 3, two pairs}: the
+// second pair keeps each SM's tensor core fed while the first waits on its stages).
+using PairTile = PairCfg<192, 3, 2>;
 
 int launch_gemm_pair(const moe_shape* s, const uint8_t* codes, const GemmParams& gp, bool w13, cudaStream_t st) {
-  return w13 ? launch_pair_w<true>(s, codes, gp, st) : launch_pair_w<false>(s, codes, gp, st);
+  return w13 ? launch_pair_t<true, PairTile>(s, codes, gp, st) : launch_pair_t<false, PairTile>(s, codes, gp, st);
 }
 
 }  // namespace moe

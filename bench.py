@@ -378,8 +378,9 @@ class ClockSampler:
 # ----------------------------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------------------------
-def launches_per_step(cfg) -> int:
-    """Kernels one moe_forward launches for this shape (mirrors the library's dispatch)."""
+def launches_per_step(cfg, shared: bool = False) -> int:
+    """Kernels one moe_forward launches for this shape (mirrors the library's dispatch); `shared`:
+    with a shared expert (its identity plan and two GEMMs on the side stream)."""
     T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
     nc = H // 64
     decode_router = T <= 64 and 2 * nc <= 256 and (min(T, 16) * nc * 144 + 2 * T * nc * 4) <= 210 * 1024
@@ -392,7 +393,10 @@ def launches_per_step(cfg) -> int:
     n += 1 if T <= 256 else 4                         # top-k + plan (+ grid-wide select, scan, scatter)
     if not decode_router:
         n += 1                                        # MXFP8 quantisation (straight into plan order when wide)
-    return n + (2 if fused_gemms(cfg) else 3)         # W13 + W2 (one launch for decode tiles), combine
+    if fused_gemms(cfg):
+        # W13 + W2 (+ the combine, unless a shared expert's row is added in a separate combine)
+        return n + (1 + 3 + 1 if shared else 1)
+    return n + 3 + (3 if shared else 0)               # W13, W2, combine (+ the shared expert's three)
 
 
 def wide_w13(cfg) -> bool:
@@ -782,7 +786,7 @@ def gpu_arm(args):
                        **({"shared_expert_inter": args.shared_inter, "shared_expert": "MXFP8, side stream"}
                           if args.shared_inter else {})},
             "step_ms": head["step_ms"],
-            "e2e": e2e, "gpu_launches": (launches_per_step(cfg) + (3 if args.shared_inter else 0)) * args.steps,
+            "e2e": e2e, "gpu_launches": launches_per_step(cfg, bool(args.shared_inter)) * args.steps,
             "clocks": head["clocks"],
             "roofline": head["roofline"],
             "w2_roofline": head["w2_roofline"],

@@ -146,7 +146,7 @@ extern "C" int moe_experts_grouped(const moe_shape* s, const uint8_t* xq, const 
   const bool plan_order = (s->flags & MOE_FLAG_X_PLAN_ORDER) != 0;
   if (fused_gemms_supported(s) && !plan_order) {
     uint32_t* ready = ws_ptr<uint32_t>(ws, L.ready);
-    if (cudaMemsetAsync(ready, 0, sizeof(uint32_t) * s->E, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(ready, 0, sizeof(uint32_t) * (s->E + 1), st) != cudaSuccess) return MOE_ERR_CUDA;
     return launch_w13_w2_fused(s, xq, xs, w13, w13_s, w2, w2_s, expert_offsets, slot_of_row, hq, hs, dbg, y, status,
                                ready, st);
   }
@@ -301,9 +301,12 @@ int forward_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router
       }
     }
   }
+  // with no shared expert to add, the one-launch GEMMs also run the combine at their end
+  const bool fused_combine = fuse_gemms && !shared;
   if (fuse_gemms) {
     rc = launch_w13_w2_fused(s, xq, xs, w13, w13_s, w2, w2_s, offsets, slot_of_row, hq, hs, im.swiglu, y, status,
-                             ready, st);
+                             ready, st, fused_combine ? topk_w : nullptr, fused_combine ? row_of_slot : nullptr,
+                             fused_combine ? out : nullptr);
   } else {
     rc = launch_w13(s, xq, xs, w13, w13_s, offsets, slot_of_row, hq, hs, im.swiglu, status, xqp, xsp, plan_rows, st);
     if (!rc) rc = launch_w2(s, hq, hs, w2, w2_s, offsets, slot_of_row, y, status, st);
@@ -313,6 +316,7 @@ int forward_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router
     cudaEventDestroy(ev_join);
   }
   if (rc) return rc;
+  if (fused_combine) return MOE_OK;
   return launch_combine(s, y, topk_w, row_of_slot, out, st, y_shared, dead, status);
 }
 

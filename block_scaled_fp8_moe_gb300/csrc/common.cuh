@@ -77,7 +77,7 @@ inline Workspace workspace_layout(const moe_shape* s) {
   w.wnorm = take(E * 4);
   w.cand = take(T * 64 * 4);
   w.ncand = take(T * 4);
-  w.ready = take(E * 4);
+  w.ready = take((E + 1) * 4);
   w.total = off;
   return w;
 }
@@ -187,19 +187,21 @@ int launch_quant_mxfp8_plan(int rows, int cols, int k, const uint16_t* x, uint8_
 bool w13_wants_plan_rows(const moe_shape* s);
 // When xq/xs are given and the small-batch router runs, it also writes the MXFP8 quantisation of x
 // and sets *quant_done. anchor (nullable): rows that reuse another row's experts. ready (nullable):
-// E per-expert counters the plan kernel zeroes for the one-launch W13 + W2 GEMM.
+// E + 1 counters the plan kernel zeroes for the one-launch W13 + W2 GEMM.
 int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, const uint8_t* dead,
                  int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
                  int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done,
                  const int32_t* anchor, uint32_t* ready);
 // W13 then W2 in one persistent launch, for decode-sized token tiles (fused_gemms_supported):
-// writes hq/hs (and dbg) like launch_w13 and y like launch_w2. ready: E counters, zeroed by the
-// plan kernel of this layer call.
+// writes hq/hs (and dbg) like launch_w13 and y like launch_w2, and with out non-null also the
+// combine's output, like launch_combine without a shared expert or dead mask. ready: E + 1
+// counters, zeroed by the plan kernel of this layer call.
 bool fused_gemms_supported(const moe_shape* s);
 int launch_w13_w2_fused(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13,
                         const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, const int32_t* offsets,
                         const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg, float* y, uint32_t* status,
-                        uint32_t* ready, cudaStream_t st);
+                        uint32_t* ready, cudaStream_t st, const float* topk_w = nullptr,
+                        const int32_t* row_of_slot = nullptr, uint16_t* out = nullptr);
 int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
                const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
                uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, bool plan_rows_ready, cudaStream_t st,

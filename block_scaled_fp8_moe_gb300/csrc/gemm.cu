@@ -29,6 +29,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "combine.cuh"
 #include "common.cuh"
 #include "gemm.cuh"
 #include "mx.cuh"
@@ -532,13 +533,37 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
             epi_w2_chunk(r, qd, lane, c0, m, row0, nrows, q);
         }
       }
+      if (kFused) __threadfence();                    // this lane's stores of the tile, before the count
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && ok) mbar_arrive(&acc_empty[acc]);
-      if (kFused && w13_item && lane == 0 && ok) {
-        // this warp's stores of the tile are done (the set's named barrier ordered them): publish
+      if (kFused && lane == 0 && ok) {
+        // publish the warp's part of the tile: per expert for a W13 tile (its h rows), in the grid
+        // total for a W2 tile (the combine waits for all of them)
         __threadfence();
-        atomicAdd(q.ready + e, 1u);
+        atomicAdd(w13_item ? q.ready + e : q.ready + E, 1u);
+      }
+    }
+    if (kFused && p2.out) {
+      // ===================== the combine, after every W2 tile of the grid =====================
+      // Unit u = (row t, 8 hidden features); the epilogue threads of all CTAs take units in turn.
+      // A warp with units waits (one lane, bounded) until every W2 tile is counted, then folds
+      // its rows exactly as the combine kernel does.
+      constexpr int kEpiThreads = Threads<BN>::kEpiWarps * 32;
+      const long long units = (long long)p2.T * (p2.H / 8);
+      const long long gt = (long long)blockIdx.x * kEpiThreads + (threadIdx.x - 128);
+      const long long gstride = (long long)gridDim.x * kEpiThreads;
+      if (gt - lane < units) {
+        uint32_t go = ok ? 1u : 0u;
+        if (lane == 0 && go)
+          go = wait_count_at_least(p2.ready + E, (uint32_t)(s_cum2[E] * Threads<BN>::kEpiWarps), kWaitLimitNs,
+                                   abort_flag, p2.status) ? 1u : 0u;
+        go = __shfl_sync(0xffffffffu, go, 0);
+        __syncwarp();
+        if (go)
+          for (long long u = gt; u < units; u += gstride)
+            combine_unit<true>(p2.y, p2.topk_w, p2.row_of_slot, (int)(u / (p2.H / 8)), (int)(u % (p2.H / 8)),
+                               p2.H, p2.k, p2.out, nullptr, nullptr, nullptr);
       }
     }
   }
@@ -747,7 +772,8 @@ bool fused_gemms_supported(const moe_shape* s) { return pick_bn(s) <= 32; }
 int launch_w13_w2_fused(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13,
                         const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, const int32_t* offsets,
                         const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg, float* y, uint32_t* status,
-                        uint32_t* ready, cudaStream_t st) {
+                        uint32_t* ready, cudaStream_t st, const float* topk_w, const int32_t* row_of_slot,
+                        uint16_t* out) {
   if (s->T == 0) return MOE_OK;
   const int bn = pick_bn(s);
   if (bn > 32 || !ready) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -755,6 +781,13 @@ int launch_w13_w2_fused(const moe_shape* s, const uint8_t* xq, const uint8_t* xs
   GemmParams g2 = w2_params(s, hq, hs, w2, w2s, offsets, slot_of_row, y, status, false);
   g13.ready = ready;
   g2.ready = ready;
+  if (out) {
+    if (!topk_w || !row_of_slot) return MOE_ERR_INVALID_ARG;
+    g2.topk_w = topk_w;
+    g2.row_of_slot = row_of_slot;
+    g2.out = out;
+    g2.T = s->T;
+  }
   if ((long long)s->E * std::max(g13.MT * g13.KC, g2.MT * g2.KC) * 128 >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
   CUtensorMap t13, t2;
   int rc = weight_tmap(&t13, s, w13, g13, Smem<16>::KT);

@@ -38,10 +38,17 @@ struct GemmParams {
   // W2 output: per-slot rows in plan order, before the routing weight
   float* y;
   uint32_t* status;
-  // W13 then W2 in one launch: W13 epilogue warps count finished tiles per expert here (after their
-  // stores), and a W2 tile gathers its expert's rows only once every W13 tile of that expert has
-  // been counted. Zeroed by the plan kernel before each layer call.
+  // W13 then W2 in one launch: W13 epilogue warps count finished tiles per expert in ready[0..E)
+  // (after their stores), and a W2 tile gathers its expert's rows only once every W13 tile of that
+  // expert has been counted; W2 epilogue warps count their finished tiles in ready[E]. Zeroed by the
+  // plan kernel before each layer call.
   uint32_t* ready;
+  // ... and, when out is set, the fixed-order combine of the T rows at the end of the launch, once
+  // ready[E] says every W2 tile is stored
+  const float* topk_w;
+  const int32_t* row_of_slot;
+  uint16_t* out;
+  int T;
 };
 
 

@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "combine.cuh"
 #include "common.cuh"
 #include "mx.cuh"
 #include "ptx.cuh"
@@ -562,9 +563,9 @@ __global__ void __launch_bounds__(512) topk_plan_single_kernel(const float* __re
                                                                uint32_t* __restrict__ ready) {
   pdl_trigger();
   pdl_wait();
-  // per-expert tile counters of the one-launch W13 + W2 GEMM (nullable): zero before it runs
+  // tile counters of the one-launch W13 + W2 GEMM (E per expert + 1 total; nullable): zero them
   if (ready)
-    for (int e = threadIdx.x; e < E; e += blockDim.x) ready[e] = 0;
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) ready[e] = 0;
   extern __shared__ __align__(16) uint8_t psm[];
   uint32_t* mask = reinterpret_cast<uint32_t*>(psm);
   int16_t* sidx = reinterpret_cast<int16_t*>(psm + align_up((size_t)E * 8 * 4, 16));
@@ -626,7 +627,7 @@ __global__ void __launch_bounds__(512) plan_scan_kernel(const int32_t* __restric
   pdl_trigger();
   pdl_wait();
   if (ready)
-    for (int e = threadIdx.x; e < E; e += blockDim.x) ready[e] = 0;
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) ready[e] = 0;
   __shared__ int tot[kMaxE];
   __shared__ int total_s;
   constexpr int U = 8;                            // block counts loaded per step (all in flight)
@@ -818,45 +819,8 @@ __global__ void combine_kernel(const float* __restrict__ y, const float* __restr
   pdl_wait();
   const int H8 = H / 8;
   const long long n = (long long)T * H8;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(i / H8), h8 = (int)(i % H8);
-    float acc[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-    const bool held = row_of_slot[(size_t)t * k] >= 0;
-    const bool flagged = dead != nullptr && dead[t] != 0;
-    if (flagged && held && h8 == 0 && status) atomicCAS(status, 0u, (uint32_t)DEV_BAD_INPUT);
-    const bool live = held && !flagged;
-    if (live) {
-      for (int j = 0; j < k; ++j) {
-        const int r = __ldg(row_of_slot + (size_t)t * k + j);
-        const float w = __ldg(topk_w + (size_t)t * k + j);
-        const float4* yp = reinterpret_cast<const float4*>(y + (size_t)r * H) + 2 * h8;
-        const float4 a = __ldg(yp), b = __ldg(yp + 1);
-        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float wv = __fmul_rn(w, v[q]);
-          acc[q] = (j == 0) ? wv : __fadd_rn(acc[q], wv);
-        }
-      }
-      if (y_shared) {
-        const float4* yp = reinterpret_cast<const float4*>(y_shared + (size_t)t * H) + 2 * h8;
-        const float4 a = __ldg(yp), b = __ldg(yp + 1);
-        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], v[q]);
-      }
-    }
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * q] + 0.0f));
-      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * q + 1] + 0.0f));
-      o[q] = lo | (hi << 16);
-    }
-    *reinterpret_cast<uint4*>(out + (size_t)t * H + 8 * h8) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    combine_unit<false>(y, topk_w, row_of_slot, (int)(i / H8), (int)(i % H8), H, k, out, y_shared, dead, status);
 }
 
 int launch_combine(const moe_shape* s, const float* y, const float* topk_w, const int32_t* row_of_slot,

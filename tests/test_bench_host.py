@@ -30,9 +30,9 @@ def test_decode_router_predicate_matches_the_library_constants():
         for H in (256, 4096, 8192, 16384):
             cfg = synth.custom("p", T, H, 256, 8, 128, seed=0)
             n = bench.launches_per_step(cfg)
-            fused = 1 if T * 8 / 256 <= 32 else 0          # one launch for W13 + W2 (decode tiles)
+            fused = 2 if T * 8 / 256 <= 32 else 0          # one launch for W13 + W2 + combine (decode tiles)
             if _decode_router(T, H):
-                assert n == 5 - fused, (T, H)      # router (+ quant), top-k + plan, W13 (+) W2, combine
+                assert n == 5 - fused, (T, H)      # router (+ quant), top-k + plan, W13, W2, combine
             else:
                 assert n >= 6 - fused, (T, H)      # separate quantiser and a non-decode router
 
@@ -40,7 +40,9 @@ def test_decode_router_predicate_matches_the_library_constants():
 def test_launch_counts_of_the_benchmarked_workloads():
     counts = {name: bench.launches_per_step(synth.CONFIGS[name]) for name in
               ("decode-6", "decode-48", "prefill-4k", "prefill-32k")}
-    # decode: fused router+quant, top-k/plan, W13 + W2 in one launch, combine; prefill: norms,
+    # decode: fused router+quant, top-k/plan, W13 + W2 + combine in one launch; prefill: norms,
     # screen, exact recompute, grid-wide select, plan, scan, scatter, quantiser into plan order,
     # W13, W2, combine
-    assert counts == {"decode-6": 4, "decode-48": 4, "prefill-4k": 11, "prefill-32k": 11}
+    assert counts == {"decode-6": 3, "decode-48": 3, "prefill-4k": 11, "prefill-32k": 11}
+    # with a shared expert the combine is its own launch after the side stream joins
+    assert bench.launches_per_step(synth.CONFIGS["decode-6"], shared=True) == 7

@@ -97,7 +97,7 @@ def median_ci(values, level=0.95, resamples=2000, seed=0):
             "mean": round(float(v.mean()), 5), "n": int(v.size)}
 
 
-GEMM_SOURCES = ("gemm.cu", "gemm.cuh", "gemm2sm.cu", "ptx.cuh", "mx.cuh", "common.cuh")
+GEMM_SOURCES = ("gemm.cu", "gemm.cuh", "gemm2sm.cu", "gemm_ws.cu", "combine.cuh", "ptx.cuh", "mx.cuh", "common.cuh")
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -462,16 +462,22 @@ def mma_peak(gpu, stream, ws, bf16_tflops, peak_src) -> dict:
     launches) and 2 x the measured bf16 peak."""
     from block_scaled_fp8_moe_gb300 import binding as B
     iters = 16384
-    B.moe_probe_mma_rate(256, ws)                              # warm-up launch
-    best = 0.0
-    ctas = flops = 0
-    for _ in range(5):
-        e0, e1 = gpu.events(1)[0]
-        e0.record(stream)
-        ctas, flops = B.moe_probe_mma_rate(iters, ws)
-        e1.record(stream)
-        e1.synchronize()
-        best = max(best, flops / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+    def rate(mode):
+        B.moe_probe_mma_rate(256, ws, mode)                    # warm-up launch
+        best = 0.0
+        ctas = 0
+        for _ in range(5):
+            e0, e1 = gpu.events(1)[0]
+            e0.record(stream)
+            ctas, flops = B.moe_probe_mma_rate(iters, ws, mode)
+            e1.record(stream)
+            e1.synchronize()
+            best = max(best, flops / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+        return best, ctas
+    best, ctas = rate(0)
+    # the same instruction stream as the grouped GEMMs' wide tiles issue it (context, not the peak):
+    # 4 rotating operand buffers, scale copies before each K-chunk, N = 224
+    gemm_like, _ = rate(7)
     B.moe_check_device_status(ws)
     doubled = FP8_OVER_BF16 * bf16_tflops
     use_probe = best >= doubled
@@ -479,7 +485,8 @@ def mma_peak(gpu, stream, ws, bf16_tflops, peak_src) -> dict:
             "source": ("tcgen05 kind::mxf8f6f4 rate probe (M=128 N=256 K=32, operands resident, "
                        f"{ctas} CTAs, best of 5)") if use_probe else
                       f"{peak_src} bf16 x {FP8_OVER_BF16} (nominal fp8/bf16 ratio)",
-            "probe_tflops": round(best, 1), "bf16_x2_tflops": round(doubled, 1)}
+            "probe_tflops": round(best, 1), "bf16_x2_tflops": round(doubled, 1),
+            "gemm_sequence_tflops": round(gemm_like, 1)}
 
 
 def measure(cfg, args, gpu, world, headline: bool, peak_info=None):

@@ -75,7 +75,7 @@ lib.moe_w13_swiglu_grouped.argtypes = [_SHP] + [_P] * 9 + [_P, _SZ, _P]
 lib.moe_w2_combine_grouped.argtypes = [_SHP] + [_P] * 10 + [_P, _SZ, _P]
 lib.moe_w2_grouped.argtypes = [_SHP] + [_P] * 7 + [_P, _SZ, _P]
 lib.moe_combine.argtypes = [_SHP] + [_P] * 5 + [_P, _SZ, _P]
-lib.moe_probe_mma_rate.argtypes = [_I32, ctypes.POINTER(_I32), ctypes.POINTER(ctypes.c_int64), _P, _SZ, _P]
+lib.moe_probe_mma_rate.argtypes = [_I32, _I32, ctypes.POINTER(_I32), ctypes.POINTER(ctypes.c_int64), _P, _SZ, _P]
 lib.moe_forward.argtypes = [_SHP] + [_P] * 9 + [ctypes.POINTER(MoeIntermediates), _P, _SZ, _P]
 lib.moe_check_device_status.argtypes = [_P, _P]
 lib.moe_route_topk_noalloc.argtypes = [_SHP] + [_P] * 10 + [_P]
@@ -405,13 +405,13 @@ def moe_forward(shp: MoeShape, x, w_router, bias, dead, w13p, w13sp, w2p, w2sp, 
     return out
 
 
-def moe_probe_mma_rate(iters: int, ws, stream=None) -> tuple[int, int]:
+def moe_probe_mma_rate(iters: int, ws, mode: int = 0, stream=None) -> tuple[int, int]:
     """Launch the block-scaled MMA rate probe (time it with events on `stream`); returns
-    (CTAs, FLOPs of the launch)."""
+    (CTAs, FLOPs of the launch). mode: see include/moe.h (0 = the tensor-peak denominator)."""
     ctas = _I32(0)
     flops = ctypes.c_int64(0)
-    _check(lib.moe_probe_mma_rate(int(iters), ctypes.byref(ctas), ctypes.byref(flops), _ptr(ws), ws.numel(),
-                                  _stream(stream)), "moe_probe_mma_rate")
+    _check(lib.moe_probe_mma_rate(int(iters), int(mode), ctypes.byref(ctas), ctypes.byref(flops), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "moe_probe_mma_rate")
     return int(ctas.value), int(flops.value)
 
 

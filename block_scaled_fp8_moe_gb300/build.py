@@ -10,7 +10,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
-SOURCES = ["quant.cu", "route.cu", "router_screen.cu", "gemm.cu", "gemm2sm.cu", "api.cu", "peak.cu"]
+SOURCES = ["quant.cu", "route.cu", "router_screen.cu", "gemm.cu", "gemm2sm.cu", "gemm_ws.cu", "api.cu", "peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xcompiler", "-fvisibility=hidden"]

@@ -621,11 +621,9 @@ static int launch_gemm(const moe_shape* s, const uint8_t* codes, const GemmParam
   // TMA row coordinates of the packed weights are 32-bit: 128 rows per tile
   if ((long long)s->E * gp.MT * gp.KC * 128 >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
   const int bn = pick_bn(s);
-  // a wide down projection with a short K (fewer than 8 K-chunks of 128) runs on CTA pairs: each of
-  // its tiles is short work with a long epilogue of per-slot stores, and the pairs' extra pipelines
-  // per SM keep the tensor cores fed through it (measured faster than one-CTA tiles; with a long K,
-  // and for the gate/up GEMM, the one-CTA wide tiles measured faster)
-  if (!W13 && bn > 64 && gp.KC < 8) return launch_gemm_pair(s, codes, gp, false, st);
+  // a wide down projection with a short K keeps each weight panel resident while the expert's token
+  // tiles stream past it (gemm_ws.cu); with a long K, and for the gate/up GEMM, one-CTA wide tiles
+  if (!W13 && bn > 64 && ws_down_supported(s)) return launch_gemm_ws(s, codes, gp, st);
   CUtensorMap tm;
   const int box_tiles = (bn <= 32) ? Smem<16>::KT : (bn <= 64 ? Smem<64>::KT : Smem<MOE_WIDE_BN>::KT);
   int rc0 = weight_tmap(&tm, s, codes, gp, box_tiles);

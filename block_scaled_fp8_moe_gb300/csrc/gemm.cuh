@@ -243,5 +243,9 @@ inline int make_act_tmap(CUtensorMap* m, const uint8_t* base, int row_bytes, lon
 // CTA-pair grouped GEMM (gemm2sm.cu) for wide token tiles: same inputs and results as the one-CTA
 // kernel's wide tiles.
 int launch_gemm_pair(const moe_shape* s, const uint8_t* codes, const GemmParams& gp, bool w13, cudaStream_t st);
+// Weight-stationary down projection (gemm_ws.cu) for a short K with wide token tiles: same inputs
+// and results as the one-CTA kernel's W2.
+bool ws_down_supported(const moe_shape* s);
+int launch_gemm_ws(const moe_shape* s, const uint8_t* codes, const GemmParams& gp, cudaStream_t st);
 
 }  // namespace moe

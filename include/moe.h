@@ -312,12 +312,15 @@ MOE_API int moe_selftest_timeout(void* ws, uint64_t limit_ns, void* stream);
 /* Rate probe of the block-scaled tensor-core instruction the grouped GEMMs use (tcgen05.mma
  * kind::mxf8f6f4, E2M1 x E4M3 with UE8M0 scales per 32; "New Deepseek 4.1 flash recipe", post 6
  * "How it works" item 1): one CTA per SM issues `iters` back-to-back M = 128, N = 256, K = 32 MMAs
- * from operands resident in shared memory, with nothing else to do. The caller times the call with
- * CUDA events on `stream`; *flops receives the multiply-add work (2 * 128 * 256 * 32 * iters *
- * CTAs) and *ctas the grid. It is the denominator of the prefill GEMMs' tensor utilisation, not part
- * of the layer. iters in [1, 2^24]; ws: at least 256 bytes, its first 4 bytes the status word. */
-MOE_API int moe_probe_mma_rate(int32_t iters, int32_t* ctas, int64_t* flops, void* ws, size_t ws_bytes,
-                               void* stream);
+ * from operands resident in shared memory, with nothing else to do (mode 0: the denominator of the
+ * prefill GEMMs' tensor utilisation). Mode bits move it toward what the GEMMs issue: bit 0, the
+ * K-chunks (4 MMAs each) read 4 different operand buffers in turn; bit 1, each K-chunk is preceded
+ * by its scale copies (tcgen05.cp of one A and two B scale atoms); bit 2, N = 224. The caller times
+ * the call with CUDA events on `stream`; *flops receives the multiply-add work (2 * 128 * N * 32 *
+ * iters * CTAs) and *ctas the grid. Not part of the layer. iters in [1, 2^24], mode in [0, 7];
+ * ws: at least 256 bytes, its first 4 bytes the status word. */
+MOE_API int moe_probe_mma_rate(int32_t iters, int32_t mode, int32_t* ctas, int64_t* flops, void* ws,
+                               size_t ws_bytes, void* stream);
 
 /* Allocation-free variant of moe_route_topk, for callers that cannot allocate device memory:
  * engines that reserved all of HBM for their own pool at start-up, or code running inside a host

@@ -110,20 +110,6 @@ def gemm_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def gemm_kind(name: str):
-    """Which GEMM a profiled kernel name is: 'experts' (W13 then W2 in one launch), 'w13' or 'w2'."""
-    import re
-    m = re.search(r"grouped_gemm_kernel<\s*\d+\s*,\s*(\d)\s*>", name)
-    if m:
-        return {"2": "experts", "1": "w13", "0": "w2"}[m.group(1)]
-    m = re.search(r"grouped_gemm_pair_kernel<\s*(\w+)\s*,", name)
-    if m:
-        return "w13" if m.group(1) in ("1", "true") else "w2"
-    if "grouped_gemm_ws_kernel" in name:
-        return "w2"
-    return None
-
-
 def record_traffic(raw_csv: str, workload: str) -> dict:
     """Average dram__bytes_read.sum + dram__bytes_write.sum per launch of each grouped GEMM."""
     import csv
@@ -134,9 +120,10 @@ def record_traffic(raw_csv: str, workload: str) -> dict:
     acc: dict = {}
     for r in rows[2:]:
         d = dict(zip(hdr, r))
-        key = gemm_kind(d.get("Kernel Name", ""))
-        if key is None:
+        name = d.get("Kernel Name", "")
+        if "grouped_gemm_kernel" not in name:
             continue
+        key = "w13" if name.rstrip().endswith("1>(CUtensorMap_st, CUtensorMap_st, GemmParams)") else "w2"
         b = sum(float(d[m]) * scale[unit[m]] for m in ("dram__bytes_read.sum", "dram__bytes_write.sum"))
         acc.setdefault(key, []).append(b)
     entry = {k: sum(v) / len(v) for k, v in acc.items()}

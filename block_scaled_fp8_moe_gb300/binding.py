@@ -295,8 +295,7 @@ def moe_w2_combine_grouped(shp: MoeShape, hq, hs, w2p, w2sp, plan: Plan, ws, out
 
 
 def moe_w2_grouped(shp: MoeShape, hq, hs, w2p, w2sp, plan: Plan, ws, y=None, stream=None):
-    """Down-projection GEMM alone: fp32 y in plan order, before the routing weight, panel-major
-    ([H/128][T*k][128] values; `y_rows_view` gives the [T*k, H] row view)."""
+    """Down-projection GEMM alone: fp32 rows y [T*k, H] in plan order, before the routing weight."""
     S = shp.T * shp.k
     y = torch.empty(max(S, 1), shp.H, dtype=torch.float32, device=hq.device) if y is None else y
     _check(lib.moe_w2_grouped(
@@ -304,12 +303,6 @@ def moe_w2_grouped(shp: MoeShape, hq, hs, w2p, w2sp, plan: Plan, ws, y=None, str
         _ptr(w2sp, torch.uint8), _ptr(plan.expert_offsets), _ptr(plan.slot_of_row),
         _ptr(y, torch.float32, S * shp.H, "y"), _ptr(ws), ws.numel(), _stream(stream)), "moe_w2_grouped")
     return y
-
-
-def y_rows_view(y, shp: MoeShape) -> torch.Tensor:
-    """The [T*k, H] row view (a copy) of a panel-major per-slot buffer [H/128][T*k][128]."""
-    S = shp.T * shp.k
-    return y.reshape(shp.H // 128, S, 128).permute(1, 0, 2).reshape(S, shp.H)
 
 
 def moe_combine(shp: MoeShape, y, plan: Plan, ws, dead=None, out=None, stream=None):

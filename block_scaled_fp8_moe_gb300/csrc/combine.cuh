@@ -16,16 +16,12 @@ namespace moe {
 // (+ y_shared[t]) ), r_j = row_of_slot[t k + j], w_j = topk_w[t k + j]; each w_j y is one fp32
 // multiply, the sum a left fold in fp32. Rows without slots (row_of_slot[t k] < 0) and rows the dead
 // mask flags get +0.0; a flagged row that still holds slots is recorded in *status.
-// y (y_rows rows) and y_shared (one row per token) are panel-major: feature f of row r at
-// ((f / 128) * rows + r) * 128 + f % 128.
 // kL2Only: y was written earlier in the same launch by other SMs, so it is read through L2 only.
 template <bool kL2Only>
-__device__ __forceinline__ void combine_unit(const float* __restrict__ y, int y_rows, const float* __restrict__ topk_w,
+__device__ __forceinline__ void combine_unit(const float* __restrict__ y, const float* __restrict__ topk_w,
                                              const int32_t* __restrict__ row_of_slot, int t, int h8, int H, int k,
                                              uint16_t* __restrict__ out, const float* __restrict__ y_shared,
-                                             int shared_rows, const uint8_t* __restrict__ dead, uint32_t* status) {
-  const size_t panel = (size_t)(h8 >> 4);             // 16 groups of 8 features per 128-feature panel
-  const int f8 = (h8 & 15) * 8;
+                                             const uint8_t* __restrict__ dead, uint32_t* status) {
   float acc[8];
 #pragma unroll
   for (int q = 0; q < 8; ++q) acc[q] = 0.f;
@@ -36,7 +32,7 @@ __device__ __forceinline__ void combine_unit(const float* __restrict__ y, int y_
     for (int j = 0; j < k; ++j) {
       const int r = __ldg(row_of_slot + (size_t)t * k + j);
       const float w = __ldg(topk_w + (size_t)t * k + j);
-      const float4* yp = reinterpret_cast<const float4*>(y + (panel * y_rows + r) * 128 + f8);
+      const float4* yp = reinterpret_cast<const float4*>(y + (size_t)r * H) + 2 * h8;
       const float4 a = kL2Only ? __ldcg(yp) : __ldg(yp);
       const float4 b = kL2Only ? __ldcg(yp + 1) : __ldg(yp + 1);
       const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -47,7 +43,7 @@ __device__ __forceinline__ void combine_unit(const float* __restrict__ y, int y_
       }
     }
     if (y_shared) {
-      const float4* yp = reinterpret_cast<const float4*>(y_shared + (panel * shared_rows + t) * 128 + f8);
+      const float4* yp = reinterpret_cast<const float4*>(y_shared + (size_t)t * H) + 2 * h8;
       const float4 a = __ldg(yp), b = __ldg(yp + 1);
       const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll

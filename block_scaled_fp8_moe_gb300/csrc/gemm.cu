@@ -562,8 +562,8 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
         __syncwarp();
         if (go)
           for (long long u = gt; u < units; u += gstride)
-            combine_unit<true>(p2.y, p2.y_rows, p2.topk_w, p2.row_of_slot, (int)(u / (p2.H / 8)),
-                               (int)(u % (p2.H / 8)), p2.H, p2.k, p2.out, nullptr, 0, nullptr, nullptr);
+            combine_unit<true>(p2.y, p2.topk_w, p2.row_of_slot, (int)(u / (p2.H / 8)), (int)(u % (p2.H / 8)),
+                               p2.H, p2.k, p2.out, nullptr, nullptr, nullptr);
       }
     }
   }
@@ -725,7 +725,6 @@ static GemmParams w2_params(const moe_shape* s, const uint8_t* hq, const uint8_t
   gp.I = s->I;
   gp.H = s->H;
   gp.y = y;
-  gp.y_rows = s->T * s->k;
   gp.status = status;
   return gp;
 }

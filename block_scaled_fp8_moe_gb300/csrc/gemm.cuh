@@ -35,10 +35,8 @@ struct GemmParams {
   uint8_t* hs;
   int hs_pitch;
   float* dbg;
-  // W2 output: per-slot rows in plan order, before the routing weight, panel-major:
-  // y[((f / 128) * y_rows + row) * 128 + f % 128] for plan row `row` and hidden feature f
+  // W2 output: per-slot rows in plan order, before the routing weight
   float* y;
-  int y_rows;
   uint32_t* status;
   // W13 then W2 in one launch: W13 epilogue warps count finished tiles per expert in ready[0..E)
   // (after their stores), and a W2 tile gathers its expert's rows only once every W13 tile of that
@@ -167,16 +165,15 @@ __device__ __forceinline__ void epi_w13_chunk(const uint32_t (&r)[16], float* xc
 }
 
 // W2: one 16-column chunk of a 128-row accumulator of output panel m, held by warp q (TMEM lanes
-// 32q..32q+31): plan row row0 + c0 + c of the per-slot buffer gets features 128 m + 32 q + lane.
-// The buffer is panel-major, so a tile's rows of one panel form one contiguous block (512 bytes per
-// row) and each store instruction writes 128 contiguous bytes of it (the routing weight is applied
-// by the combine).
+// 32q..32q+31): plan row row0 + c0 + c of the per-slot buffer gets features 128 m + 32 q + lane;
+// each store instruction writes 128 contiguous bytes (the routing weight is applied by the combine).
 __device__ __forceinline__ void epi_w2_chunk(const uint32_t (&r)[16], int q, int lane, int c0, int m, int row0,
                                              int nrows, const GemmParams& p) {
-  float* yrow = p.y + ((size_t)m * p.y_rows + row0 + c0) * 128 + 32 * q + lane;
+  const int feat = 128 * m + 32 * q + lane;
+  float* yrow = p.y + (size_t)(row0 + c0) * p.H + feat;
 #pragma unroll
   for (int c = 0; c < 16; ++c)
-    if (c0 + c < nrows) yrow[(size_t)c * 128] = __uint_as_float(r[c]);
+    if (c0 + c < nrows) yrow[(size_t)c * p.H] = __uint_as_float(r[c]);
 }
 
 // ---------------------------------------------------------------------------------------------

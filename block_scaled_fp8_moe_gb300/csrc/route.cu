@@ -819,10 +819,8 @@ __global__ void combine_kernel(const float* __restrict__ y, const float* __restr
   pdl_wait();
   const int H8 = H / 8;
   const long long n = (long long)T * H8;
-  // y has T*k rows (plan rows), y_shared one row per token
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
-    combine_unit<false>(y, T * k, topk_w, row_of_slot, (int)(i / H8), (int)(i % H8), H, k, out, y_shared, T, dead,
-                        status);
+    combine_unit<false>(y, topk_w, row_of_slot, (int)(i / H8), (int)(i % H8), H, k, out, y_shared, dead, status);
 }
 
 int launch_combine(const moe_shape* s, const float* y, const float* topk_w, const int32_t* row_of_slot,

@@ -206,12 +206,10 @@ MOE_API int moe_w2_combine_grouped(const moe_shape* shape, const uint8_t* hq, co
                            uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
 /* The down-projection GEMM alone (the first half of moe_w2_combine_grouped), into a per-slot buffer
- * the caller owns, in plan order and before the routing weight: y fp32, T*k*H values, 16-byte
- * aligned, panel-major: feature f of plan row p at y[((f / 128) * (T*k) + p) * 128 + f % 128],
- * i.e. y[H/128][T*k][128] (each 128-feature panel of the rows is contiguous, so a tile's results
- * leave as one block). Row p (p < live slots) = W2[e] h^[p], e the expert of plan row p; rows past
- * the live slots are not written. ws: a workspace of at least 256 bytes (its first 4 bytes are the
- * status word; moe_workspace_bytes is not needed). */
+ * the caller owns, in plan order and before the routing weight: y fp32 [T*k, H], 16-byte aligned;
+ * row p (p < live slots) = W2[e] h^[p], e the expert of plan row p; rows past the live slots are
+ * not written. ws: a workspace of at least 256 bytes (its first 4 bytes are the status word;
+ * moe_workspace_bytes is not needed). */
 MOE_API int moe_w2_grouped(const moe_shape* shape, const uint8_t* hq, const uint8_t* hs, const uint8_t* w2,
                            const uint8_t* w2_s, const int32_t* expert_offsets, const int32_t* slot_of_row,
                            float* y, void* ws, size_t ws_bytes, void* stream);
@@ -219,15 +217,15 @@ MOE_API int moe_w2_grouped(const moe_shape* shape, const uint8_t* hq, const uint
 /* The fixed-order combine alone (TP4 profile README, "Experts" row): with r_j = row_of_slot[t*k+j]
  * and y_j = topk_w[t, j] * y[r_j] (fp32, one rounding), out[t] = bf16_rne(((y_0 + y_1) + ...) +
  * y_{k-1}) in fp32, slots in rank order, for each row t with row_of_slot[t*k] >= 0 and (dead ==
- * NULL or dead[t] == 0); every other row gets +0.0. y fp32 [H/128][T*k][128] as moe_w2_grouped
- * writes it (16-byte aligned), topk_w f32 [T, k] and row_of_slot i32 [T*k] as the router writes them, dead
+ * NULL or dead[t] == 0); every other row gets +0.0. y fp32 [T*k, H] as moe_w2_grouped writes it
+ * (16-byte aligned), topk_w f32 [T, k] and row_of_slot i32 [T*k] as the router writes them, dead
  * u8 [T] or NULL, out bf16 [T, H]. A dead row that holds slots is recorded as for
  * moe_w2_combine_grouped. ws: at least 256 bytes, as for moe_w2_grouped. */
 MOE_API int moe_combine(const moe_shape* shape, const float* y, const float* topk_w, const int32_t* row_of_slot,
                         const uint8_t* dead, uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
 /* Both expert GEMMs on a plan: moe_w13_swiglu_grouped (hq / hs, and swiglu_debug when flags ask for
- * it) followed by moe_w2_grouped (y: plan order, panel-major, before the routing weight), with the same
+ * it) followed by moe_w2_grouped (y, plan order, before the routing weight), with the same
  * arguments and results as those two calls. For decode-sized batches (at most 32 plan rows per
  * expert on average) they run as ONE persistent launch: each CTA streams its down-projection weight
  * tiles as soon as it has finished its gate/up tiles, and gathers an expert's h rows once every

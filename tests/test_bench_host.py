@@ -46,14 +46,3 @@ def test_launch_counts_of_the_benchmarked_workloads():
     assert counts == {"decode-6": 3, "decode-48": 3, "prefill-4k": 11, "prefill-32k": 11}
     # with a shared expert the combine is its own launch after the side stream joins
     assert bench.launches_per_step(synth.CONFIGS["decode-6"], shared=True) == 7
-
-
-def test_profiled_kernel_names_map_to_their_gemm():
-    k = bench.gemm_kind
-    assert k("void moe::grouped_gemm_kernel<16, 2>(CUtensorMap_st, CUtensorMap_st, CUtensorMap_st, "
-             "moe::GemmParams, moe::GemmParams)") == "experts"
-    assert k("void moe::grouped_gemm_kernel<224, 1>(CUtensorMap_st, ...)") == "w13"
-    assert k("void moe::grouped_gemm_kernel<32, 0>(CUtensorMap_st, ...)") == "w2"
-    assert k("void moe::grouped_gemm_pair_kernel<0, moe::PairCfg<192, 3, 2>>(...)") == "w2"
-    assert k("moe::grouped_gemm_ws_kernel(CUtensorMap_st, CUtensorMap_st, moe::GemmParams)") == "w2"
-    assert k("moe::router_decode_kernel") is None

@@ -14,7 +14,7 @@ def _both(B, shp, xq, xs, layer, plan, ws):
     S = int(plan.expert_offsets[-1].item())
     hq, hs = B.moe_w13_swiglu_grouped(shp, xq, xs, layer.w13p, layer.w13sp, plan, ws)
     y = B.moe_w2_grouped(shp, hq, hs, layer.w2p, layer.w2sp, plan, ws)
-    return hq[:S].clone(), hs[:S].clone(), B.y_rows_view(y, shp)[:S], S
+    return hq[:S].clone(), hs[:S].clone(), y[:S].clone(), S
 
 
 @pytest.mark.parametrize("name,T,Hd,E,k,I,dead_frac", [
@@ -36,7 +36,7 @@ def test_experts_grouped_equals_two_gemms(name, T, Hd, E, k, I, dead_frac):
                                              plan, ws)
         B.moe_check_device_status(ws)
         assert torch.equal(hq2[:S], hq) and torch.equal(hs2[:S, : I // 32], hs[:, : I // 32])
-        assert torch.equal(B.y_rows_view(y2, shp)[:S], y)
+        assert torch.equal(y2[:S], y)
 
 
 def test_experts_grouped_at_decode6():
@@ -53,11 +53,8 @@ def test_experts_grouped_at_decode6():
     for _ in range(3):
         hq2, hs2, y2 = B.moe_experts_grouped(shp, xq, xs, layer.w13p, layer.w13sp, layer.w2p, layer.w2sp, plan, ws)
         B.moe_check_device_status(ws)
-        assert torch.equal(hq2[:S], hq) and torch.equal(hs2[:S], hs) and torch.equal(B.y_rows_view(y2, shp)[:S], y)
-    # and the whole layer (the forward runs the same GEMMs and the combine in one launch) against
-    # the step entry points
+        assert torch.equal(hq2[:S], hq) and torch.equal(hs2[:S], hs) and torch.equal(y2[:S], y)
+    # and the whole layer (the forward runs the same GEMMs) against the step entry points
     out = layer.forward(inp.x)
-    y_full = B.moe_w2_grouped(shp, *B.moe_w13_swiglu_grouped(shp, xq, xs, layer.w13p, layer.w13sp, plan, ws),
-                              layer.w2p, layer.w2sp, plan, ws)
-    ref = B.moe_combine(shp, y_full, plan, ws)
+    ref = B.moe_combine(shp, y, plan, ws)
     assert torch.equal(out, ref)

@@ -29,6 +29,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -110,20 +111,37 @@ def gemm_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def gemm_kind(name: str):
+    """Which step a grouped-GEMM launch is, from its demangled name: the MODE template argument of
+    grouped_gemm_kernel (0 down, 1 gate/up, 2 both in one launch), the weight-stationary and the
+    CTA-pair kernels; None for every other kernel."""
+    if name.startswith("grouped_gemm_ws_kernel"):
+        return "w2"
+    m = re.search(r"grouped_gemm_pair_kernel<(true|false)", name)
+    if m:
+        return "w13" if m.group(1) == "true" else "w2"
+    m = re.search(r"grouped_gemm_kernel<\d+, (\d)>", name)
+    if m:
+        return {"0": "w2", "1": "w13", "2": "experts"}[m.group(1)]
+    return None
+
+
 def record_traffic(raw_csv: str, workload: str) -> dict:
     """Average dram__bytes_read.sum + dram__bytes_write.sum per launch of each grouped GEMM."""
     import csv
-    rows = list(csv.reader(open(raw_csv)))
+    # ncu writes its own log lines ahead of the table: the table starts at the "ID" header
+    lines = open(raw_csv).read().splitlines()
+    start = next(i for i, ln in enumerate(lines) if ln.startswith('"ID"'))
+    rows = list(csv.reader(lines[start:]))
     hdr = rows[0]
     unit = dict(zip(hdr, rows[1]))
     scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
     acc: dict = {}
     for r in rows[2:]:
         d = dict(zip(hdr, r))
-        name = d.get("Kernel Name", "")
-        if "grouped_gemm_kernel" not in name:
+        key = gemm_kind(d.get("Kernel Name", ""))
+        if key is None:
             continue
-        key = "w13" if name.rstrip().endswith("1>(CUtensorMap_st, CUtensorMap_st, GemmParams)") else "w2"
         b = sum(float(d[m]) * scale[unit[m]] for m in ("dram__bytes_read.sum", "dram__bytes_write.sum"))
         acc.setdefault(key, []).append(b)
     entry = {k: sum(v) / len(v) for k, v in acc.items()}

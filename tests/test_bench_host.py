@@ -46,3 +46,16 @@ def test_launch_counts_of_the_benchmarked_workloads():
     assert counts == {"decode-6": 3, "decode-48": 3, "prefill-4k": 11, "prefill-32k": 11}
     # with a shared expert the combine is its own launch after the side stream joins
     assert bench.launches_per_step(synth.CONFIGS["decode-6"], shared=True) == 7
+
+
+def test_gemm_kind_classifies_every_grouped_gemm_launch_name():
+    """The traffic recorder files each ncu launch under the step it belongs to."""
+    ck = "(CUtensorMap_st, CUtensorMap_st, CUtensorMap_st, GemmParams, GemmParams)"
+    assert bench.gemm_kind("void grouped_gemm_kernel<16, 2>" + ck) == "experts"
+    assert bench.gemm_kind("void grouped_gemm_kernel<224, 1>" + ck) == "w13"
+    assert bench.gemm_kind("void grouped_gemm_kernel<64, 0>" + ck) == "w2"
+    assert bench.gemm_kind("grouped_gemm_ws_kernel(CUtensorMap_st, CUtensorMap_st, GemmParams)") == "w2"
+    assert bench.gemm_kind("void grouped_gemm_pair_kernel<true, PairCfg<192, 3, 2>>(...)") == "w13"
+    assert bench.gemm_kind("void grouped_gemm_pair_kernel<false, PairCfg<192, 3, 2>>(...)") == "w2"
+    assert bench.gemm_kind("void combine_kernel(const float *, ...)") is None
+    assert bench.gemm_kind("void quant_mxfp8_plan_kernel(...)") is None

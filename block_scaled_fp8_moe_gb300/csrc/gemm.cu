@@ -16,8 +16,8 @@
 //               and its 512-byte scale block (bulk copy); one mbarrier transaction per stage.
 //   warps 1, 3  token-operand producers: cp.async gathers of the BN activation rows (128 B each,
 //               128B-swizzled in shared memory) and their scale bytes for narrow tiles; for wide
-//               tiles warp 1 loads one TMA box of plan-order rows per K-chunk. Both arrive on the
-//               same stage mbarrier.
+//               tiles warp 1 loads one TMA box of plan-order rows per K-chunk and writes the scale
+//               atoms with 16-byte shared stores. Both arrive on the same stage mbarrier.
 //   warp 2      TMEM owner and MMA issuer: tcgen05.cp of the scale blocks to TMEM, four K=32
 //               MMAs per K-chunk, tcgen05.commit releases the stage only after the MMAs (and
 //               copies) that read it are complete.
@@ -323,42 +323,68 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
     // The token operand of a wide tile is always in plan order (W2: hq; W13: a copy of xq gathered
     // into plan order before the GEMM), so lane 0 loads the tile's contiguous plan rows with one
     // 2D TMA box; rows past the tile's end belong to the next expert (or are TMA zero fill) and
-    // their columns are never stored. Every lane also copies the scale bytes of rows lane + 32 i.
+    // their columns are never stored. The lanes also write the stage's scale atoms with 16-byte
+    // shared stores, make them visible to the MMA's async proxy and arrive on the stage barrier.
+    // Stages stream in order (items w, K-chunk groups kc0); a stage's scale words are loaded one
+    // stage ahead, before the previous stage's are stored, so their latency overlaps a whole stage.
+    constexpr int NA = (BN + 127) / 128;
+    int w = blockIdx.x, kn = 0;
+    int e = 0, m = 0, nt = 0, row0 = 0, nrows = 0, tw = 0;
+    bool first = true;
+    if (w < total) decode(w, first, e, m, nt, row0, nrows, tw);
+    auto next_stage = [&](int& r0, int& nr, int& kc0) {        // the stage at the cursor, then advance
+      if (w >= total) return false;
+      r0 = row0;
+      nr = nrows;
+      kc0 = kn;
+      kn += L::KT;
+      if (kn >= p.KC) {
+        kn = 0;
+        w += gridDim.x;
+        if (w < total) decode(w, first, e, m, nt, row0, nrows, tw);
+      }
+      return true;
+    };
+    auto load_stage = [&](ScaleLines<NA>(&sl)[L::KT], int r0, int nr, int kc0) {
+#pragma unroll
+      for (int j = 0; j < L::KT; ++j)
+        if (kc0 + j < p.KC) load_scale_lines<NA>(sl[j], p.bs, p.b_scale_pitch, r0, nr, kc0 + j, lane);
+    };
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total; w += gridDim.x) {
-      int e, m, nt, row0, nrows, tw;
-      bool first;
-      decode(w, first, e, m, nt, row0, nrows, tw);
-      for (int kc0 = 0; kc0 < p.KC; kc0 += L::KT) {
-        if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
-        if (ok) {
-          const int nv = min(L::KT, p.KC - kc0);
-          uint8_t* sB0 = tiles + stage * L::kStageBytes + L::kStageA;
-          uint8_t* sSFB0 = sB0 + L::kStageB + L::KT * 512;
-          // every stage moves KT boxes of BN rows (the transaction count the weight producer
-          // announced); rows past the tile and boxes past the end of K are never multiplied
-          if (lane == 0)
-            for (int j = 0; j < L::KT; ++j)
-              tma_load_2d(sB0 + j * L::kTileB, &tmap_b, (kc0 + j) * 128, row0, &full[stage]);
-          for (int j = 0; j < nv; ++j) {
-            const int kc = kc0 + j;
+    int r0 = 0, nr = 0, kc0 = 0;
+    bool have = next_stage(r0, nr, kc0);
+    ScaleLines<NA> sl[L::KT];
+    if (have) load_stage(sl, r0, nr, kc0);
+    while (have) {
+      int r1 = 0, nr1 = 0, kc1 = 0;
+      const bool have1 = next_stage(r1, nr1, kc1);
+      ScaleLines<NA> sl1[L::KT];
+      if (have1) load_stage(sl1, r1, nr1, kc1);
+      if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
+      if (ok) {
+        uint8_t* sB0 = tiles + stage * L::kStageBytes + L::kStageA;
+        uint8_t* sSFB0 = sB0 + L::kStageB + L::KT * 512;
+        // every stage moves KT boxes of BN rows (the transaction count the weight producer
+        // announced); rows past the tile and boxes past the end of K are never multiplied
+        if (lane == 0)
+          for (int j = 0; j < L::KT; ++j)
+            tma_load_2d(sB0 + j * L::kTileB, &tmap_b, (kc0 + j) * 128, r0, &full[stage]);
 #pragma unroll
-            for (int i = 0; i < (BN + 31) / 32; ++i) {
-              const int c = lane + 32 * i;
-              const bool valid = c < nrows;
-              const uint8_t* src = valid ? p.bs + (size_t)(row0 + c) * p.b_scale_pitch + kc * 4 : p.bs;
-              cp_async_4(sSFB0 + j * L::kSfbChunk + (c >> 7) * 512 + (c & 31) * 16 + ((c >> 5) & 3) * 4, src,
-                         valid ? 4u : 0u);
-            }
-          }
-          cp_async_arrive_noinc(&full[stage]);
-        }
-        if (++stage == S) { stage = 0; phase ^= 1; }
+        for (int j = 0; j < L::KT; ++j)
+          if (kc0 + j < p.KC) store_scale_lines<NA>(sl[j], sSFB0 + j * L::kSfbChunk, lane);
+        fence_async_smem();
+        mbar_arrive(&full[stage]);
       }
+      if (++stage == S) { stage = 0; phase ^= 1; }
+      have = have1;
+      r0 = r1;
+      nr = nr1;
+      kc0 = kc1;
+#pragma unroll
+      for (int j = 0; j < L::KT; ++j) sl[j] = sl1[j];
     }
-    cp_async_wait_all();
   } else if (!kTmaB && (warp == 1 || warp == 3)) {
     // ===================== gather producers: activations =====================
     // After an expired wait the loops keep running (doing nothing) so that both warps meet at

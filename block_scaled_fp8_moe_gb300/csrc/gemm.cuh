@@ -60,6 +60,38 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// The token operand's scale bytes of one 128-deep K-chunk, in the MMA's scale layout: per 128 tile
+// rows one 512-byte atom whose 16-byte line j holds the 4 bytes (the chunk's four 32-blocks) of
+// rows j, j + 32, j + 64 and j + 96. Lane j of the producer warp loads the words of its NA lines
+// with plain loads (a row past nrows reads as zero, scale 2^-127, and is never stored by the
+// epilogue) and later stores each line with one 16-byte shared store: 4 conflict-free wavefronts
+// per atom, where 4-byte cp.async copies into the same layout cost one wavefront per lane.
+template <int NA>
+struct ScaleLines {
+  uint32_t w[NA][4];
+};
+
+template <int NA>
+__device__ __forceinline__ void load_scale_lines(ScaleLines<NA>& s, const uint8_t* bs, size_t pitch, int row0,
+                                                 int nrows, int kc, int lane) {
+#pragma unroll
+  for (int a = 0; a < NA; ++a)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = 128 * a + 32 * q + lane;
+      s.w[a][q] = c < nrows ? *reinterpret_cast<const uint32_t*>(bs + (size_t)(row0 + c) * pitch + kc * 4) : 0u;
+    }
+}
+
+template <int NA>
+__device__ __forceinline__ void store_scale_lines(const ScaleLines<NA>& s, uint8_t* atoms, int lane) {
+#pragma unroll
+  for (int a = 0; a < NA; ++a)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(atoms + a * 512 + lane * 16)),
+                 "r"(s.w[a][0]), "r"(s.w[a][1]), "r"(s.w[a][2]), "r"(s.w[a][3])
+                 : "memory");
+}
+
 __device__ __forceinline__ int find_expert(const int* cum, int E, int w) {
   // largest e with cum[e] <= w (cum non-decreasing, cum[E] > w)
   int lo = 0, hi = E;           // invariant: cum[lo] <= w < cum[hi]

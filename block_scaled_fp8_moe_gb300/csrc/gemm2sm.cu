@@ -207,36 +207,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, Pair
   } else if (warp == 1) {
     // ===================== TMA producer: this CTA's half of the token rows =====================
     // lane 0 loads one box of BN/2 plan rows starting at the CTA's half of the tile (rows past the
-    // tile belong to the next tile or expert, or are TMA zero fill, and are never stored); every
-    // lane copies the scale bytes of columns lane + 32 i of the WHOLE tile, which each SM's MMA reads
-    // from its own Tensor Memory.
+    // tile belong to the next tile or expert, or are TMA zero fill, and are never stored); the lanes
+    // write the scale atoms of the WHOLE tile, which each SM's MMA reads from its own Tensor
+    // Memory, with 16-byte shared stores. The chunks stream in order (items w, K-chunks kc); a
+    // chunk's scale words are loaded one chunk ahead, before the previous chunk's are stored.
+    constexpr int NA = Pair::kSfbAtoms;
+    const uint32_t leader_full = mapa_shared(&full[0], 0);
+    int w = pair, kn = 0;
+    int e = 0, mp = 0, row0 = 0, nrows = 0, tw = 0;
+    if (w < total) decode(w, e, mp, row0, nrows, tw);
+    auto next_chunk = [&](int& r0, int& nr, int& tw0, int& kc) {   // the chunk at the cursor, then advance
+      if (w >= total) return false;
+      r0 = row0;
+      nr = nrows;
+      tw0 = tw;
+      kc = kn;
+      if (++kn == p.KC) {
+        kn = 0;
+        w += npairs;
+        if (w < total) decode(w, e, mp, row0, nrows, tw);
+      }
+      return true;
+    };
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    const uint32_t leader_full = mapa_shared(&full[0], 0);
-    for (int w = pair; w < total; w += npairs) {
-      int e, mp, row0, nrows, tw;
-      decode(w, e, mp, row0, nrows, tw);
-      const int brow = row0 + (int)rank * (tw >> 1);
-      for (int kc = 0; kc < p.KC; ++kc) {
-        if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
-        if (ok) {
-          uint8_t* sB = tiles + stage * Pair::kStageBytes + Pair::kTileA;
-          uint8_t* sSFB = sB + Pair::kTileB + 512;
-          if (lane == 0) tma_load_2d_pair(sB, &tmap_b, kc * 128, brow, leader_full + (uint32_t)(stage * 8));
-#pragma unroll
-          for (int i = 0; i < (Pair::BN + 31) / 32; ++i) {
-            const int c = lane + 32 * i;
-            const bool valid = c < nrows;
-            const uint8_t* src = valid ? p.bs + (size_t)(row0 + c) * p.b_scale_pitch + kc * 4 : p.bs;
-            cp_async_4(sSFB + (c >> 7) * 512 + (c & 31) * 16 + ((c >> 5) & 3) * 4, src, valid ? 4u : 0u);
-          }
-          cp_async_arrive_noinc(&full[stage]);
-        }
-        if (++stage == S) { stage = 0; phase ^= 1; }
+    int r0 = 0, nr = 0, tw0 = 0, kc = 0;
+    bool have = next_chunk(r0, nr, tw0, kc);
+    ScaleLines<NA> sl;
+    if (have) load_scale_lines(sl, p.bs, p.b_scale_pitch, r0, nr, kc, lane);
+    while (have) {
+      int r1 = 0, nr1 = 0, tw1 = 0, kc1 = 0;
+      const bool have1 = next_chunk(r1, nr1, tw1, kc1);
+      ScaleLines<NA> sl1;
+      if (have1) load_scale_lines(sl1, p.bs, p.b_scale_pitch, r1, nr1, kc1, lane);
+      if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
+      if (ok) {
+        uint8_t* sB = tiles + stage * Pair::kStageBytes + Pair::kTileA;
+        uint8_t* sSFB = sB + Pair::kTileB + 512;
+        const int brow = r0 + (int)rank * (tw0 >> 1);
+        if (lane == 0) tma_load_2d_pair(sB, &tmap_b, kc * 128, brow, leader_full + (uint32_t)(stage * 8));
+        store_scale_lines(sl, sSFB, lane);
+        fence_async_smem();
+        mbar_arrive(&full[stage]);
       }
+      if (++stage == S) { stage = 0; phase ^= 1; }
+      have = have1;
+      r0 = r1;
+      nr = nr1;
+      tw0 = tw1;
+      kc = kc1;
+      sl = sl1;
     }
-    cp_async_wait_all();
   } else if (warp == 2) {
     if (lane == 0 && rank == 0) {
       // ===================== the pair's MMA issuer (even CTA) =====================

@@ -16,8 +16,8 @@
 // Roles (384 threads):
 //   warp 0      TMA of the unit's weight panel (KC tiles) and its scale blocks into the resident
 //               region, once the previous unit's MMAs no longer read it
-//   warp 1      per (tile, K-chunk): one TMA box of plan rows (lane 0) and the scale bytes of the
-//               tile's columns (every lane, cp.async) into a ring of stages
+//   warp 1      per (tile, K-chunk): one TMA box of plan rows (lane 0) and the scale atoms of the
+//               tile's columns (every lane: plain loads, 16-byte shared stores) into a ring of stages
 //   warp 2      TMEM owner and MMA issuer: the unit's A scales into resident TMEM columns, then per
 //               K-chunk the stage's B scales and four K = 32 MMAs; commits release stages,
 //               accumulators and, after the unit's last MMA, the resident panel
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(Ws::kThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1 + 32);                       // lane 0's expect-tx arrival + 32 cp.async arrivals
+      mbar_init(&full[s], 1 + 32);                       // lane 0's expect-tx arrival + 32 scale-store arrivals
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -185,37 +185,64 @@ __global__ void __launch_bounds__(Ws::kThreads, 1)
     }
   } else if (warp == 1) {
     // ===================== token boxes and their scale bytes =====================
+    // The chunks stream in order (units u, their token tiles nt, K-chunks kc). A chunk's scale
+    // words are loaded one chunk ahead, before the previous chunk's are stored, so their latency
+    // overlaps a whole chunk instead of stalling the stores.
+    constexpr int NA = (Ws::BN + 127) / 128;
+    int u = blockIdx.x, nt = 0, kn = 0;
+    Unit d{};
+    if (u < total) {
+      d = decode(u);
+      nt = d.nt0;
+    }
+    auto next_chunk = [&](int& row0, int& nrows, int& kc) {     // the chunk at the cursor, then advance
+      if (u >= total) return false;
+      row0 = s_off[d.e] + nt * d.tw;
+      nrows = min(d.tw, d.cnt - nt * d.tw);
+      kc = kn;
+      if (++kn == KC) {
+        kn = 0;
+        if (++nt == d.nt1) {
+          u += gridDim.x;
+          if (u < total) {
+            d = decode(u);
+            nt = d.nt0;
+          }
+        }
+      }
+      return true;
+    };
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const Unit d = decode(u);
-      for (int nt = d.nt0; nt < d.nt1; ++nt) {
-        const int row0 = s_off[d.e] + nt * d.tw;
-        const int nrows = min(d.tw, d.cnt - nt * d.tw);
-        for (int kc = 0; kc < KC; ++kc) {
-          if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
-          if (ok) {
-            uint8_t* sB = stages + stage * Ws::kStageBytes;
-            uint8_t* sSFB = sB + Ws::kTileB;
-            if (lane == 0) {
-              mbar_arrive_expect_tx(&full[stage], Ws::kTileB);
-              tma_load_2d(sB, &tmap_b, kc * 128, row0, &full[stage]);
-            }
-#pragma unroll
-            for (int i = 0; i < (Ws::BN + 31) / 32; ++i) {
-              const int c = lane + 32 * i;
-              const bool valid = c < nrows;
-              const uint8_t* src = valid ? p.bs + (size_t)(row0 + c) * p.b_scale_pitch + kc * 4 : p.bs;
-              cp_async_4(sSFB + (c >> 7) * 512 + (c & 31) * 16 + ((c >> 5) & 3) * 4, src, valid ? 4u : 0u);
-            }
-            cp_async_arrive_noinc(&full[stage]);
-          }
-          if (++stage == S) { stage = 0; phase ^= 1; }
+    int row0 = 0, nrows = 0, kc = 0;
+    bool have = next_chunk(row0, nrows, kc);
+    ScaleLines<NA> sl;
+    if (have) load_scale_lines(sl, p.bs, p.b_scale_pitch, row0, nrows, kc, lane);
+    while (have) {
+      int row1 = 0, nrows1 = 0, kc1 = 0;
+      const bool have1 = next_chunk(row1, nrows1, kc1);
+      ScaleLines<NA> sl1;
+      if (have1) load_scale_lines(sl1, p.bs, p.b_scale_pitch, row1, nrows1, kc1, lane);
+      if (ok) ok = warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
+      if (ok) {
+        uint8_t* sB = stages + stage * Ws::kStageBytes;
+        uint8_t* sSFB = sB + Ws::kTileB;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], Ws::kTileB);
+          tma_load_2d(sB, &tmap_b, kc * 128, row0, &full[stage]);
         }
+        store_scale_lines(sl, sSFB, lane);
+        fence_async_smem();
+        mbar_arrive(&full[stage]);
       }
+      if (++stage == S) { stage = 0; phase ^= 1; }
+      have = have1;
+      row0 = row1;
+      nrows = nrows1;
+      kc = kc1;
+      sl = sl1;
     }
-    cp_async_wait_all();
   } else if (warp == 2) {
     // ===================== MMA issuer =====================
     if (lane == 0) {

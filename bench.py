@@ -396,12 +396,29 @@ class ClockSampler:
 # ----------------------------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------------------------
+def decode_router_fits(T: int, H: int, E: int) -> bool:
+    """Whether moe_forward routes T rows with the decode router (mirrors decode_router_cfg in the
+    library: experts per CTA and per thread, rows per token block, threads and shared memory)."""
+    nc = H // 64
+    small = T <= 16
+    ept, epc = (1, 2) if small else (2, 8)
+    epc = min(epc, E)
+    tpc = T if small else 16
+    threads = -(-epc // ept) * nc
+
+    def smem(tp):
+        return tp * nc * 144 + epc * tp * (nc + 1) * 4
+
+    while tpc > 1 and smem(tpc) > 210 * 1024:
+        tpc -= 1
+    return T <= 64 and threads <= 512 and smem(tpc) <= 210 * 1024
+
+
 def launches_per_step(cfg, shared: bool = False) -> int:
     """Kernels one moe_forward launches for this shape (mirrors the library's dispatch); `shared`:
     with a shared expert (its identity plan and two GEMMs on the side stream)."""
     T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
-    nc = H // 64
-    decode_router = T <= 64 and 2 * nc <= 256 and (min(T, 16) * nc * 144 + 2 * T * nc * 4) <= 210 * 1024
+    decode_router = decode_router_fits(T, H, E)
     if decode_router:
         n = 1                                         # logits (+ fused MXFP8 quantisation)
     elif T > 16 and E <= 256 and H % 64 == 0 and H <= 4096:

@@ -74,125 +74,159 @@ __global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __res
 }
 
 // ---------------------------------------------------------------------------------------------
-// Logits, small T (decode), x staged in shared memory kDecGroup rows at a time by cp.async (all
-// of a group's 16-byte copies in flight at once; chunk pitch 144 B so a quarter-warp's 16-byte
-// reads of consecutive chunks hit distinct banks). A CTA owns kDecEpc experts; each thread item
-// (expert, chunk) loads its 128 bytes of Wr once (8 loads in flight) and, for every staged token,
-// runs the sequential fma chain of that chunk (bf16 operands, fp32 accumulate); the chunk
-// partials are then folded left to right per (expert, token). The same order as
-// router_small_kernel and the tiled kernel. Optionally each CTA also MXFP8-quantises a share of
-// the rows it has staged.
+// Logits, small T (decode). The grid is (expert blocks of epc experts) x (token blocks of up to tpc
+// rows). A CTA stages its token block's rows of x in shared memory by cp.async (every 16-byte copy
+// in flight at once; chunk pitch 144 B so a quarter-warp's 16-byte reads of consecutive chunks hit
+// distinct banks). Thread (g, c) owns chunk c of the EPT experts g EPT .. g EPT + EPT - 1 of the
+// block: it loads their 128-byte Wr chunks into registers once and, for every staged token, runs
+// the sequential fma chain of the chunk for each of them (bf16 operands, fp32 accumulate; two
+// tokens at a time, as independent chains). The chunk partials go to shared memory, then one
+// thread per (expert, token) folds them left to right and applies the sigmoid: the same order as
+// router_small_kernel and the tiled kernel. Optionally the CTAs of a token block also
+// MXFP8-quantise its rows, each a share of the 32-blocks.
 // ---------------------------------------------------------------------------------------------
-#ifndef MOE_DEC_EPC
-#define MOE_DEC_EPC 2
-#endif
-constexpr int kDecEpc = MOE_DEC_EPC;  // experts per CTA
-constexpr int kDecGroup = 16;       // token rows staged at a time
 constexpr int kDecMaxT = 64;
+constexpr int kDecThreadsMax = 512;
 constexpr size_t kDecodeSmemMax = 210 * 1024;
 constexpr int kDecPitch = 144;      // bytes per staged 64-element chunk
+constexpr int kDecSmallT = 16;      // up to this many rows: one token block, kDecEpcSmall experts per CTA
+constexpr int kDecEpcSmall = 2;
+constexpr int kDecEpcLarge = 8;     // more rows: blocks of kDecTpcLarge rows, kDecEpcLarge experts per CTA
+constexpr int kDecTpcLarge = 16;
 
-__host__ __device__ inline size_t router_decode_smem(int T, int H) {
+struct DecodeRouterCfg {
+  int ept, epc, tpc, threads;
+  size_t smem;
+};
+
+// Up to kDecSmallT rows: one token block and two experts per CTA (one per thread; the Wr stream is
+// spread over E / 2 CTAs). Beyond that: blocks of 16 rows and eight experts per CTA (two per
+// thread), so that each CTA stages few rows of x and serves many experts with them.
+inline DecodeRouterCfg decode_router_cfg(int T, int H, int E) {
   const int NC = H / kRouterChunk;
-  const int G = T < kDecGroup ? T : kDecGroup;
-  return (size_t)G * NC * kDecPitch + (size_t)kDecEpc * T * NC * 4;
+  DecodeRouterCfg c{};
+  const bool small = T <= kDecSmallT;
+  c.ept = small ? 1 : 2;
+  c.epc = small ? kDecEpcSmall : kDecEpcLarge;
+  if (c.epc > E) c.epc = E;
+  c.tpc = small ? T : kDecTpcLarge;
+  c.threads = ((c.epc + c.ept - 1) / c.ept) * NC;
+  auto smem = [&](int tpc) { return (size_t)tpc * NC * kDecPitch + (size_t)c.epc * tpc * (NC + 1) * 4; };
+  while (c.tpc > 1 && smem(c.tpc) > kDecodeSmemMax) --c.tpc;
+  c.smem = smem(c.tpc);
+  return c;
 }
 
-__global__ void __launch_bounds__(256) router_decode_kernel(const uint16_t* __restrict__ x,
-                                                            const uint16_t* __restrict__ wr,
-                                                            const float* __restrict__ bias, int T, int H, int E,
-                                                            float* __restrict__ score, float* __restrict__ key,
-                                                            uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
+template <int EPT>
+__global__ void __launch_bounds__(kDecThreadsMax) router_decode_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, const float* __restrict__ bias, int T, int H,
+    int E, int epc, int tpc, float* __restrict__ score, float* __restrict__ key, uint8_t* __restrict__ xq,
+    uint8_t* __restrict__ xs) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(16) uint8_t dsm_dec[];
   const int NC = H / kRouterChunk;
-  const int G = T < kDecGroup ? T : kDecGroup;
-  uint8_t* xsm = dsm_dec;                                                        // [G][NC] chunks
-  float* part = reinterpret_cast<float*>(dsm_dec + (size_t)G * NC * kDecPitch);  // [kDecEpc][T][NC]
-  const int e0 = blockIdx.x * kDecEpc;
-  // this thread's (expert, chunk) item and its Wr chunk, loaded once for every token group
-  const int items = kDecEpc * NC;
-  const int it0 = threadIdx.x;
-  const bool has_item = it0 < items && e0 + it0 / NC < E;     // kDecEpc * NC <= blockDim.x
-  uint4 wv[8];
-  if (has_item) {
-    const uint4* wp =
-        reinterpret_cast<const uint4*>(wr + (size_t)(e0 + it0 / NC) * H + (size_t)(it0 % NC) * kRouterChunk);
+  const int t0 = blockIdx.y * tpc;
+  const int tn = min(tpc, T - t0);
+  const int e0 = blockIdx.x * epc;
+  uint8_t* xsm = dsm_dec;                                                          // [tn][NC] chunks
+  float* part = reinterpret_cast<float*>(dsm_dec + (size_t)tpc * NC * kDecPitch);  // [epc][tpc][NC + 1]
+  const int c = threadIdx.x % NC;
+  const int g = threadIdx.x / NC;
+  // this thread's experts and their Wr chunks, loaded once (all loads in flight together)
+  uint4 wv[EPT][8];
+  bool has[EPT];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) wv[i] = __ldg(wp + i);
+  for (int j = 0; j < EPT; ++j) {
+    const int el = g * EPT + j;
+    has[j] = el < epc && e0 + el < E;
+    const uint4* wp = reinterpret_cast<const uint4*>(wr + (size_t)(has[j] ? e0 + el : 0) * H + (size_t)c * kRouterChunk);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wv[j][i] = has[j] ? __ldg(wp + i) : make_uint4(0, 0, 0, 0);
   }
-  for (int g0 = 0; g0 < T; g0 += G) {
-    const int gn = min(G, T - g0);
-    if (g0 > 0) __syncthreads();                  // previous group's rows no longer read
-    // stage rows g0 .. g0 + gn: 16-byte unit u of chunk (t, c) from x[g0 + t, 64 c + 8 u]
-    for (int i = threadIdx.x; i < gn * NC * 8; i += blockDim.x) {
-      const int u = i & 7, tc = i >> 3;
-      const int t = tc / NC, c = tc - t * NC;
-      cp_async_16(xsm + (size_t)tc * kDecPitch + u * 16, x + (size_t)(g0 + t) * H + c * kRouterChunk + u * 8, 16);
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    if (has_item) {
-      const int el = it0 / NC, c = it0 % NC;
-      for (int t = 0; t < gn; ++t) {
-        const uint4* xp = reinterpret_cast<const uint4*>(xsm + ((size_t)t * NC + c) * kDecPitch);
-        float p = 0.f;
+  // stage the block's rows: 16-byte unit u of chunk (t, c) from x[t0 + t, 64 c + 8 u]
+  for (int i = threadIdx.x; i < tn * NC * 8; i += blockDim.x) {
+    const int u = i & 7, tc = i >> 3;
+    const int t = tc / NC, cc = tc - t * NC;
+    cp_async_16(xsm + (size_t)tc * kDecPitch + u * 16, x + (size_t)(t0 + t) * H + cc * kRouterChunk + u * 8, 16);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  // two tokens per pass: independent chains, each in element order from +0
+  for (int t = 0; t < tn; t += 2) {
+    const bool two = t + 1 < tn;
+    const uint4* xp0 = reinterpret_cast<const uint4*>(xsm + ((size_t)t * NC + c) * kDecPitch);
+    const uint4* xp1 = reinterpret_cast<const uint4*>(xsm + ((size_t)(two ? t + 1 : t) * NC + c) * kDecPitch);
+    float p0[EPT], p1[EPT];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 xv = xp[i];
-          p = fma2_bf16(xv.x, wv[i].x, p);
-          p = fma2_bf16(xv.y, wv[i].y, p);
-          p = fma2_bf16(xv.z, wv[i].z, p);
-          p = fma2_bf16(xv.w, wv[i].w, p);
-        }
-        part[((size_t)el * T + g0 + t) * NC + c] = p;
+    for (int j = 0; j < EPT; ++j) p0[j] = p1[j] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 a = xp0[i];
+      const uint4 b = xp1[i];
+#pragma unroll
+      for (int j = 0; j < EPT; ++j) {
+        p0[j] = fma2_bf16(a.x, wv[j][i].x, p0[j]);
+        p1[j] = fma2_bf16(b.x, wv[j][i].x, p1[j]);
+        p0[j] = fma2_bf16(a.y, wv[j][i].y, p0[j]);
+        p1[j] = fma2_bf16(b.y, wv[j][i].y, p1[j]);
+        p0[j] = fma2_bf16(a.z, wv[j][i].z, p0[j]);
+        p1[j] = fma2_bf16(b.z, wv[j][i].z, p1[j]);
+        p0[j] = fma2_bf16(a.w, wv[j][i].w, p0[j]);
+        p1[j] = fma2_bf16(b.w, wv[j][i].w, p1[j]);
       }
     }
-    // MXFP8 quantisation of a share of the staged rows (one 32-block per thread item)
-    if (xq) {
-      const int nblk = gn * H / 32;
-      for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += gridDim.x * blockDim.x) {
-        const int t = b / (H / 32), h = (b % (H / 32)) * 32;
-        const uint4* src = reinterpret_cast<const uint4*>(xsm + ((size_t)t * NC + h / kRouterChunk) * kDecPitch +
-                                                          (h % kRouterChunk) * 2);
-        float f[32];
-        float m = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 v = src[i];
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    for (int j = 0; j < EPT; ++j) {
+      if (!has[j]) continue;
+      float* pp = part + ((size_t)(g * EPT + j) * tpc + t) * (NC + 1) + c;
+      pp[0] = p0[j];
+      if (two) pp[NC + 1] = p1[j];
+    }
+  }
+  // MXFP8 quantisation of this token block's rows: the CTAs of the block take the 32-blocks in turn
+  if (xq) {
+    const int nblk = tn * H / 32;
+    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += gridDim.x * blockDim.x) {
+      const int t = b / (H / 32), h = (b % (H / 32)) * 32;
+      const uint4* src = reinterpret_cast<const uint4*>(xsm + ((size_t)t * NC + h / kRouterChunk) * kDecPitch +
+                                                        (h % kRouterChunk) * 2);
+      float f[32];
+      float m = 0.f;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            f[8 * i + 2 * q] = bf_lo(w4[q]);
-            f[8 * i + 2 * q + 1] = bf_hi(w4[q]);
-            m = fmaxf(m, fmaxf(fabsf(f[8 * i + 2 * q]), fabsf(f[8 * i + 2 * q + 1])));
-          }
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = src[i];
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          f[8 * i + 2 * q] = bf_lo(w4[q]);
+          f[8 * i + 2 * q + 1] = bf_hi(w4[q]);
+          m = fmaxf(m, fmaxf(fabsf(f[8 * i + 2 * q]), fabsf(f[8 * i + 2 * q + 1])));
         }
-        const int se = e4m3_scale_exp(m);
-        const float sc = pow2_neg(se);
-        uint32_t o[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          o[i] = e4m3x2(f[4 * i] * sc, f[4 * i + 1] * sc) | (e4m3x2(f[4 * i + 2] * sc, f[4 * i + 3] * sc) << 16);
-        uint4* dq = reinterpret_cast<uint4*>(xq + (size_t)(g0 + t) * H + h);
-        dq[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dq[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        xs[(size_t)(g0 + t) * (H / 32) + h / 32] = (uint8_t)(se + 127);
       }
+      const int se = e4m3_scale_exp(m);
+      const float sc = pow2_neg(se);
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        o[i] = e4m3x2(f[4 * i] * sc, f[4 * i + 1] * sc) | (e4m3x2(f[4 * i + 2] * sc, f[4 * i + 3] * sc) << 16);
+      uint4* dq = reinterpret_cast<uint4*>(xq + (size_t)(t0 + t) * H + h);
+      dq[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dq[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      xs[(size_t)(t0 + t) * (H / 32) + h / 32] = (uint8_t)(se + 127);
     }
   }
   __syncthreads();
-  for (int it = threadIdx.x; it < kDecEpc * T; it += blockDim.x) {
-    const int el = it / T, t = it % T;
+  for (int it = threadIdx.x; it < epc * tn; it += blockDim.x) {
+    const int el = it / tn, t = it - el * tn;
     const int e = e0 + el;
     if (e >= E) continue;
-    const float* pp = part + ((size_t)el * T + t) * NC;
+    const float* pp = part + ((size_t)el * tpc + t) * (NC + 1);
     float acc = 0.f;
-    for (int c = 0; c < NC; ++c) acc = __fadd_rn(acc, pp[c]);
+    for (int cc = 0; cc < NC; ++cc) acc = __fadd_rn(acc, pp[cc]);
     const float sc = sigmoid_cw(acc);
-    score[(size_t)t * E + e] = sc;
-    key[(size_t)t * E + e] = __fadd_rn(sc, bias[e]);
+    score[(size_t)(t0 + t) * E + e] = sc;
+    key[(size_t)(t0 + t) * E + e] = __fadd_rn(sc, bias[e]);
   }
 }
 
@@ -370,53 +404,68 @@ __device__ __forceinline__ void anchored_weights(const float* __restrict__ srow,
   *w = __fdiv_rn(sc, sum);
 }
 
-// One token's top-k on one warp. Lane l holds experts l, l + 32, ... (NI of them) and its own
-// best untaken (key desc, expert asc); each round is a warp arg-max over the lanes' bests (two
-// warp reductions), after which only the winning lane rescans its NI values. Selected weights: sigma_j / sum, the sum
-// accumulated in rank order (identical on every lane). Lane j < k ends with the j-th choice.
+// One token's top-k on one warp. Lane l holds experts l, l + 32, ... (NI of them), sorted once in
+// registers by (key desc, expert asc); each round is a warp arg-max over the lanes' heads (two warp
+// reductions: the largest key, then the lowest expert holding it), after which the winning lane
+// drops its head (a predicated shift, no divergent rescan). Selected weights: sigma_j / sum, the
+// sum accumulated in rank order (identical on every lane). Lane j < k ends with the j-th choice.
 template <int NI>
 __device__ __forceinline__ void warp_topk(const float* __restrict__ krow, const float* __restrict__ srow, int E, int k,
                                           int lane, int16_t* sidx, int* my_e, float* my_s, float* sum_out) {
-  float kv[NI], sv[NI];
+  // lane l holds experts e = l + 32 i: the key as an order-preserving unsigned image (keys are never
+  // -0 or NaN, so every key maps above 0; 0 marks "nothing"), its score and its id
+  uint32_t ku[NI];
+  float sv[NI];
+  int ev[NI];
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int e = lane + 32 * i;
-    kv[i] = (e < E) ? __ldcg(krow + e) : 0.f;          // through L2: another CTA may have written them
-    sv[i] = (e < E) ? __ldcg(srow + e) : 0.f;
+    const bool in = e < E;
+    const uint32_t bits = in ? __float_as_uint(__ldcg(krow + e)) : 0u;   // through L2: another CTA wrote them
+    ku[i] = in ? ((bits & 0x80000000u) ? ~bits : (bits | 0x80000000u)) : 0u;
+    sv[i] = in ? __ldcg(srow + e) : 0.f;
+    ev[i] = in ? e : 0x7fffffff;
   }
-  uint32_t taken = 0;
-  auto local_best = [&](float& bk, int& be) {
-    bk = 0.f;
-    be = 0x7fffffff;
+  // each lane sorts its items best first, (key desc, id asc), with a bitonic network in registers
 #pragma unroll
-    for (int i = 0; i < NI; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (be == 0x7fffffff || kv[i] > bk)) { bk = kv[i]; be = e; }
-    }
-  };
-  float lk;
-  int le;
-  local_best(lk, le);
+  for (int size = 2; size <= NI; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool j_better = ku[j] > ku[i] || (ku[j] == ku[i] && ev[j] < ev[i]);
+          const bool swap = ((i & size) == 0) ? j_better : !j_better;
+          const uint32_t tk = ku[i];
+          const float ts = sv[i];
+          const int te = ev[i];
+          ku[i] = swap ? ku[j] : ku[i];
+          sv[i] = swap ? sv[j] : sv[i];
+          ev[i] = swap ? ev[j] : ev[i];
+          ku[j] = swap ? tk : ku[j];
+          sv[j] = swap ? ts : sv[j];
+          ev[j] = swap ? te : ev[j];
+        }
+      }
+  // k rounds over the lanes' heads: the largest key, then the lowest id holding it; the winning
+  // lane drops its head
   float sel_sum = 0.f;
   for (int j = 0; j < k; ++j) {
-    // warp arg-max: the largest key (order-preserving unsigned image; keys are never -0 or NaN),
-    // then the lowest expert among the lanes holding it; a lane with nothing left offers 0
-    uint32_t u = 0;
-    if (le != 0x7fffffff) {
-      const uint32_t bits = __float_as_uint(lk);
-      u = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
-    }
-    const uint32_t m = __reduce_max_sync(0xffffffffu, u);
-    const int be = __reduce_min_sync(0xffffffffu, (u == m && le != 0x7fffffff) ? le : 0x7fffffff);
-    float own = 0.f;                            // the winner's score, read by its owner lane
-    if ((be & 31) == lane) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, ku[0]);
+    const int be = __reduce_min_sync(0xffffffffu, ku[0] == m ? ev[0] : 0x7fffffff);
+    const float sc = __shfl_sync(0xffffffffu, sv[0], be & 31);
+    const bool win = ev[0] == be;
 #pragma unroll
-      for (int i = 0; i < NI; ++i)
-        if (i == (be >> 5)) own = sv[i];
-      taken |= 1u << (be >> 5);
-      local_best(lk, le);
+    for (int i = 0; i + 1 < NI; ++i) {
+      ku[i] = win ? ku[i + 1] : ku[i];
+      sv[i] = win ? sv[i + 1] : sv[i];
+      ev[i] = win ? ev[i + 1] : ev[i];
     }
-    const float sc = __shfl_sync(0xffffffffu, own, be & 31);
+    if (win) {
+      ku[NI - 1] = 0u;
+      ev[NI - 1] = 0x7fffffff;
+    }
     sel_sum = __fadd_rn(sel_sum, sc);
     if (lane == j) { *my_e = be; *my_s = sc; }
     if (sidx && lane == 0) sidx[j] = (int16_t)be;
@@ -479,7 +528,6 @@ __device__ void plan_single_block(const float* __restrict__ score, const float* 
                                   int32_t* __restrict__ row_of_slot, const int32_t* __restrict__ anchor,
                                   uint32_t* status, uint32_t* mask, int16_t* sidx, int* scnt, int* wsum, int* total) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  for (int i = threadIdx.x; i < E * 8; i += blockDim.x) mask[i] = 0;
   for (int t = warp; t < T; t += nwarps) {
     if (anchor_of(anchor, t, T, status) >= 0) continue;      // after every self-routed row
     int my_e = -1;
@@ -490,6 +538,8 @@ __device__ void plan_single_block(const float* __restrict__ score, const float* 
       topk_w[(size_t)t * k + lane] = __fdiv_rn(my_s, sum);
     }
   }
+  // the bitmasks are first used after the barrier below: zeroed after the selection, off its path
+  for (int i = threadIdx.x; i < E * 8; i += blockDim.x) mask[i] = 0;
   if (anchor) {
     __syncthreads();
     for (int t = warp; t < T; t += nwarps) {
@@ -549,8 +599,13 @@ inline size_t plan_single_smem(int E, int k) {
 }
 
 // T <= kPlanBlock: top-k and plan in one CTA.
+// Threads of the one-CTA plan: a warp selects one row at a time, so more warps take more rows at
+// once; up to 8 keys per lane (E <= 256) the registers allow 32 warps.
 template <int NI>
-__global__ void __launch_bounds__(512) topk_plan_single_kernel(const float* __restrict__ score,
+constexpr int plan_single_threads() { return NI <= 8 ? 1024 : 512; }
+
+template <int NI>
+__global__ void __launch_bounds__(plan_single_threads<NI>()) topk_plan_single_kernel(const float* __restrict__ score,
                                                                const float* __restrict__ key,
                                                                const uint8_t* __restrict__ dead, int T, int E, int k,
                                                                int32_t* __restrict__ topk_idx,
@@ -563,9 +618,6 @@ __global__ void __launch_bounds__(512) topk_plan_single_kernel(const float* __re
                                                                uint32_t* __restrict__ ready) {
   pdl_trigger();
   pdl_wait();
-  // tile counters of the one-launch W13 + W2 GEMM (E per expert + 1 total; nullable): zero them
-  if (ready)
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) ready[e] = 0;
   extern __shared__ __align__(16) uint8_t psm[];
   uint32_t* mask = reinterpret_cast<uint32_t*>(psm);
   int16_t* sidx = reinterpret_cast<int16_t*>(psm + align_up((size_t)E * 8 * 4, 16));
@@ -574,6 +626,10 @@ __global__ void __launch_bounds__(512) topk_plan_single_kernel(const float* __re
   int* total = wsum + 32;
   plan_single_block<NI>(score, key, dead, T, E, k, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot,
                         anchor, status, mask, sidx, scnt, wsum, total);
+  // tile counters of the one-launch W13 + W2 GEMM (E per expert + 1 total; nullable): zero them
+  // (that GEMM reads them only after this grid has completed)
+  if (ready)
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) ready[e] = 0;
 }
 
 // Multi-block plan, step 1: one CTA per kPlanBlock tokens reads the choices from topk_idx (written
@@ -691,7 +747,8 @@ static int launch_topk_plan_ni(int nb, int E, size_t smem, cudaStream_t st, cons
       ensure_smem_limit((const void*)topk_plan_kernel, 64 * 1024))
     return MOE_ERR_CUDA;
   if (nb == 1)
-    return launch_pdl(topk_plan_single_kernel<NI>, dim3(1), dim3(512), plan_single_smem(E, k), st, score, key, dead, T,
+    return launch_pdl(topk_plan_single_kernel<NI>, dim3(1), dim3(plan_single_threads<NI>()), plan_single_smem(E, k),
+                      st, score, key, dead, T,
                       E, k, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, anchor, status, ready);
   // many blocks: selection spread over the whole GPU (anchored rows next), then the per-block plan
   const int sel_blocks = (int)std::min<long long>(((long long)T + 7) / 8, (long long)num_sms() * 8);
@@ -731,7 +788,8 @@ static int launch_topk_single_plain_ni(cudaStream_t st, const float* score, cons
                                        int T, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* counts,
                                        int32_t* offsets, int32_t* slot_of_row, int32_t* row_of_slot) {
   if (ensure_smem_limit((const void*)topk_plan_single_kernel<NI>, 64 * 1024)) return MOE_ERR_CUDA;
-  topk_plan_single_kernel<NI><<<1, 512, plan_single_smem(E, k), st>>>(score, key, dead, T, E, k, topk_idx, topk_w,
+  topk_plan_single_kernel<NI><<<1, plan_single_threads<NI>(), plan_single_smem(E, k), st>>>(score, key, dead, T, E, k,
+                                                                                          topk_idx, topk_w,
                                                                        counts, offsets, slot_of_row, row_of_slot,
                                                                        nullptr, nullptr, nullptr);
   return launch_status();
@@ -768,15 +826,22 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
   }
   float* score = ws_ptr<float>(ws, L.score);
   float* key = ws_ptr<float>(ws, L.key);
-  const size_t dec_smem = router_decode_smem(T, H);
+  const DecodeRouterCfg dc = decode_router_cfg(T, H, E);
   int rc0 = MOE_OK;
-  if (T <= kDecMaxT && kDecEpc * (H / kRouterChunk) <= 256 && dec_smem <= kDecodeSmemMax) {
-    if (ensure_smem_limit((const void*)router_decode_kernel, (int)kDecodeSmemMax)) return MOE_ERR_CUDA;
+  if (T <= kDecMaxT && dc.threads <= kDecThreadsMax && dc.smem <= kDecodeSmemMax) {
     const bool fuse = xq && xs;
     uint8_t* fq = fuse ? xq : nullptr;
     uint8_t* fs = fuse ? xs : nullptr;
-    rc0 = launch_pdl(router_decode_kernel, dim3(ceil_div(E, kDecEpc)), dim3(256), dec_smem, st, x, wr, bias, T, H, E,
-                     score, key, fq, fs);
+    const dim3 grid(ceil_div(E, dc.epc), ceil_div(T, dc.tpc));
+    if (dc.ept == 1) {
+      if (ensure_smem_limit((const void*)router_decode_kernel<1>, (int)kDecodeSmemMax)) return MOE_ERR_CUDA;
+      rc0 = launch_pdl(router_decode_kernel<1>, grid, dim3(dc.threads), dc.smem, st, x, wr, bias, T, H, E, dc.epc,
+                       dc.tpc, score, key, fq, fs);
+    } else {
+      if (ensure_smem_limit((const void*)router_decode_kernel<2>, (int)kDecodeSmemMax)) return MOE_ERR_CUDA;
+      rc0 = launch_pdl(router_decode_kernel<2>, grid, dim3(dc.threads), dc.smem, st, x, wr, bias, T, H, E, dc.epc,
+                       dc.tpc, score, key, fq, fs);
+    }
     if (quant_done) *quant_done = fuse;
   } else if (T <= kSmallT) {
     rc0 = launch_pdl(router_small_kernel, dim3(ceil_div(E, 8)), dim3(256), 0, st, x, wr, bias, T, H, E, score, key);

@@ -18,11 +18,21 @@ def _const(name):
     return eval(m.group(1))  # noqa: S307 - integer literals / products from our own source
 
 
-def _decode_router(T, H):
+def _decode_router(T, H, E=256):
     nc = H // 64
-    epc, pitch, group = _const("MOE_DEC_EPC"), _const("kDecPitch"), _const("kDecGroup")
-    smem = min(T, group) * nc * pitch + epc * T * nc * 4
-    return T <= _const("kDecMaxT") and epc * nc <= 256 and smem <= _const("kDecodeSmemMax")
+    small = T <= _const("kDecSmallT")
+    ept = 1 if small else 2
+    epc = min(E, _const("kDecEpcSmall") if small else _const("kDecEpcLarge"))
+    tpc = T if small else _const("kDecTpcLarge")
+    pitch, cap = _const("kDecPitch"), _const("kDecodeSmemMax")
+
+    def smem(tp):
+        return tp * nc * pitch + epc * tp * (nc + 1) * 4
+
+    while tpc > 1 and smem(tpc) > cap:
+        tpc -= 1
+    threads = -(-epc // ept) * nc
+    return T <= _const("kDecMaxT") and threads <= _const("kDecThreadsMax") and smem(tpc) <= cap
 
 
 def test_decode_router_predicate_matches_the_library_constants():

@@ -474,7 +474,10 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
             ok = false;
             break;
           }
-          fence_async_smem();
+          // narrow tiles' token rows and scales arrive by cp.async (generic proxy): make them visible
+          // to the MMA's async proxy here; the wide tiles' producer fences its own stores before it
+          // arrives on the stage barrier
+          if (!kTmaB) fence_async_smem();
           tc_fence_after();
           const int nv = min(L::KT, q.KC - kc0);
           uint8_t* sA0 = tiles + stage * L::kStageBytes;

@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(Ws::kThreads, 1)
               ok = false;
               break;
             }
-            fence_async_smem();
+            // (the token producer fenced its scale stores to the async proxy before arriving)
             tc_fence_after();
             uint8_t* sB = stages + stage * Ws::kStageBytes;
             uint8_t* sSFB = sB + Ws::kTileB;

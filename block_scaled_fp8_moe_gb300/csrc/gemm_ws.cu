@@ -15,10 +15,12 @@
 //
 // Roles (384 threads):
 //   warp 0      TMA of the unit's weight panel (KC tiles) and its scale blocks into the resident
-//               region, once the previous unit's MMAs no longer read it
+//               region, each K-chunk as soon as the previous unit's last MMAs on it are done (one
+//               barrier pair per resident chunk)
 //   warp 1      per (tile, K-chunk): one TMA box of plan rows (lane 0) and the scale atoms of the
 //               tile's columns (every lane: plain loads, 16-byte shared stores) into a ring of stages
-//   warp 2      TMEM owner and MMA issuer: the unit's A scales into resident TMEM columns, then per
+//   warp 2      TMEM owner and MMA issuer: the unit's A scales into resident TMEM columns as its
+//               chunks land, then per
 //               K-chunk the stage's B scales and four K = 32 MMAs; commits release stages,
 //               accumulators and, after the unit's last MMA, the resident panel
 //   warps 4-11  epilogue: plan-order fp32 rows of the per-slot buffer (two sets of four warps,
@@ -79,9 +81,9 @@ __global__ void __launch_bounds__(Ws::kThreads, 1)
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;                        // [2]
   uint64_t* acc_empty = acc_full + 2;                    // [2]
-  uint64_t* a_full = acc_empty + 2;
-  uint64_t* a_empty = a_full + 1;
-  uint64_t* drain = a_empty + 1;
+  uint64_t* a_full = acc_empty + 2;                      // [kKcMax]: one per resident K-chunk
+  uint64_t* a_empty = a_full + Ws::kKcMax;               // [kKcMax]
+  uint64_t* drain = a_empty + Ws::kKcMax;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   int* s_off = reinterpret_cast<int*>(misc + Ws::kMisc);   // expert offsets [E+1]
@@ -102,8 +104,10 @@ __global__ void __launch_bounds__(Ws::kThreads, 1)
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], Ws::kEpiWarps);
     }
-    mbar_init(a_full, 1);
-    mbar_init(a_empty, 1);
+    for (int kc = 0; kc < Ws::kKcMax; ++kc) {
+      mbar_init(&a_full[kc], 1);
+      mbar_init(&a_empty[kc], 1);
+    }
     mbar_init(drain, 1);
     mbar_fence_init();
   }
@@ -173,13 +177,18 @@ __global__ void __launch_bounds__(Ws::kThreads, 1)
       const uint32_t tile_bytes = p.a_fp8 ? 2 * kTileCodeBytes : kTileCodeBytes;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit d = decode(u);
-        if (!mbar_wait(a_empty, a_phase ^ 1, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_EMPTY)) break;
+        // K-chunk kc of the panel is replaced as soon as the previous unit's last MMAs on it are done
         const int tile0 = (d.e * p.MT + d.m) * KC;
-        mbar_arrive_expect_tx(a_full, KC * (tile_bytes + kTileScaleBytes));
-        for (int kc = 0; kc < KC; ++kc) {
-          tma_load_2d(resA + kc * Ws::kTileA, &tmap_a, 0, (tile0 + kc) * 128, a_full);
-          bulk_load(resSfa + kc * 512, p.a_scales + (size_t)(tile0 + kc) * kTileScaleBytes, kTileScaleBytes, a_full);
+        bool okw = true;
+        for (int kc = 0; kc < KC && okw; ++kc) {
+          okw = mbar_wait(&a_empty[kc], a_phase ^ 1, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_EMPTY);
+          if (!okw) break;
+          mbar_arrive_expect_tx(&a_full[kc], tile_bytes + kTileScaleBytes);
+          tma_load_2d(resA + kc * Ws::kTileA, &tmap_a, 0, (tile0 + kc) * 128, &a_full[kc]);
+          bulk_load(resSfa + kc * 512, p.a_scales + (size_t)(tile0 + kc) * kTileScaleBytes, kTileScaleBytes,
+                    &a_full[kc]);
         }
+        if (!okw) break;
         a_phase ^= 1;
       }
     }
@@ -253,15 +262,8 @@ __global__ void __launch_bounds__(Ws::kThreads, 1)
       const uint32_t tsfa0 = tmem + Ws::kSfaCol;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
         const Unit d = decode(u);
-        if (!mbar_wait(a_full, a_phase, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_FULL)) {
-          ok = false;
-          break;
-        }
-        a_phase ^= 1;
-        tc_fence_after();
-        for (int kc = 0; kc < KC; ++kc)
-          tc_cp_32x128b_warpx4(tsfa0 + 4 * kc, smem_desc(smem_u32(resSfa + kc * 512), 16, 128, 0));
         for (int nt = d.nt0; nt < d.nt1 && ok; ++nt, ++it) {
+          const bool first_tile = nt == d.nt0, last_tile = nt + 1 == d.nt1;
           const int tw = d.tw;
           const uint32_t idesc_base = idesc_mxf8f6f4(p.a_fp8 ? 0 : 5 /*weights E4M3 or E2M1*/, 0 /*E4M3*/, 128, tw, 0, 0);
           const int acc = it & 1;
@@ -274,6 +276,16 @@ __global__ void __launch_bounds__(Ws::kThreads, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem + (uint32_t)(acc * Ws::kAccStride);
           for (int kc = 0; kc < KC; ++kc) {
+            if (first_tile) {
+              // the unit's K-chunk kc of the panel has landed: its A scales go to their TMEM columns
+              // (issued after the previous unit's MMAs that read them, in the tcgen05 pipe's order)
+              if (!mbar_wait(&a_full[kc], a_phase, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_FULL)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              tc_cp_32x128b_warpx4(tsfa0 + 4 * kc, smem_desc(smem_u32(resSfa + kc * 512), 16, 128, 0));
+            }
             if (!mbar_wait(&full[stage], phase, kWaitLimitNs, abort_flag, p.status, DEV_TIMEOUT_FULL)) {
               ok = false;
               break;
@@ -294,14 +306,16 @@ __global__ void __launch_bounds__(Ws::kThreads, 1)
               mma_mxf8f6f4(d_tmem, ad, bd, id, tsfa0 + 4 * kc, tsfb, (kc > 0 || kb > 0) ? 1u : 0u);
             }
             tc_commit(&empty[stage]);
+            // after the unit's last MMAs on K-chunk kc, that chunk of the panel (and its TMEM scales)
+            // may be replaced by the next unit's
+            if (last_tile) tc_commit(&a_empty[kc]);
             if (++stage == S) { stage = 0; phase ^= 1; }
           }
           if (!ok) break;
           tc_commit(&acc_full[acc]);
         }
         if (!ok) break;
-        // the resident panel (and its TMEM scales) may be replaced once this unit's MMAs are done
-        tc_commit(a_empty);
+        a_phase ^= 1;
       }
       tc_commit(drain);
       mbar_wait(drain, 0, kWaitLimitNs, nullptr, p.status, DEV_TIMEOUT_DRAIN);

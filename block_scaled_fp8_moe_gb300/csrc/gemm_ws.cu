@@ -20,9 +20,8 @@
 //   warp 1      per (tile, K-chunk): one TMA box of plan rows (lane 0) and the scale atoms of the
 //               tile's columns (every lane: plain loads, 16-byte shared stores) into a ring of stages
 //   warp 2      TMEM owner and MMA issuer: the unit's A scales into resident TMEM columns as its
-//               chunks land, then per
-//               K-chunk the stage's B scales and four K = 32 MMAs; commits release stages,
-//               accumulators and, after the unit's last MMA, the resident panel
+//               chunks land, then per K-chunk the stage's B scales and four K = 32 MMAs; commits
+//               release stages, accumulators and, after the unit's last tile, each resident chunk
 //   warps 4-11  epilogue: plan-order fp32 rows of the per-slot buffer (two sets of four warps,
 //               alternating column groups; two accumulator slots)
 // Every wait is bounded; after an expired wait the CTA records a code in the status word and its

@@ -16,7 +16,8 @@ namespace moe {
 // (+ y_shared[t]) ), r_j = row_of_slot[t k + j], w_j = topk_w[t k + j]; each w_j y is one fp32
 // multiply, the sum a left fold in fp32. Rows without slots (row_of_slot[t k] < 0) and rows the dead
 // mask flags get +0.0; a flagged row that still holds slots is recorded in *status.
-// kL2Only: y was written earlier in the same launch by other SMs, so it is read through L2 only.
+// kL2Only: y was written earlier in the same launch by other SMs, so it is read through L2 only;
+// otherwise (the combine kernel) each y row is read exactly once, with evict-first loads.
 template <bool kL2Only>
 __device__ __forceinline__ void combine_unit(const float* __restrict__ y, const float* __restrict__ topk_w,
                                              const int32_t* __restrict__ row_of_slot, int t, int h8, int H, int k,
@@ -33,8 +34,8 @@ __device__ __forceinline__ void combine_unit(const float* __restrict__ y, const 
       const int r = __ldg(row_of_slot + (size_t)t * k + j);
       const float w = __ldg(topk_w + (size_t)t * k + j);
       const float4* yp = reinterpret_cast<const float4*>(y + (size_t)r * H) + 2 * h8;
-      const float4 a = kL2Only ? __ldcg(yp) : __ldg(yp);
-      const float4 b = kL2Only ? __ldcg(yp + 1) : __ldg(yp + 1);
+      const float4 a = kL2Only ? __ldcg(yp) : __ldcs(yp);
+      const float4 b = kL2Only ? __ldcg(yp + 1) : __ldcs(yp + 1);
       const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int q = 0; q < 8; ++q) {

@@ -559,7 +559,7 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
             epi_w13_chunk(r, xchg + half * 2 * 16 * 64, qd, lane, threadIdx.x - 128 - 128 * half, bar_id, ok, true,
                           c0, m, row0, nrows, q);
           else if (ok)
-            epi_w2_chunk(r, qd, lane, c0, m, row0, nrows, q);
+            epi_w2_chunk<!kFused>(r, qd, lane, c0, m, row0, nrows, q);
         }
       }
       if (kFused) __threadfence();                    // this lane's stores of the tile, before the count

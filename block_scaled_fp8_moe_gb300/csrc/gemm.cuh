@@ -199,13 +199,20 @@ __device__ __forceinline__ void epi_w13_chunk(const uint32_t (&r)[16], float* xc
 // W2: one 16-column chunk of a 128-row accumulator of output panel m, held by warp q (TMEM lanes
 // 32q..32q+31): plan row row0 + c0 + c of the per-slot buffer gets features 128 m + 32 q + lane;
 // each store instruction writes 128 contiguous bytes (the routing weight is applied by the combine).
+// kStream: evict-first stores, for per-slot buffers that the combine reads only after the launch
+// (prefill: gigabytes that no later step of the GEMM reads from L2); the one-launch decode kernel
+// reads its rows back from L2 and stores them normally.
+template <bool kStream>
 __device__ __forceinline__ void epi_w2_chunk(const uint32_t (&r)[16], int q, int lane, int c0, int m, int row0,
                                              int nrows, const GemmParams& p) {
   const int feat = 128 * m + 32 * q + lane;
   float* yrow = p.y + (size_t)(row0 + c0) * p.H + feat;
 #pragma unroll
   for (int c = 0; c < 16; ++c)
-    if (c0 + c < nrows) yrow[(size_t)c * p.H] = __uint_as_float(r[c]);
+    if (c0 + c < nrows) {
+      if (kStream) __stcs(yrow + (size_t)c * p.H, __uint_as_float(r[c]));
+      else yrow[(size_t)c * p.H] = __uint_as_float(r[c]);
+    }
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -374,7 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair::kThreads, Pair
             epi_w13_chunk(rg[h], xchg + half * 2 * 16 * 64, q, lane, threadIdx.x - 128 - 128 * half, bar_id, ok,
                           store, c0, m, row0, nrows, p);
           else if (ok && store)
-            epi_w2_chunk(rg[h], q, lane, c0, m, row0, nrows, p);
+            epi_w2_chunk<true>(rg[h], q, lane, c0, m, row0, nrows, p);
         }
       }
       tc_fence_before();

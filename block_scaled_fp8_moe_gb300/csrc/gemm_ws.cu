@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(Ws::kThreads, 1)
 #pragma unroll
             for (int h = 0; h < kGrp; ++h) {
               const int c0 = cg + 16 * h;
-              if (c0 < d.tw) epi_w2_chunk(rg[h], qd, lane, c0, d.m, row0, nrows, p);
+              if (c0 < d.tw) epi_w2_chunk<true>(rg[h], qd, lane, c0, d.m, row0, nrows, p);
             }
           }
         }

@@ -49,6 +49,31 @@ def test_route_bit_exact(T, H, E, k):
     assert np.array_equal(plan.row_of_slot.cpu().numpy()[:T * k], ref.row_of_slot)
 
 
+@pytest.mark.parametrize("E,n_tied", [(64, 40), (128, 100)])
+def test_route_screen_long_candidate_lists(E, n_tied):
+    """Screened routing (T = 300) where every row's candidate list is long: n_tied experts share one
+    router row and a bias that puts them on top, so each row has at least n_tied candidates (40: a
+    long list; 100: more than a list holds, every expert recomputed). The tied keys are equal, so
+    the lowest expert ids win."""
+    from block_scaled_fp8_moe_gb300 import binding as B
+    T, H, k = 300, 256, 8
+    rng = np.random.default_rng(E + n_tied)
+    x = _bf16(rng.standard_normal((T, H)))
+    wr = _bf16(rng.standard_normal((E, H)) * 0.02)
+    wr[:n_tied] = wr[0]
+    bias = (rng.standard_normal(E) * 0.01).astype(np.float32)
+    bias[:n_tied] = 1.0
+    shp = B.shape(T, H, E, k, 64)
+    ws = B.alloc_workspace(shp)
+    plan = B.moe_route_topk(shp, x.cuda(), wr.cuda(), torch.from_numpy(bias).cuda(), None, ws)
+    B.moe_check_device_status(ws)
+    ref = M.route(x.float().numpy(), wr.float().numpy(), bias, k, None)
+    assert np.array_equal(ref.topk_idx, np.tile(np.arange(k, dtype=ref.topk_idx.dtype), (T, 1)))
+    assert np.array_equal(plan.topk_idx.cpu().numpy(), ref.topk_idx)
+    assert np.array_equal(plan.topk_w.cpu().numpy().view(np.uint32), ref.topk_w.view(np.uint32))
+    assert np.array_equal(plan.expert_offsets.cpu().numpy(), ref.offsets)
+
+
 @pytest.mark.parametrize("T", [5, 48, 300])
 def test_route_dead_rows_and_ties(T):
     plan, ref = _route_case(T, 256, 16, 4, seed=T, dead_frac=0.3, ties=True)

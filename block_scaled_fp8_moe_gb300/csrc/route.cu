@@ -600,9 +600,12 @@ inline size_t plan_single_smem(int E, int k) {
 
 // T <= kPlanBlock: top-k and plan in one CTA.
 // Threads of the one-CTA plan: a warp selects one row at a time, so more warps take more rows at
-// once; up to 8 keys per lane (E <= 256) the registers allow 32 warps.
+// once; up to 8 keys per lane (E <= 256) the registers allow 32 warps. Small batches launch 8 warps
+// (every later step of the plan meets at block-wide barriers, cheaper with fewer warps).
 template <int NI>
 constexpr int plan_single_threads() { return NI <= 8 ? 1024 : 512; }
+template <int NI>
+inline int plan_single_launch_threads(int T) { return (NI <= 8 && T <= 8) ? 256 : plan_single_threads<NI>(); }
 
 template <int NI>
 __global__ void __launch_bounds__(plan_single_threads<NI>()) topk_plan_single_kernel(const float* __restrict__ score,
@@ -747,7 +750,8 @@ static int launch_topk_plan_ni(int nb, int E, size_t smem, cudaStream_t st, cons
       ensure_smem_limit((const void*)topk_plan_kernel, 64 * 1024))
     return MOE_ERR_CUDA;
   if (nb == 1)
-    return launch_pdl(topk_plan_single_kernel<NI>, dim3(1), dim3(plan_single_threads<NI>()), plan_single_smem(E, k),
+    return launch_pdl(topk_plan_single_kernel<NI>, dim3(1), dim3(plan_single_launch_threads<NI>(T)),
+                      plan_single_smem(E, k),
                       st, score, key, dead, T,
                       E, k, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, anchor, status, ready);
   // many blocks: selection spread over the whole GPU (anchored rows next), then the per-block plan
@@ -788,7 +792,8 @@ static int launch_topk_single_plain_ni(cudaStream_t st, const float* score, cons
                                        int T, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* counts,
                                        int32_t* offsets, int32_t* slot_of_row, int32_t* row_of_slot) {
   if (ensure_smem_limit((const void*)topk_plan_single_kernel<NI>, 64 * 1024)) return MOE_ERR_CUDA;
-  topk_plan_single_kernel<NI><<<1, plan_single_threads<NI>(), plan_single_smem(E, k), st>>>(score, key, dead, T, E, k,
+  topk_plan_single_kernel<NI><<<1, plan_single_launch_threads<NI>(T), plan_single_smem(E, k), st>>>(score, key, dead,
+                                                                                                   T, E, k,
                                                                                           topk_idx, topk_w,
                                                                        counts, offsets, slot_of_row, row_of_slot,
                                                                        nullptr, nullptr, nullptr);

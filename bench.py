@@ -566,6 +566,10 @@ def measure(cfg, args, gpu, world, headline: bool, peak_info=None):
     clocks = ClockSampler(dev.index or 0)
     clocks.start()
     time.sleep(0.3)
+    # the pause idles the GPU: a few untimed steps bring its clocks back up before the timed ones
+    for i in range(3):
+        gpu.flush_l2(float(i))
+        fwd()
     barrier()
     torch.cuda.synchronize()
     step_ms = gpu.timed(fwd, args.steps, stream)

@@ -583,6 +583,13 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
       const long long gt = (long long)blockIdx.x * kEpiThreads + (threadIdx.x - 128);
       const long long gstride = (long long)gridDim.x * kEpiThreads;
       if (gt - lane < units) {
+        // the unit's routing data come from the plan, written before this launch: pull them into L1
+        // while the last down-projection tiles finish, so only the per-slot rows remain to fetch
+        if (gt < units) {
+          const int tt = (int)(gt / (p2.H / 8));
+          asm volatile("prefetch.global.L1 [%0];" ::"l"(p2.row_of_slot + (size_t)tt * p2.k));
+          asm volatile("prefetch.global.L1 [%0];" ::"l"(p2.topk_w + (size_t)tt * p2.k));
+        }
         uint32_t go = ok ? 1u : 0u;
         if (lane == 0 && go)
           go = wait_count_at_least(p2.ready + E, (uint32_t)(s_cum2[E] * Threads<BN>::kEpiWarps), kWaitLimitNs,

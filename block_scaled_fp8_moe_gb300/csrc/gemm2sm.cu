@@ -1,7 +1,7 @@
 // Grouped block-scaled GEMMs of the routed experts on CTA pairs (tcgen05 .cta_group::2), for wide
-// (prefill) token tiles. The layer uses it for down projections with a short K (fewer than 8
-// K-chunks, e.g. 576-wide experts), where it measured faster than one-CTA tiles; it computes the
-// gate/up GEMM too (same results), which runs faster on one-CTA tiles.
+// (prefill) token tiles. Built and parity-checked for both GEMMs (same results as every other tile
+// kind); the layer dispatches neither to it: the gate/up GEMM runs faster on one-CTA tiles and the
+// short-K down projection on weight-stationary tiles (gemm_ws.cu).
 //
 // "New Deepseek 4.1 flash recipe", post 6 "How it works" items 1-2: FP8 activations x FP4 weights
 // through a block-scaled MMA (kind::mxf8f6f4); prefill rasterises weights larger than L2 in panels.

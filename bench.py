@@ -113,8 +113,8 @@ def gemm_source_hash() -> str:
 
 def gemm_kind(name: str):
     """Which step a grouped-GEMM launch is, from its demangled name: the MODE template argument of
-    grouped_gemm_kernel (0 down, 1 gate/up, 2 both in one launch), the weight-stationary and the
-    CTA-pair kernels; None for every other kernel."""
+    grouped_gemm_kernel (0 down, 1 gate/up, 2 both in one launch, 3 the same launch routing a small
+    batch itself), the weight-stationary and the CTA-pair kernels; None for every other kernel."""
     if name.startswith("grouped_gemm_ws_kernel"):
         return "w2"
     m = re.search(r"grouped_gemm_pair_kernel<(true|false)", name)
@@ -122,7 +122,7 @@ def gemm_kind(name: str):
         return "w13" if m.group(1) == "true" else "w2"
     m = re.search(r"grouped_gemm_kernel<\d+, (\d)>", name)
     if m:
-        return {"0": "w2", "1": "w13", "2": "experts"}[m.group(1)]
+        return {"0": "w2", "1": "w13", "2": "experts", "3": "experts_selfroute"}[m.group(1)]
     return None
 
 
@@ -419,6 +419,8 @@ def launches_per_step(cfg, shared: bool = False) -> int:
     with a shared expert (its identity plan and two GEMMs on the side stream)."""
     T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
     decode_router = decode_router_fits(T, H, E)
+    if decode_router and self_routed_gemms(cfg) and not shared:
+        return 2                                      # router (+ quantisation), then GEMMs routing themselves
     if decode_router:
         n = 1                                         # logits (+ fused MXFP8 quantisation)
     elif T > 16 and E <= 256 and H % 64 == 0 and H <= 4096:
@@ -437,6 +439,12 @@ def launches_per_step(cfg, shared: bool = False) -> int:
 def wide_w13(cfg) -> bool:
     """True when W13 runs the wide (prefill) token tiles, which read plan-order activation rows."""
     return cfg.T * cfg.k / cfg.E > 64
+
+
+def self_routed_gemms(cfg) -> bool:
+    """True when the one-launch GEMMs also select the experts and build the plan (at most 8 rows,
+    256 experts; the library's self_plan_supported, given the decode router and no shared expert)."""
+    return 1 <= cfg.T <= 8 and cfg.E <= 256 and fused_gemms(cfg)
 
 
 def fused_gemms(cfg) -> bool:

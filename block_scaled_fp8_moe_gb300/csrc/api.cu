@@ -244,12 +244,20 @@ int forward_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   // decode-sized tiles run W13 and W2 as one persistent launch (its per-expert counters are zeroed
-  // by this call's plan kernel)
+  // by this call's plan kernel); a batch of a few self-routed rows without a shared expert runs
+  // the router and then that launch alone, which selects the experts and builds the plan itself
+  // (the decode router zeroes the counters)
   uint32_t* ready = ws_ptr<uint32_t>(ws, L.ready);
   const bool fuse_gemms = fused_gemms_supported(s);
+  const bool self_plan = fuse_gemms && !shared && !anchor && self_plan_supported(s);
   bool quant_done = false;
-  rc = launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, ws, st,
-                    xq, xs, &quant_done, anchor, fuse_gemms ? ready : nullptr);
+  if (self_plan) {
+    rc = launch_router_decode_scores(s, x, w_router, bias, ws, st, xq, xs, ready);
+    quant_done = true;
+  } else {
+    rc = launch_route(s, x, w_router, bias, dead, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot, ws,
+                      st, xq, xs, &quant_done, anchor, fuse_gemms ? ready : nullptr);
+  }
   if (rc) return rc;
   uint8_t* xqp = ws_ptr<uint8_t>(ws, L.xqp);
   uint8_t* xsp = ws_ptr<uint8_t>(ws, L.xsp);
@@ -304,9 +312,11 @@ int forward_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router
   // with no shared expert to add, the one-launch GEMMs also run the combine at their end
   const bool fused_combine = fuse_gemms && !shared;
   if (fuse_gemms) {
+    const SelfPlanArgs sp{ws_ptr<float>(ws, L.score), ws_ptr<float>(ws, L.key), dead, topk_idx, topk_w, counts,
+                          offsets, slot_of_row, row_of_slot};
     rc = launch_w13_w2_fused(s, xq, xs, w13, w13_s, w2, w2_s, offsets, slot_of_row, hq, hs, im.swiglu, y, status,
                              ready, st, fused_combine ? topk_w : nullptr, fused_combine ? row_of_slot : nullptr,
-                             fused_combine ? out : nullptr);
+                             fused_combine ? out : nullptr, self_plan ? &sp : nullptr);
   } else {
     rc = launch_w13(s, xq, xs, w13, w13_s, offsets, slot_of_row, hq, hs, im.swiglu, status, xqp, xsp, plan_rows, st);
     if (!rc) rc = launch_w2(s, hq, hs, w2, w2_s, offsets, slot_of_row, y, status, st);

@@ -18,7 +18,8 @@ namespace moe {
 // mask flags get +0.0; a flagged row that still holds slots is recorded in *status.
 // kL2Only: y was written earlier in the same launch by other SMs, so it is read through L2 only;
 // otherwise (the combine kernel) each y row is read exactly once, with evict-first loads.
-template <bool kL2Only>
+// kPlanShared: topk_w and row_of_slot point to shared memory (plain loads, not the read-only path).
+template <bool kL2Only, bool kPlanShared = false>
 __device__ __forceinline__ void combine_unit(const float* __restrict__ y, const float* __restrict__ topk_w,
                                              const int32_t* __restrict__ row_of_slot, int t, int h8, int H, int k,
                                              uint16_t* __restrict__ out, const float* __restrict__ y_shared,
@@ -31,8 +32,8 @@ __device__ __forceinline__ void combine_unit(const float* __restrict__ y, const 
   if (flagged && held && h8 == 0 && status) atomicCAS(status, 0u, (uint32_t)DEV_BAD_INPUT);
   if (held && !flagged) {
     for (int j = 0; j < k; ++j) {
-      const int r = __ldg(row_of_slot + (size_t)t * k + j);
-      const float w = __ldg(topk_w + (size_t)t * k + j);
+      const int r = kPlanShared ? row_of_slot[(size_t)t * k + j] : __ldg(row_of_slot + (size_t)t * k + j);
+      const float w = kPlanShared ? topk_w[(size_t)t * k + j] : __ldg(topk_w + (size_t)t * k + j);
       const float4* yp = reinterpret_cast<const float4*>(y + (size_t)r * H) + 2 * h8;
       const float4 a = kL2Only ? __ldcg(yp) : __ldcs(yp);
       const float4 b = kL2Only ? __ldcg(yp + 1) : __ldcs(yp + 1);

@@ -17,6 +17,11 @@ constexpr int kRouterChunk = 64;       // fixed reduction chunk of the router lo
 constexpr int kPlanBlock = 256;        // tokens per plan-count block
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
+// One-launch decode layer that routes itself: at most one row per warp of the fused GEMM CTA, and
+// every expert's key in 8 registers per lane of the selecting warp
+constexpr int kSelfPlanMaxT = 8;
+constexpr int kSelfPlanMaxE = 256;
+constexpr int kSelfPlanNI = kSelfPlanMaxE / 32;
 constexpr int kTileK = 128;            // K elements per packed tile / pipeline stage
 constexpr int kTileRows = 128;         // weight rows per packed tile
 constexpr int kTileCodeBytes = kTileRows * kTileK / 2;   // 8192
@@ -192,16 +197,38 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
                  int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
                  int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done,
                  const int32_t* anchor, uint32_t* ready);
+// The decode router alone (scores, keys, and the MXFP8 quantisation of x into xq/xs), for a layer
+// call whose fused GEMM routes itself (self_plan_supported); it also zeroes the E + 1 counters in
+// ready.
+bool self_plan_supported(const moe_shape* s);
+int launch_router_decode_scores(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, void* ws,
+                                cudaStream_t st, uint8_t* xq, uint8_t* xs, uint32_t* ready);
+// The routing plan a self-routing fused GEMM builds (every CTA in shared memory) from the router's
+// scores and keys, and the arrays its CTA 0 writes it to.
+struct SelfPlanArgs {
+  const float* score;
+  const float* key;
+  const uint8_t* dead;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* slot_of_row;
+  int32_t* row_of_slot;
+};
 // W13 then W2 in one persistent launch, for decode-sized token tiles (fused_gemms_supported):
 // writes hq/hs (and dbg) like launch_w13 and y like launch_w2, and with out non-null also the
 // combine's output, like launch_combine without a shared expert or dead mask. ready: E + 1
-// counters, zeroed by the plan kernel of this layer call.
+// counters, zeroed by the kernel before it in this layer call. With sp non-null (requires out and
+// self_plan_supported) the launch routes itself and offsets / slot_of_row / topk_w / row_of_slot
+// are not read.
 bool fused_gemms_supported(const moe_shape* s);
 int launch_w13_w2_fused(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13,
                         const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, const int32_t* offsets,
                         const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg, float* y, uint32_t* status,
                         uint32_t* ready, cudaStream_t st, const float* topk_w = nullptr,
-                        const int32_t* row_of_slot = nullptr, uint16_t* out = nullptr);
+                        const int32_t* row_of_slot = nullptr, uint16_t* out = nullptr,
+                        const SelfPlanArgs* sp = nullptr);
 int launch_w13(const moe_shape* s, const uint8_t* xq, const uint8_t* xs, const uint8_t* w13, const uint8_t* w13s,
                const int32_t* offsets, const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg,
                uint32_t* status, uint8_t* xq_plan, uint8_t* xs_plan, bool plan_rows_ready, cudaStream_t st,

@@ -34,6 +34,7 @@
 #include "gemm.cuh"
 #include "mx.cuh"
 #include "ptx.cuh"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -128,15 +129,20 @@ struct Smem {
   static constexpr int kRows = 128 * 8;                         // gather row table
   static constexpr int kFixed = 1024 + kTiles + kXchg + kMisc + kRows;
   // + plan tables sized per launch: (E + 1) x (offsets, tile starts) ints, and a second table of
-  // tile starts when one launch runs both GEMMs
-  static int total(int E, bool two_gemms) {
-    return kFixed + (int)align_up((size_t)(E + 1) * (two_gemms ? 12 : 8), 16);
+  // tile starts when one launch runs both GEMMs; + when the launch plans for itself, a token bitmask
+  // per expert and per slot its expert, weight, plan row and (indexed by plan row) its slot
+  static int total(int E, bool two_gemms, int self_plan_slots = 0) {
+    return kFixed + (int)align_up((size_t)(E + 1) * (two_gemms ? 12 : 8), 16) +
+           (self_plan_slots ? (int)align_up((size_t)E * 4 + (size_t)self_plan_slots * 16, 16) : 0);
   }
   static_assert(kFixed + (kMaxE + 1) * 8 + 16 <= 227 * 1024, "shared memory per CTA at the largest E");
 };
 
 // MODE 0: the down projection (W2); 1: gate/up with SwiGLU and requant (W13); 2: W13 then W2 in
-// one persistent launch (decode tiles): every CTA works through its W13 items, then its W2 items.
+// one persistent launch (decode tiles): every CTA works through its W13 items, then its W2 items;
+// 3: mode 2 for a batch of at most kSelfPlanMaxT rows that routes itself: every CTA takes the top-k
+// of the rows from the router's scores (one warp per row, the plan kernel's selection) and builds
+// the plan in its shared memory, so no plan kernel runs between the router and the GEMMs.
 // A W2 item's weight tiles stream as soon as the CTA reaches it; its token rows (h) are gathered
 // once the W13 epilogues have counted every W13 tile of that expert (GemmParams::ready). All CTAs
 // are resident (the grid is sized to the GPU), and each CTA finishes its W13 items before its W2
@@ -148,7 +154,8 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
                         const __grid_constant__ CUtensorMap tmap_a2, const __grid_constant__ GemmParams p,
                         const __grid_constant__ GemmParams p2) {
   using L = Smem<BN>;
-  constexpr bool kFused = MODE == 2;
+  constexpr bool kFused = MODE >= 2;
+  constexpr bool kSelfPlan = MODE == 3;
   constexpr bool kW13Only = MODE == 1;
   constexpr int S = L::kStages;
   constexpr int NACC = L::kAcc;                    // accumulator slots in TMEM
@@ -169,6 +176,13 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
   int* s_off = reinterpret_cast<int*>(misc + L::kMisc + L::kRows);      // expert offsets [E+1]
   int* s_cum = s_off + (p.E + 1);                                       // MT * tile starts [E+1]
   int* s_cum2 = s_cum + (p.E + 1);                                      // the same for p2.MT (mode 2)
+  // mode 3: the plan built here (nsl = T k slots)
+  const int nsl = kSelfPlan ? p.T * p.k : 0;
+  uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_cum2 + (p.E + 1));   // live rows choosing e, bit t
+  int* s_se = reinterpret_cast<int*>(s_mask + p.E);                     // slot -> expert
+  float* s_sw = reinterpret_cast<float*>(s_se + nsl);                   // slot -> routing weight
+  int* s_ros = s_se + 2 * nsl;                                          // slot -> plan row or -1
+  int* s_sor = s_se + 3 * nsl;                                          // plan row -> slot
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
@@ -196,30 +210,100 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
     prefetch_tmap(&tmap_a);
     if (kTmaB) prefetch_tmap(&tmap_b);
   }
+  if (kSelfPlan) {
+    for (int i = threadIdx.x; i < E; i += Threads<BN>::kCount) s_mask[i] = 0;
+    __syncthreads();
+  }
   pdl_wait();                                    // everything below may read upstream results
-  for (int i = threadIdx.x; i <= E; i += Threads<BN>::kCount) s_off[i] = p.offsets[i];
-  __syncthreads();
-  if (warp == 0) {
-    // tile starts: warp-parallel prefix sum of ceil(count_e / BN), times MT
-    const int per = (E + 31) / 32;
-    const int e0 = lane * per;
-    int local = 0;
-    for (int e = e0; e < min(E, e0 + per); ++e) local += (s_off[e + 1] - s_off[e] + BN - 1) / BN;
-    int incl = local;
+  if (kSelfPlan) {
+    // top-k of row t on warp t (the choices and weights of the plan kernel); a live row sets its
+    // bit in the masks of its k experts
+    for (int t = warp; t < p.T; t += Threads<BN>::kCount / 32) {
+      int my_e = 0;
+      float my_s = 0.f, sum = 0.f;
+      warp_topk<kSelfPlanNI>(p.key + (size_t)t * E, p.score + (size_t)t * E, E, p.k, lane, nullptr, &my_e, &my_s,
+                             &sum);
+      const bool live = p.dead == nullptr || p.dead[t] == 0;
+      if (lane < p.k) {
+        s_se[t * p.k + lane] = my_e;
+        s_sw[t * p.k + lane] = __fdiv_rn(my_s, sum);
+        if (live) atomicOr(&s_mask[my_e], 1u << t);
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // offsets and tile starts: warp-parallel prefix sums of count_e and ceil(count_e / BN)
+      const int per = (E + 31) / 32;
+      const int e0 = lane * per;
+      int lc = 0, lt = 0;
+      for (int e = e0; e < min(E, e0 + per); ++e) {
+        const int c = __popc(s_mask[e]);
+        lc += c;
+        lt += (c + BN - 1) / BN;
+      }
+      int ic = lc, it = lt;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      int v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
+      for (int off = 1; off < 32; off <<= 1) {
+        const int vc = __shfl_up_sync(0xffffffffu, ic, off);
+        const int vt = __shfl_up_sync(0xffffffffu, it, off);
+        if (lane >= off) {
+          ic += vc;
+          it += vt;
+        }
+      }
+      int rc = ic - lc, rt = it - lt;
+      for (int e = e0; e < min(E, e0 + per); ++e) {
+        const int c = __popc(s_mask[e]);
+        s_off[e] = rc;
+        s_cum[e] = rt * p.MT;
+        s_cum2[e] = rt * p2.MT;
+        rc += c;
+        rt += (c + BN - 1) / BN;
+      }
+      if (lane == 31) {
+        s_off[E] = ic;
+        s_cum[E] = it * p.MT;
+        s_cum2[E] = it * p2.MT;
+      }
+      __syncwarp();
+      // a live slot's plan row: its expert's offset plus the expert's rows of lower tokens
+      for (int i = lane; i < nsl; i += 32) {
+        const int t = i / p.k;
+        const int e = s_se[i];
+        const uint32_t bits = s_mask[e];
+        int row = -1;
+        if ((bits >> t) & 1u) {
+          row = s_off[e] + __popc(bits & ((1u << t) - 1u));
+          s_sor[row] = i;
+        }
+        s_ros[i] = row;
+      }
     }
-    int run = incl - local;
-    for (int e = e0; e < min(E, e0 + per); ++e) {
-      s_cum[e] = run * p.MT;
-      if (kFused) s_cum2[e] = run * p2.MT;
-      run += (s_off[e + 1] - s_off[e] + BN - 1) / BN;
-    }
-    if (lane == 31) {
-      s_cum[E] = incl * p.MT;
-      if (kFused) s_cum2[E] = incl * p2.MT;
+  } else {
+    for (int i = threadIdx.x; i <= E; i += Threads<BN>::kCount) s_off[i] = p.offsets[i];
+    __syncthreads();
+    if (warp == 0) {
+      // tile starts: warp-parallel prefix sum of ceil(count_e / BN), times MT
+      const int per = (E + 31) / 32;
+      const int e0 = lane * per;
+      int local = 0;
+      for (int e = e0; e < min(E, e0 + per); ++e) local += (s_off[e + 1] - s_off[e] + BN - 1) / BN;
+      int incl = local;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      int run = incl - local;
+      for (int e = e0; e < min(E, e0 + per); ++e) {
+        s_cum[e] = run * p.MT;
+        if (kFused) s_cum2[e] = run * p2.MT;
+        run += (s_off[e + 1] - s_off[e] + BN - 1) / BN;
+      }
+      if (lane == 31) {
+        s_cum[E] = incl * p.MT;
+        if (kFused) s_cum2[E] = incl * p2.MT;
+      }
     }
   }
   tc_fence_before();
@@ -317,6 +401,18 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
+    } else if (kSelfPlan && blockIdx.x == 0) {
+      // the plan, for the caller: written by CTA 0 on this warp's otherwise idle lanes 1..31
+      for (int i = lane - 1; i < nsl; i += 31) {
+        p.plan_topk_idx[i] = s_se[i];
+        p.plan_topk_w[i] = s_sw[i];
+        p.plan_row_of_slot[i] = s_ros[i];
+        if (s_ros[i] >= 0) p.plan_slot_of_row[s_ros[i]] = i;
+      }
+      for (int e = lane - 1; e <= E; e += 31) {
+        p.plan_offsets[e] = s_off[e];
+        if (e < E) p.plan_counts[e] = __popc(s_mask[e]);
+      }
     }
   } else if (kTmaB && warp == 1) {
     // ===================== TMA producer: activations (wide token tiles) =====================
@@ -403,7 +499,9 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
         long long r = -1;
         if (c < nrows) {
           const int prow = row0 + c;
-          r = (is_w13(first) && !q.b_plan_rows) ? (long long)(q.slot_of_row[prow] / q.k) : (long long)prow;
+          r = (is_w13(first) && !q.b_plan_rows)
+                  ? (long long)((kSelfPlan ? s_sor[prow] : q.slot_of_row[prow]) / q.k)
+                  : (long long)prow;
         }
         s_rows[c] = r;
       }
@@ -585,7 +683,8 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
       if (gt - lane < units) {
         // the unit's routing data come from the plan, written before this launch: pull them into L1
         // while the last down-projection tiles finish, so only the per-slot rows remain to fetch
-        if (gt < units) {
+        // (mode 3 holds them in shared memory)
+        if (!kSelfPlan && gt < units) {
           const int tt = (int)(gt / (p2.H / 8));
           asm volatile("prefetch.global.L1 [%0];" ::"l"(p2.row_of_slot + (size_t)tt * p2.k));
           asm volatile("prefetch.global.L1 [%0];" ::"l"(p2.topk_w + (size_t)tt * p2.k));
@@ -598,8 +697,9 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
         __syncwarp();
         if (go)
           for (long long u = gt; u < units; u += gstride)
-            combine_unit<true>(p2.y, p2.topk_w, p2.row_of_slot, (int)(u / (p2.H / 8)), (int)(u % (p2.H / 8)),
-                               p2.H, p2.k, p2.out, nullptr, nullptr, nullptr);
+            combine_unit<true, kSelfPlan>(p2.y, kSelfPlan ? s_sw : p2.topk_w, kSelfPlan ? s_ros : p2.row_of_slot,
+                                          (int)(u / (p2.H / 8)), (int)(u % (p2.H / 8)), p2.H, p2.k, p2.out, nullptr,
+                                          nullptr, nullptr);
       }
     }
   }
@@ -636,8 +736,9 @@ static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const C
                           const GemmParams& gp2, long long max_items, cudaStream_t st) {
   using L = Smem<BN>;
   auto kern = grouped_gemm_kernel<BN, MODE>;
-  const int smem = L::total(gp.E, MODE == 2);
-  if (ensure_smem_limit((const void*)kern, L::total(kMaxE, MODE == 2))) return MOE_ERR_CUDA;
+  const int smem = L::total(gp.E, MODE >= 2, MODE == 3 ? gp.T * gp.k : 0);
+  const int smem_max = MODE == 3 ? L::total(kSelfPlanMaxE, true, kSelfPlanMaxT * kMaxK) : L::total(kMaxE, MODE == 2);
+  if (ensure_smem_limit((const void*)kern, smem_max)) return MOE_ERR_CUDA;
   // persistent grid: as many CTAs as fit on the GPU at once (smem depends on E); the one-launch
   // W13 + W2 mode relies on every CTA being resident
   const int occ = ctas_per_sm_by_smem((size_t)smem, L::kCtasPerSm);
@@ -807,10 +908,11 @@ int launch_w13_w2_fused(const moe_shape* s, const uint8_t* xq, const uint8_t* xs
                         const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, const int32_t* offsets,
                         const int32_t* slot_of_row, uint8_t* hq, uint8_t* hs, float* dbg, float* y, uint32_t* status,
                         uint32_t* ready, cudaStream_t st, const float* topk_w, const int32_t* row_of_slot,
-                        uint16_t* out) {
+                        uint16_t* out, const SelfPlanArgs* sp) {
   if (s->T == 0) return MOE_OK;
   const int bn = pick_bn(s);
   if (bn > 32 || !ready) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (sp && (!out || !self_plan_supported(s))) return MOE_ERR_UNSUPPORTED_SHAPE;
   GemmParams g13 = w13_params(s, xq, xs, false, w13, w13s, offsets, slot_of_row, hq, hs, dbg, status, false);
   GemmParams g2 = w2_params(s, hq, hs, w2, w2s, offsets, slot_of_row, y, status, false);
   g13.ready = ready;
@@ -822,6 +924,18 @@ int launch_w13_w2_fused(const moe_shape* s, const uint8_t* xq, const uint8_t* xs
     g2.out = out;
     g2.T = s->T;
   }
+  if (sp) {
+    g13.T = s->T;
+    g13.score = sp->score;
+    g13.key = sp->key;
+    g13.dead = sp->dead;
+    g13.plan_topk_idx = sp->topk_idx;
+    g13.plan_topk_w = sp->topk_w;
+    g13.plan_counts = sp->counts;
+    g13.plan_offsets = sp->offsets;
+    g13.plan_slot_of_row = sp->slot_of_row;
+    g13.plan_row_of_slot = sp->row_of_slot;
+  }
   if ((long long)s->E * std::max(g13.MT * g13.KC, g2.MT * g2.KC) * 128 >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
   CUtensorMap t13, t2;
   int rc = weight_tmap(&t13, s, w13, g13, Smem<16>::KT);
@@ -829,6 +943,9 @@ int launch_w13_w2_fused(const moe_shape* s, const uint8_t* xq, const uint8_t* xs
   if (rc) return rc;
   const long long slots = (long long)s->T * s->k;
   const long long max_items = (long long)(g13.MT + g2.MT) * ((slots + bn - 1) / bn + std::min<long long>(s->E, slots));
+  if (sp)
+    return bn == 16 ? launch_gemm_bn<16, 3>(t13, t13, t2, g13, g2, max_items, st)
+                    : launch_gemm_bn<32, 3>(t13, t13, t2, g13, g2, max_items, st);
   return bn == 16 ? launch_gemm_bn<16, 2>(t13, t13, t2, g13, g2, max_items, st)
                   : launch_gemm_bn<32, 2>(t13, t13, t2, g13, g2, max_items, st);
 }

@@ -40,8 +40,9 @@ struct GemmParams {
   uint32_t* status;
   // W13 then W2 in one launch: W13 epilogue warps count finished tiles per expert in ready[0..E)
   // (after their stores), and a W2 tile gathers its expert's rows only once every W13 tile of that
-  // expert has been counted; W2 epilogue warps count their finished tiles in ready[E]. Zeroed by the
-  // plan kernel before each layer call.
+  // expert has been counted; W2 epilogue warps count their finished tiles in ready[E]. Zeroed before
+  // each layer call by the kernel that ran before this one (the plan kernel, or the decode router
+  // when the GEMM plans for itself).
   uint32_t* ready;
   // ... and, when out is set, the fixed-order combine of the T rows at the end of the launch, once
   // ready[E] says every W2 tile is stored
@@ -49,6 +50,18 @@ struct GemmParams {
   const int32_t* row_of_slot;
   uint16_t* out;
   int T;
+  // One-launch decode layer (small batches): every CTA selects the top-k of the T rows from the
+  // router's scores and keys [T, E] and builds the plan in its own shared memory (rows the dead
+  // mask flags get no plan rows); CTA 0 also writes the plan to the plan_* arrays for the caller.
+  const float* score;
+  const float* key;
+  const uint8_t* dead;
+  int32_t* plan_topk_idx;
+  float* plan_topk_w;
+  int32_t* plan_counts;
+  int32_t* plan_offsets;
+  int32_t* plan_slot_of_row;
+  int32_t* plan_row_of_slot;
 };
 
 

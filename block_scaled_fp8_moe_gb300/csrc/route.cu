@@ -13,6 +13,7 @@
 #include "mx.cuh"
 #include "ptx.cuh"
 #include "router_math.cuh"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -121,9 +122,12 @@ template <int EPT>
 __global__ void __launch_bounds__(kDecThreadsMax) router_decode_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, const float* __restrict__ bias, int T, int H,
     int E, int epc, int tpc, float* __restrict__ score, float* __restrict__ key, uint8_t* __restrict__ xq,
-    uint8_t* __restrict__ xs) {
+    uint8_t* __restrict__ xs, uint32_t* __restrict__ ready) {
   pdl_trigger();
   pdl_wait();
+  // the one-launch W13 + W2 GEMM's counters (nullable), when no plan kernel runs in between
+  if (ready && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) ready[i] = 0;
   extern __shared__ __align__(16) uint8_t dsm_dec[];
   const int NC = H / kRouterChunk;
   const int t0 = blockIdx.y * tpc;
@@ -402,75 +406,6 @@ __device__ __forceinline__ void anchored_weights(const float* __restrict__ srow,
   float sum = 0.f;
   for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, sc, j));
   *w = __fdiv_rn(sc, sum);
-}
-
-// One token's top-k on one warp. Lane l holds experts l, l + 32, ... (NI of them), sorted once in
-// registers by (key desc, expert asc); each round is a warp arg-max over the lanes' heads (two warp
-// reductions: the largest key, then the lowest expert holding it), after which the winning lane
-// drops its head (a predicated shift, no divergent rescan). Selected weights: sigma_j / sum, the
-// sum accumulated in rank order (identical on every lane). Lane j < k ends with the j-th choice.
-template <int NI>
-__device__ __forceinline__ void warp_topk(const float* __restrict__ krow, const float* __restrict__ srow, int E, int k,
-                                          int lane, int16_t* sidx, int* my_e, float* my_s, float* sum_out) {
-  // lane l holds experts e = l + 32 i: the key as an order-preserving unsigned image (keys are never
-  // -0 or NaN, so every key maps above 0; 0 marks "nothing"), its score and its id
-  uint32_t ku[NI];
-  float sv[NI];
-  int ev[NI];
-#pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    const int e = lane + 32 * i;
-    const bool in = e < E;
-    const uint32_t bits = in ? __float_as_uint(__ldcg(krow + e)) : 0u;   // through L2: another CTA wrote them
-    ku[i] = in ? ((bits & 0x80000000u) ? ~bits : (bits | 0x80000000u)) : 0u;
-    sv[i] = in ? __ldcg(srow + e) : 0.f;
-    ev[i] = in ? e : 0x7fffffff;
-  }
-  // each lane sorts its items best first, (key desc, id asc), with a bitonic network in registers
-#pragma unroll
-  for (int size = 2; size <= NI; size <<= 1)
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1)
-#pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool j_better = ku[j] > ku[i] || (ku[j] == ku[i] && ev[j] < ev[i]);
-          const bool swap = ((i & size) == 0) ? j_better : !j_better;
-          const uint32_t tk = ku[i];
-          const float ts = sv[i];
-          const int te = ev[i];
-          ku[i] = swap ? ku[j] : ku[i];
-          sv[i] = swap ? sv[j] : sv[i];
-          ev[i] = swap ? ev[j] : ev[i];
-          ku[j] = swap ? tk : ku[j];
-          sv[j] = swap ? ts : sv[j];
-          ev[j] = swap ? te : ev[j];
-        }
-      }
-  // k rounds over the lanes' heads: the largest key, then the lowest id holding it; the winning
-  // lane drops its head
-  float sel_sum = 0.f;
-  for (int j = 0; j < k; ++j) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, ku[0]);
-    const int be = __reduce_min_sync(0xffffffffu, ku[0] == m ? ev[0] : 0x7fffffff);
-    const float sc = __shfl_sync(0xffffffffu, sv[0], be & 31);
-    const bool win = ev[0] == be;
-#pragma unroll
-    for (int i = 0; i + 1 < NI; ++i) {
-      ku[i] = win ? ku[i + 1] : ku[i];
-      sv[i] = win ? sv[i + 1] : sv[i];
-      ev[i] = win ? ev[i + 1] : ev[i];
-    }
-    if (win) {
-      ku[NI - 1] = 0u;
-      ev[NI - 1] = 0x7fffffff;
-    }
-    sel_sum = __fadd_rn(sel_sum, sc);
-    if (lane == j) { *my_e = be; *my_s = sc; }
-    if (sidx && lane == 0) sidx[j] = (int16_t)be;
-  }
-  *sum_out = sel_sum;
 }
 
 // Top-k alone, one warp per token over the whole grid (the multi-block plan reads its result).
@@ -817,6 +752,41 @@ static int launch_topk_single_plain(int E, cudaStream_t st, const float* score, 
   return MOE_ERR_UNSUPPORTED_SHAPE;
 }
 
+static bool decode_router_fits(int T, int H, int E) {
+  const DecodeRouterCfg dc = decode_router_cfg(T, H, E);
+  return T <= kDecMaxT && dc.threads <= kDecThreadsMax && dc.smem <= kDecodeSmemMax;
+}
+
+// The decode router (decode_router_fits): scores and keys, plus xq/xs and the zeroed counters in
+// ready when those are non-null.
+static int launch_router_decode(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias,
+                                float* score, float* key, uint8_t* xq, uint8_t* xs, uint32_t* ready, cudaStream_t st) {
+  const int T = s->T, E = s->E, H = s->H;
+  const DecodeRouterCfg dc = decode_router_cfg(T, H, E);
+  const dim3 grid(ceil_div(E, dc.epc), ceil_div(T, dc.tpc));
+  if (dc.ept == 1) {
+    if (ensure_smem_limit((const void*)router_decode_kernel<1>, (int)kDecodeSmemMax)) return MOE_ERR_CUDA;
+    return launch_pdl(router_decode_kernel<1>, grid, dim3(dc.threads), dc.smem, st, x, wr, bias, T, H, E, dc.epc,
+                      dc.tpc, score, key, xq, xs, ready);
+  }
+  if (ensure_smem_limit((const void*)router_decode_kernel<2>, (int)kDecodeSmemMax)) return MOE_ERR_CUDA;
+  return launch_pdl(router_decode_kernel<2>, grid, dim3(dc.threads), dc.smem, st, x, wr, bias, T, H, E, dc.epc,
+                    dc.tpc, score, key, xq, xs, ready);
+}
+
+bool self_plan_supported(const moe_shape* s) {
+  return s->T >= 1 && s->T <= kSelfPlanMaxT && s->E <= kSelfPlanMaxE && fused_gemms_supported(s) &&
+         decode_router_fits(s->T, s->H, s->E);
+}
+
+int launch_router_decode_scores(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, void* ws,
+                                cudaStream_t st, uint8_t* xq, uint8_t* xs, uint32_t* ready) {
+  if (!self_plan_supported(s) || !xq || !xs || !ready) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const Workspace L = workspace_layout(s);
+  return launch_router_decode(s, x, wr, bias, ws_ptr<float>(ws, L.score), ws_ptr<float>(ws, L.key), xq, xs, ready,
+                              st);
+}
+
 int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, const uint8_t* dead,
                  int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
                  int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done,
@@ -831,22 +801,10 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
   }
   float* score = ws_ptr<float>(ws, L.score);
   float* key = ws_ptr<float>(ws, L.key);
-  const DecodeRouterCfg dc = decode_router_cfg(T, H, E);
   int rc0 = MOE_OK;
-  if (T <= kDecMaxT && dc.threads <= kDecThreadsMax && dc.smem <= kDecodeSmemMax) {
+  if (decode_router_fits(T, H, E)) {
     const bool fuse = xq && xs;
-    uint8_t* fq = fuse ? xq : nullptr;
-    uint8_t* fs = fuse ? xs : nullptr;
-    const dim3 grid(ceil_div(E, dc.epc), ceil_div(T, dc.tpc));
-    if (dc.ept == 1) {
-      if (ensure_smem_limit((const void*)router_decode_kernel<1>, (int)kDecodeSmemMax)) return MOE_ERR_CUDA;
-      rc0 = launch_pdl(router_decode_kernel<1>, grid, dim3(dc.threads), dc.smem, st, x, wr, bias, T, H, E, dc.epc,
-                       dc.tpc, score, key, fq, fs);
-    } else {
-      if (ensure_smem_limit((const void*)router_decode_kernel<2>, (int)kDecodeSmemMax)) return MOE_ERR_CUDA;
-      rc0 = launch_pdl(router_decode_kernel<2>, grid, dim3(dc.threads), dc.smem, st, x, wr, bias, T, H, E, dc.epc,
-                       dc.tpc, score, key, fq, fs);
-    }
+    rc0 = launch_router_decode(s, x, wr, bias, score, key, fuse ? xq : nullptr, fuse ? xs : nullptr, nullptr, st);
     if (quant_done) *quant_done = fuse;
   } else if (T <= kSmallT) {
     rc0 = launch_pdl(router_small_kernel, dim3(ceil_div(E, 8)), dim3(256), 0, st, x, wr, bias, T, H, E, score, key);

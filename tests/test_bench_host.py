@@ -11,8 +11,8 @@ CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                     "csrc")
 
 
-def _const(name):
-    src = open(os.path.join(CSRC, "route.cu")).read()
+def _const(name, fname="route.cu"):
+    src = open(os.path.join(CSRC, fname)).read()
     m = re.search(r"#define %s (\d+)" % name, src) or re.search(r"constexpr \w+ %s = ([\d *]+);" % name, src)
     assert m, name
     return eval(m.group(1))  # noqa: S307 - integer literals / products from our own source
@@ -41,7 +41,10 @@ def test_decode_router_predicate_matches_the_library_constants():
             cfg = synth.custom("p", T, H, 256, 8, 128, seed=0)
             n = bench.launches_per_step(cfg)
             fused = 2 if T * 8 / 256 <= 32 else 0          # one launch for W13 + W2 + combine (decode tiles)
-            if _decode_router(T, H):
+            self_routed = T <= _const("kSelfPlanMaxT", "common.cuh") and _const("kSelfPlanMaxE", "common.cuh") >= 256
+            if _decode_router(T, H) and self_routed:
+                assert n == 2, (T, H)              # router (+ quant), GEMMs that route the rows themselves
+            elif _decode_router(T, H):
                 assert n == 5 - fused, (T, H)      # router (+ quant), top-k + plan, W13, W2, combine
             else:
                 assert n >= 6 - fused, (T, H)      # separate quantiser and a non-decode router
@@ -50,10 +53,10 @@ def test_decode_router_predicate_matches_the_library_constants():
 def test_launch_counts_of_the_benchmarked_workloads():
     counts = {name: bench.launches_per_step(synth.CONFIGS[name]) for name in
               ("decode-6", "decode-48", "prefill-4k", "prefill-32k")}
-    # decode: fused router+quant, top-k/plan, W13 + W2 + combine in one launch; prefill: norms,
-    # screen, exact recompute, grid-wide select, plan, scan, scatter, quantiser into plan order,
-    # W13, W2, combine
-    assert counts == {"decode-6": 3, "decode-48": 3, "prefill-4k": 11, "prefill-32k": 11}
+    # decode-6: fused router+quant, then top-k, plan, W13 + W2 + combine in one launch; decode-48:
+    # the same with the top-k + plan kernel between them; prefill: norms, screen, exact recompute,
+    # grid-wide select, plan, scan, scatter, quantiser into plan order, W13, W2, combine
+    assert counts == {"decode-6": 2, "decode-48": 3, "prefill-4k": 11, "prefill-32k": 11}
     # with a shared expert the combine is its own launch after the side stream joins
     assert bench.launches_per_step(synth.CONFIGS["decode-6"], shared=True) == 7
 
@@ -62,6 +65,7 @@ def test_gemm_kind_classifies_every_grouped_gemm_launch_name():
     """The traffic recorder files each ncu launch under the step it belongs to."""
     ck = "(CUtensorMap_st, CUtensorMap_st, CUtensorMap_st, GemmParams, GemmParams)"
     assert bench.gemm_kind("void grouped_gemm_kernel<16, 2>" + ck) == "experts"
+    assert bench.gemm_kind("void grouped_gemm_kernel<16, 3>" + ck) == "experts_selfroute"
     assert bench.gemm_kind("void grouped_gemm_kernel<224, 1>" + ck) == "w13"
     assert bench.gemm_kind("void grouped_gemm_kernel<64, 0>" + ck) == "w2"
     assert bench.gemm_kind("grouped_gemm_ws_kernel(CUtensorMap_st, CUtensorMap_st, GemmParams)") == "w2"

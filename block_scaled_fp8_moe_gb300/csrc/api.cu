@@ -312,8 +312,8 @@ int forward_impl(const moe_shape* s, const uint16_t* x, const uint16_t* w_router
   // with no shared expert to add, the one-launch GEMMs also run the combine at their end
   const bool fused_combine = fuse_gemms && !shared;
   if (fuse_gemms) {
-    const SelfPlanArgs sp{ws_ptr<float>(ws, L.score), ws_ptr<float>(ws, L.key), dead, topk_idx, topk_w, counts,
-                          offsets, slot_of_row, row_of_slot};
+    const SelfPlanArgs sp{ws_ptr<float2>(ws, L.selrep), dead, topk_idx, topk_w, counts, offsets, slot_of_row,
+                          row_of_slot};
     rc = launch_w13_w2_fused(s, xq, xs, w13, w13_s, w2, w2_s, offsets, slot_of_row, hq, hs, im.swiglu, y, status,
                              ready, st, fused_combine ? topk_w : nullptr, fused_combine ? row_of_slot : nullptr,
                              fused_combine ? out : nullptr, self_plan ? &sp : nullptr);

@@ -22,6 +22,9 @@ constexpr int kMaxK = 32;
 constexpr int kSelfPlanMaxT = 8;
 constexpr int kSelfPlanMaxE = 256;
 constexpr int kSelfPlanNI = kSelfPlanMaxE / 32;
+// ... reading its rows' (key, score) pairs from one of this many copies (CTA b: copy b mod n), so
+// that the GPU's CTAs do not all queue on the same few L2 lines
+constexpr int kSelfPlanReplicas = 8;
 constexpr int kTileK = 128;            // K elements per packed tile / pipeline stage
 constexpr int kTileRows = 128;         // weight rows per packed tile
 constexpr int kTileCodeBytes = kTileRows * kTileK / 2;   // 8192
@@ -50,6 +53,7 @@ struct Workspace {
   size_t xqp, xsp;                                             // plan-order copy of xq / xs
   size_t xnorm, wnorm, cand, ncand;                            // router screen
   size_t ready;                                                // per-expert W13 tile counters
+  size_t selrep;                                               // self-routed batches: (key, score) copies
   size_t total;
 };
 
@@ -83,6 +87,7 @@ inline Workspace workspace_layout(const moe_shape* s) {
   w.cand = take(T * 64 * 4);
   w.ncand = take(T * 4);
   w.ready = take((E + 1) * 4);
+  w.selrep = take((T <= (size_t)kSelfPlanMaxT && E <= (size_t)kSelfPlanMaxE) ? kSelfPlanReplicas * T * E * 8 : 0);
   w.total = off;
   return w;
 }
@@ -197,17 +202,16 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
                  int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
                  int32_t* row_of_slot, void* ws, cudaStream_t st, uint8_t* xq, uint8_t* xs, bool* quant_done,
                  const int32_t* anchor, uint32_t* ready);
-// The decode router alone (scores, keys, and the MXFP8 quantisation of x into xq/xs), for a layer
-// call whose fused GEMM routes itself (self_plan_supported); it also zeroes the E + 1 counters in
-// ready.
+// The decode router alone (scores, keys, kSelfPlanReplicas copies of the (key, score) pairs in the
+// workspace, and the MXFP8 quantisation of x into xq/xs), for a layer call whose fused GEMM routes
+// itself (self_plan_supported); it also zeroes the E + 1 counters in ready.
 bool self_plan_supported(const moe_shape* s);
 int launch_router_decode_scores(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, void* ws,
                                 cudaStream_t st, uint8_t* xq, uint8_t* xs, uint32_t* ready);
 // The routing plan a self-routing fused GEMM builds (every CTA in shared memory) from the router's
-// scores and keys, and the arrays its CTA 0 writes it to.
+// (key, score) pairs [kSelfPlanReplicas][T][E], and the arrays its CTA 0 writes it to.
 struct SelfPlanArgs {
-  const float* score;
-  const float* key;
+  const float2* sel;
   const uint8_t* dead;
   int32_t* topk_idx;
   float* topk_w;

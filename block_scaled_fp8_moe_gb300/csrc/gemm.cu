@@ -221,8 +221,9 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
     for (int t = warp; t < p.T; t += Threads<BN>::kCount / 32) {
       int my_e = 0;
       float my_s = 0.f, sum = 0.f;
-      warp_topk<kSelfPlanNI>(p.key + (size_t)t * E, p.score + (size_t)t * E, E, p.k, lane, nullptr, &my_e, &my_s,
-                             &sum);
+      const float2* srow = p.sel + ((size_t)(blockIdx.x % kSelfPlanReplicas) * p.T + t) * E;
+      warp_topk<kSelfPlanNI, true>(reinterpret_cast<const float*>(srow), nullptr, E, p.k, lane, nullptr, &my_e,
+                                   &my_s, &sum);
       const bool live = p.dead == nullptr || p.dead[t] == 0;
       if (lane < p.k) {
         s_se[t * p.k + lane] = my_e;
@@ -232,14 +233,18 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
     }
     __syncthreads();
     if (warp == 0) {
-      // offsets and tile starts: warp-parallel prefix sums of count_e and ceil(count_e / BN)
+      // offsets and tile starts: warp-parallel prefix sums of count_e and ceil(count_e / BN); lane l
+      // takes experts l per .. l per + per - 1 (per <= kSelfPlanNI), all its mask loads in flight
       const int per = (E + 31) / 32;
       const int e0 = lane * per;
+      int cnt[kSelfPlanNI];
       int lc = 0, lt = 0;
-      for (int e = e0; e < min(E, e0 + per); ++e) {
-        const int c = __popc(s_mask[e]);
-        lc += c;
-        lt += (c + BN - 1) / BN;
+#pragma unroll
+      for (int j = 0; j < kSelfPlanNI; ++j) {
+        const int e = e0 + j;
+        cnt[j] = (j < per && e < E) ? __popc(s_mask[e]) : 0;
+        lc += cnt[j];
+        lt += (cnt[j] + BN - 1) / BN;
       }
       int ic = lc, it = lt;
 #pragma unroll
@@ -252,13 +257,17 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
         }
       }
       int rc = ic - lc, rt = it - lt;
-      for (int e = e0; e < min(E, e0 + per); ++e) {
-        const int c = __popc(s_mask[e]);
-        s_off[e] = rc;
-        s_cum[e] = rt * p.MT;
-        s_cum2[e] = rt * p2.MT;
-        rc += c;
-        rt += (c + BN - 1) / BN;
+      const int mt1 = p.MT, mt2 = p2.MT;
+#pragma unroll
+      for (int j = 0; j < kSelfPlanNI; ++j) {
+        const int e = e0 + j;
+        if (j < per && e < E) {
+          s_off[e] = rc;
+          s_cum[e] = rt * mt1;
+          s_cum2[e] = rt * mt2;
+        }
+        rc += cnt[j];
+        rt += (cnt[j] + BN - 1) / BN;
       }
       if (lane == 31) {
         s_off[E] = ic;
@@ -267,6 +276,7 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
       }
       __syncwarp();
       // a live slot's plan row: its expert's offset plus the expert's rows of lower tokens
+#pragma unroll 2
       for (int i = lane; i < nsl; i += 32) {
         const int t = i / p.k;
         const int e = s_se[i];
@@ -926,8 +936,7 @@ int launch_w13_w2_fused(const moe_shape* s, const uint8_t* xq, const uint8_t* xs
   }
   if (sp) {
     g13.T = s->T;
-    g13.score = sp->score;
-    g13.key = sp->key;
+    g13.sel = sp->sel;
     g13.dead = sp->dead;
     g13.plan_topk_idx = sp->topk_idx;
     g13.plan_topk_w = sp->topk_w;

@@ -51,10 +51,10 @@ struct GemmParams {
   uint16_t* out;
   int T;
   // One-launch decode layer (small batches): every CTA selects the top-k of the T rows from the
-  // router's scores and keys [T, E] and builds the plan in its own shared memory (rows the dead
-  // mask flags get no plan rows); CTA 0 also writes the plan to the plan_* arrays for the caller.
-  const float* score;
-  const float* key;
+  // router's (key, score) pairs (CTA b reads copy b mod kSelfPlanReplicas of [T, E]) and builds
+  // the plan in its own shared memory (rows the dead mask flags get no plan rows); CTA 0 also
+  // writes the plan to the plan_* arrays for the caller.
+  const float2* sel;
   const uint8_t* dead;
   int32_t* plan_topk_idx;
   float* plan_topk_w;

@@ -122,7 +122,7 @@ template <int EPT>
 __global__ void __launch_bounds__(kDecThreadsMax) router_decode_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, const float* __restrict__ bias, int T, int H,
     int E, int epc, int tpc, float* __restrict__ score, float* __restrict__ key, uint8_t* __restrict__ xq,
-    uint8_t* __restrict__ xs, uint32_t* __restrict__ ready) {
+    uint8_t* __restrict__ xs, uint32_t* __restrict__ ready, float2* __restrict__ sel) {
   pdl_trigger();
   pdl_wait();
   // the one-launch W13 + W2 GEMM's counters (nullable), when no plan kernel runs in between
@@ -229,8 +229,12 @@ __global__ void __launch_bounds__(kDecThreadsMax) router_decode_kernel(
     float acc = 0.f;
     for (int cc = 0; cc < NC; ++cc) acc = __fadd_rn(acc, pp[cc]);
     const float sc = sigmoid_cw(acc);
+    const float ky = __fadd_rn(sc, bias[e]);
     score[(size_t)(t0 + t) * E + e] = sc;
-    key[(size_t)(t0 + t) * E + e] = __fadd_rn(sc, bias[e]);
+    key[(size_t)(t0 + t) * E + e] = ky;
+    // the self-routing GEMM's copies of the (key, score) pairs (nullable)
+    if (sel)
+      for (int r = 0; r < kSelfPlanReplicas; ++r) sel[((size_t)r * T + t0 + t) * E + e] = make_float2(ky, sc);
   }
 }
 
@@ -757,21 +761,22 @@ static bool decode_router_fits(int T, int H, int E) {
   return T <= kDecMaxT && dc.threads <= kDecThreadsMax && dc.smem <= kDecodeSmemMax;
 }
 
-// The decode router (decode_router_fits): scores and keys, plus xq/xs and the zeroed counters in
-// ready when those are non-null.
+// The decode router (decode_router_fits): scores and keys, plus xq/xs, the zeroed counters in
+// ready and the (key, score) copies in sel when those are non-null.
 static int launch_router_decode(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias,
-                                float* score, float* key, uint8_t* xq, uint8_t* xs, uint32_t* ready, cudaStream_t st) {
+                                float* score, float* key, uint8_t* xq, uint8_t* xs, uint32_t* ready, float2* sel,
+                                cudaStream_t st) {
   const int T = s->T, E = s->E, H = s->H;
   const DecodeRouterCfg dc = decode_router_cfg(T, H, E);
   const dim3 grid(ceil_div(E, dc.epc), ceil_div(T, dc.tpc));
   if (dc.ept == 1) {
     if (ensure_smem_limit((const void*)router_decode_kernel<1>, (int)kDecodeSmemMax)) return MOE_ERR_CUDA;
     return launch_pdl(router_decode_kernel<1>, grid, dim3(dc.threads), dc.smem, st, x, wr, bias, T, H, E, dc.epc,
-                      dc.tpc, score, key, xq, xs, ready);
+                      dc.tpc, score, key, xq, xs, ready, sel);
   }
   if (ensure_smem_limit((const void*)router_decode_kernel<2>, (int)kDecodeSmemMax)) return MOE_ERR_CUDA;
   return launch_pdl(router_decode_kernel<2>, grid, dim3(dc.threads), dc.smem, st, x, wr, bias, T, H, E, dc.epc,
-                    dc.tpc, score, key, xq, xs, ready);
+                    dc.tpc, score, key, xq, xs, ready, sel);
 }
 
 bool self_plan_supported(const moe_shape* s) {
@@ -784,7 +789,7 @@ int launch_router_decode_scores(const moe_shape* s, const uint16_t* x, const uin
   if (!self_plan_supported(s) || !xq || !xs || !ready) return MOE_ERR_UNSUPPORTED_SHAPE;
   const Workspace L = workspace_layout(s);
   return launch_router_decode(s, x, wr, bias, ws_ptr<float>(ws, L.score), ws_ptr<float>(ws, L.key), xq, xs, ready,
-                              st);
+                              ws_ptr<float2>(ws, L.selrep), st);
 }
 
 int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, const float* bias, const uint8_t* dead,
@@ -804,7 +809,8 @@ int launch_route(const moe_shape* s, const uint16_t* x, const uint16_t* wr, cons
   int rc0 = MOE_OK;
   if (decode_router_fits(T, H, E)) {
     const bool fuse = xq && xs;
-    rc0 = launch_router_decode(s, x, wr, bias, score, key, fuse ? xq : nullptr, fuse ? xs : nullptr, nullptr, st);
+    rc0 = launch_router_decode(s, x, wr, bias, score, key, fuse ? xq : nullptr, fuse ? xs : nullptr, nullptr, nullptr,
+                               st);
     if (quant_done) *quant_done = fuse;
   } else if (T <= kSmallT) {
     rc0 = launch_pdl(router_small_kernel, dim3(ceil_div(E, 8)), dim3(256), 0, st, x, wr, bias, T, H, E, score, key);

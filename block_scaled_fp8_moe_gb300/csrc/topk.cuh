@@ -14,7 +14,8 @@ namespace moe {
 // reductions: the largest key, then the lowest expert holding it), after which the winning lane
 // drops its head (a predicated shift, no divergent rescan). Selected weights: sigma_j / sum, the
 // sum accumulated in rank order (identical on every lane). Lane j < k ends with the j-th choice.
-template <int NI>
+// kPairs: krow holds (key, score) pairs, one 8-byte load per expert; srow is not read.
+template <int NI, bool kPairs = false>
 __device__ __forceinline__ void warp_topk(const float* __restrict__ krow, const float* __restrict__ srow, int E, int k,
                                           int lane, int16_t* sidx, int* my_e, float* my_s, float* sum_out) {
   // lane l holds experts e = l + 32 i: the key as an order-preserving unsigned image (keys are never
@@ -26,9 +27,12 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ krow, const 
   for (int i = 0; i < NI; ++i) {
     const int e = lane + 32 * i;
     const bool in = e < E;
-    const uint32_t bits = in ? __float_as_uint(__ldcg(krow + e)) : 0u;   // through L2: another CTA wrote them
+    // through L2: another kernel wrote them
+    float2 ks = make_float2(0.f, 0.f);
+    if (kPairs && in) ks = __ldcg(reinterpret_cast<const float2*>(krow) + e);
+    const uint32_t bits = in ? __float_as_uint(kPairs ? ks.x : __ldcg(krow + e)) : 0u;
     ku[i] = in ? ((bits & 0x80000000u) ? ~bits : (bits | 0x80000000u)) : 0u;
-    sv[i] = in ? __ldcg(srow + e) : 0.f;
+    sv[i] = in ? (kPairs ? ks.y : __ldcg(srow + e)) : 0.f;
     ev[i] = in ? e : 0x7fffffff;
   }
   // each lane sorts its items best first, (key desc, id asc), with a bitonic network in registers

@@ -90,8 +90,9 @@ constexpr int kDecMaxT = 64;
 constexpr int kDecThreadsMax = 512;
 constexpr size_t kDecodeSmemMax = 210 * 1024;
 constexpr int kDecPitch = 144;      // bytes per staged 64-element chunk
-constexpr int kDecSmallT = 16;      // up to this many rows: one token block, kDecEpcSmall experts per CTA
+constexpr int kDecSmallT = 16;      // up to this many rows: kDecEpcSmall experts per CTA,
 constexpr int kDecEpcSmall = 2;
+constexpr int kDecTpcSmall = 2;     // ... blocks of this many rows
 constexpr int kDecEpcLarge = 8;     // more rows: blocks of kDecTpcLarge rows, kDecEpcLarge experts per CTA
 constexpr int kDecTpcLarge = 16;
 
@@ -100,9 +101,11 @@ struct DecodeRouterCfg {
   size_t smem;
 };
 
-// Up to kDecSmallT rows: one token block and two experts per CTA (one per thread; the Wr stream is
-// spread over E / 2 CTAs). Beyond that: blocks of 16 rows and eight experts per CTA (two per
-// thread), so that each CTA stages few rows of x and serves many experts with them.
+// Up to kDecSmallT rows: blocks of two rows and two experts per CTA (one per thread; the Wr stream
+// is spread over E / 2 CTAs per block). Every CTA staging all the rows had each L2 line of x read
+// by all E / 2 CTAs at once: two-row blocks were the fastest of 1, 2, 3 and all 6 at decode-6.
+// Beyond that: blocks of 16 rows and eight experts per CTA (two per thread), so that each CTA
+// stages few rows of x and serves many experts with them.
 inline DecodeRouterCfg decode_router_cfg(int T, int H, int E) {
   const int NC = H / kRouterChunk;
   DecodeRouterCfg c{};
@@ -110,7 +113,7 @@ inline DecodeRouterCfg decode_router_cfg(int T, int H, int E) {
   c.ept = small ? 1 : 2;
   c.epc = small ? kDecEpcSmall : kDecEpcLarge;
   if (c.epc > E) c.epc = E;
-  c.tpc = small ? T : kDecTpcLarge;
+  c.tpc = small ? std::min(T, kDecTpcSmall) : kDecTpcLarge;
   c.threads = ((c.epc + c.ept - 1) / c.ept) * NC;
   auto smem = [&](int tpc) { return (size_t)tpc * NC * kDecPitch + (size_t)c.epc * tpc * (NC + 1) * 4; };
   while (c.tpc > 1 && smem(c.tpc) > kDecodeSmemMax) --c.tpc;

@@ -23,7 +23,7 @@ def _decode_router(T, H, E=256):
     small = T <= _const("kDecSmallT")
     ept = 1 if small else 2
     epc = min(E, _const("kDecEpcSmall") if small else _const("kDecEpcLarge"))
-    tpc = T if small else _const("kDecTpcLarge")
+    tpc = min(T, _const("kDecTpcSmall")) if small else _const("kDecTpcLarge")
     pitch, cap = _const("kDecPitch"), _const("kDecodeSmemMax")
 
     def smem(tp):

@@ -403,7 +403,7 @@ def decode_router_fits(T: int, H: int, E: int) -> bool:
     small = T <= 16
     ept, epc = (1, 2) if small else (2, 8)
     epc = min(epc, E)
-    tpc = min(T, 2) if small else 16
+    tpc = min(T, 2) if small else 8
     threads = -(-epc // ept) * nc
 
     def smem(tp):

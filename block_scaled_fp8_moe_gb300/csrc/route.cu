@@ -94,7 +94,7 @@ constexpr int kDecSmallT = 16;      // up to this many rows: kDecEpcSmall expert
 constexpr int kDecEpcSmall = 2;
 constexpr int kDecTpcSmall = 2;     // ... blocks of this many rows
 constexpr int kDecEpcLarge = 8;     // more rows: blocks of kDecTpcLarge rows, kDecEpcLarge experts per CTA
-constexpr int kDecTpcLarge = 16;
+constexpr int kDecTpcLarge = 8;
 
 struct DecodeRouterCfg {
   int ept, epc, tpc, threads;
@@ -104,8 +104,9 @@ struct DecodeRouterCfg {
 // Up to kDecSmallT rows: blocks of two rows and two experts per CTA (one per thread; the Wr stream
 // is spread over E / 2 CTAs per block). Every CTA staging all the rows had each L2 line of x read
 // by all E / 2 CTAs at once: two-row blocks were the fastest of 1, 2, 3 and all 6 at decode-6.
-// Beyond that: blocks of 16 rows and eight experts per CTA (two per thread), so that each CTA
-// stages few rows of x and serves many experts with them.
+// Beyond that: blocks of 8 rows and eight experts per CTA (two per thread), so that each CTA
+// stages few rows of x and serves many experts with them (16-row blocks: the same at 48 rows,
+// 4 us slower at 32).
 inline DecodeRouterCfg decode_router_cfg(int T, int H, int E) {
   const int NC = H / kRouterChunk;
   DecodeRouterCfg c{};

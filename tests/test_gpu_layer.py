@@ -20,6 +20,7 @@ CASES = [
     ("c5w576", 5, 256, 8, 2, 576),      # BN 16: two K-chunks per stage, W2 K = 576 -> odd chunk count
     ("c1000", 1000, 256, 4, 2, 256),    # wide W13 tiles: 500 rows per expert -> 3 tiles of 176 / 148
     ("c640w", 640, 256, 4, 2, 1024),    # wide tiles in both GEMMs (W2 K = 1024 = 8 chunks)
+    ("c900o", 900, 256, 4, 2, 192),     # wide gate/up tiles, 3 panels: the last panel pair holds one
 ]
 
 

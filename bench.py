@@ -98,7 +98,8 @@ def median_ci(values, level=0.95, resamples=2000, seed=0):
             "mean": round(float(v.mean()), 5), "n": int(v.size)}
 
 
-GEMM_SOURCES = ("gemm.cu", "gemm.cuh", "gemm2sm.cu", "gemm_ws.cu", "combine.cuh", "ptx.cuh", "mx.cuh", "common.cuh")
+GEMM_SOURCES = ("gemm.cu", "gemm.cuh", "gemm2sm.cu", "gemm_ws.cu", "combine.cuh", "topk.cuh", "ptx.cuh", "mx.cuh",
+                "common.cuh")
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 

@@ -692,9 +692,15 @@ def measure(cfg, args, gpu, world, headline: bool, peak_info=None):
         if fused_gemms(cfg):
             # the layer runs both GEMMs as one persistent launch: that launch is the dominant kernel
             achf = (alg13 + alg2) / (kms["experts"] * 1e-3) / 1e9
+            # DRAM bytes per launch: of this launch if captured, else of the layer's own launch of
+            # the same GEMMs (the self-routing variant, which also reads the router's scores from L2)
+            traffic, traffic_kernel = measured_traffic(cfg.name, ("experts",)), "grouped_gemm_kernel<BN, 2>"
+            if traffic is None:
+                traffic, traffic_kernel = measured_traffic(cfg.name, ("experts_selfroute",)), "grouped_gemm_kernel<BN, 3>"
             rec["roofline"] = {"kernel": "experts_grouped (grouped_gemm_kernel, gate/up then down in one launch)",
                                "bound": "hbm", "achieved": round(achf, 1), "peak": hbm_gbs, "unit": "GB/s",
-                               "frac": round(achf / hbm_gbs, 4), "traffic": measured_traffic(cfg.name, ("experts",)),
+                               "frac": round(achf / hbm_gbs, 4), "traffic": traffic,
+                               "traffic_kernel": traffic_kernel if traffic is not None else None,
                                "peak_source": f"{peak_src} HBM copy bandwidth (burst)",
                                "alg_bytes_per_launch": alg13 + alg2, "touched_experts": touched,
                                "launch_ms": round(kms["experts"], 5)}

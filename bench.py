@@ -443,9 +443,9 @@ def wide_w13(cfg) -> bool:
 
 
 def self_routed_gemms(cfg) -> bool:
-    """True when the one-launch GEMMs also select the experts and build the plan (at most 8 rows,
+    """True when the one-launch GEMMs also select the experts and build the plan (at most 12 rows,
     256 experts; the library's self_plan_supported, given the decode router and no shared expert)."""
-    return 1 <= cfg.T <= 8 and cfg.E <= 256 and fused_gemms(cfg)
+    return 1 <= cfg.T <= 12 and cfg.E <= 256 and fused_gemms(cfg)
 
 
 def fused_gemms(cfg) -> bool:

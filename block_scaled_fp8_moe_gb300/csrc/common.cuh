@@ -17,9 +17,10 @@ constexpr int kRouterChunk = 64;       // fixed reduction chunk of the router lo
 constexpr int kPlanBlock = 256;        // tokens per plan-count block
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
-// One-launch decode layer that routes itself: at most one row per warp of the fused GEMM CTA, and
+// One-launch decode layer that routes itself: up to 12 rows (a warp of the fused GEMM CTA selects
+// one or two of them; all 8 warps taking two, at 16 rows, measured slower than the plan kernel),
 // every expert's key in 8 registers per lane of the selecting warp
-constexpr int kSelfPlanMaxT = 8;
+constexpr int kSelfPlanMaxT = 12;
 constexpr int kSelfPlanMaxE = 256;
 constexpr int kSelfPlanNI = kSelfPlanMaxE / 32;
 // ... reading its rows' (key, score) pairs from one of this many copies (CTA b: copy b mod n), so

@@ -141,7 +141,7 @@ struct Smem {
 // MODE 0: the down projection (W2); 1: gate/up with SwiGLU and requant (W13); 2: W13 then W2 in
 // one persistent launch (decode tiles): every CTA works through its W13 items, then its W2 items;
 // 3: mode 2 for a batch of at most kSelfPlanMaxT rows that routes itself: every CTA takes the top-k
-// of the rows from the router's scores (one warp per row, the plan kernel's selection) and builds
+// of the rows from the router's scores (a warp per row, the plan kernel's selection) and builds
 // the plan in its shared memory, so no plan kernel runs between the router and the GEMMs.
 // A W2 item's weight tiles stream as soon as the CTA reaches it; its token rows (h) are gathered
 // once the W13 epilogues have counted every W13 tile of that expert (GemmParams::ready). All CTAs
@@ -216,8 +216,8 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, Smem<BN>::kCtasPerSm)
   }
   pdl_wait();                                    // everything below may read upstream results
   if (kSelfPlan) {
-    // top-k of row t on warp t (the choices and weights of the plan kernel); a live row sets its
-    // bit in the masks of its k experts
+    // top-k of row t on warp t % 8, rows in turn (the choices and weights of the plan kernel); a live
+    // row sets its bit in the masks of its k experts
     for (int t = warp; t < p.T; t += Threads<BN>::kCount / 32) {
       int my_e = 0;
       float my_s = 0.f, sum = 0.f;

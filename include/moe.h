@@ -238,7 +238,7 @@ MOE_API int moe_experts_grouped(const moe_shape* shape, const uint8_t* xq, const
 
 /* The whole layer: route -> quant -> W13+SwiGLU+requant -> W2 -> combine, on one stream, no host
  * synchronisation and no allocation (capturable in a CUDA graph for a fixed shape). For
- * decode-sized batches W13 and W2 run as one launch, as in moe_experts_grouped; for at most 8 rows
+ * decode-sized batches W13 and W2 run as one launch, as in moe_experts_grouped; for at most 12 rows
  * and 256 experts that launch also takes the top-k and builds the plan itself (every CTA from the
  * router's scores, the same choices and weights as moe_route_topk), so the layer is two launches.
  * `inter` (nullable) receives the intermediates the caller wants to keep. */

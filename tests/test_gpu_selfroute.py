@@ -1,8 +1,8 @@
-"""The layer call for a batch of at most 8 self-routed rows (no shared expert) runs the router and
-then one GEMM launch that selects the top-k and builds the plan in each CTA. It must give the bits
-of the step entry points (route -> quant -> W13 -> W2 + combine), hand the caller the same plan,
-and agree with the oracle; rows keep their bits across the 8 / 9 row boundary, where the layer
-goes back to the separate plan kernel."""
+"""The layer call for a batch of at most 12 self-routed rows (no shared expert) runs the router and
+then one GEMM launch that selects the top-k and builds the plan in each CTA (a warp takes one or two
+rows). It must give the bits of the step entry points (route -> quant -> W13 -> W2 + combine), hand
+the caller the same plan, and agree with the oracle; rows keep their bits across the 12 / 13 row
+boundary, where the layer goes back to the separate plan kernel."""
 import numpy as np
 import pytest
 import torch
@@ -20,6 +20,8 @@ CASES = [
     ("s7e200", 7, 384, 200, 4, 256, ()),          # E not a multiple of 32
     ("s8k32", 8, 256, 64, 32, 128, (3,)),         # 256 slots, 32 choices per row
     ("s3e33", 3, 256, 33, 1, 64, ()),             # one choice per row
+    ("s12", 12, 512, 64, 8, 192, (1, 11)),         # warps 0-3 select two rows each
+    ("s10k32", 10, 256, 64, 32, 128, (9,)),       # 320 slots, two rows on warps 0 and 1
 ]
 
 
@@ -73,15 +75,16 @@ def test_self_routed_layer_equals_steps_and_oracle(case):
         assert np.all(got[d] == 0.0) and not np.any(np.signbit(got[d]))
 
 
-def test_rows_keep_their_bits_across_the_eight_row_boundary():
-    inp = synth.make_inputs_cpu(synth.custom("b9", 9, 512, 64, 8, 192, seed=5))
+def test_rows_keep_their_bits_across_the_twelve_row_boundary():
+    inp = synth.make_inputs_cpu(synth.custom("b13", 13, 512, 64, 8, 192, seed=5))
     g = H.GpuLayer(inp)
-    nine = g.forward()                                     # plan kernel + one-launch GEMMs
-    eight = g.forward(x=g.x[:8].contiguous())              # routes itself
-    one = g.forward(x=g.x[8:9].contiguous())
-    assert torch.equal(eight, nine[:8]) and torch.equal(one[0], nine[8])
-    for t in (0, 3, 7):
-        assert torch.equal(g.forward(x=g.x[t:t + 1].contiguous())[0], nine[t])
+    full = g.forward()                                     # plan kernel + one-launch GEMMs
+    twelve = g.forward(x=g.x[:12].contiguous())            # routes itself
+    nine = g.forward(x=g.x[3:12].contiguous())
+    one = g.forward(x=g.x[12:13].contiguous())
+    assert torch.equal(twelve, full[:12]) and torch.equal(nine, full[3:12]) and torch.equal(one[0], full[12])
+    for t in (0, 7, 11):
+        assert torch.equal(g.forward(x=g.x[t:t + 1].contiguous())[0], full[t])
 
 
 def test_one_expert_pair_takes_every_row_and_all_dead():
@@ -113,3 +116,32 @@ def test_repeated_calls_alternating_with_the_plan_kernel_path():
         assert torch.equal(g.forward(x=small), a)
         assert torch.equal(g.forward(), b)
     assert torch.equal(a, b[:6])
+
+
+def test_self_routed_layer_replays_from_a_cuda_graph():
+    """The router inside the captured graph zeroes the GEMM's tile counters before every replay, and
+    new rows copied into the captured input route afresh."""
+    inp = synth.make_inputs_cpu(synth.custom("g6", 6, 512, 64, 8, 192, seed=21))
+    g = H.GpuLayer(inp)
+    other = synth.make_inputs_cpu(synth.custom("g6b", 6, 512, 64, 8, 192, seed=22))
+    x2 = other.x.cuda()
+    ref1 = g.forward().clone()
+    ref2 = g.forward(x=x2).clone()
+    xin = g.x.clone()
+    out = torch.empty(6, 512, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g.layer.forward(xin, out=out)                                    # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.layer.forward(xin, out=out)
+    for _ in range(3):
+        for x_new, ref in ((g.x, ref1), (x2, ref2)):
+            xin.copy_(x_new)
+            out.zero_()
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out, ref)

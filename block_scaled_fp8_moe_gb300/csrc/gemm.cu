@@ -750,7 +750,7 @@ static int launch_gemm_bn(const CUtensorMap& tm, const CUtensorMap& tmb, const C
   const int smem_max = MODE == 3 ? L::total(kSelfPlanMaxE, true, kSelfPlanMaxT * kMaxK) : L::total(kMaxE, MODE == 2);
   if (ensure_smem_limit((const void*)kern, smem_max)) return MOE_ERR_CUDA;
   // persistent grid: as many CTAs as fit on the GPU at once (smem depends on E); the one-launch
-  // W13 + W2 mode relies on every CTA being resident
+  // W13 + W2 modes rely on every CTA being resident
   const int occ = ctas_per_sm_by_smem((size_t)smem, L::kCtasPerSm);
   const long long grid = std::min<long long>(max_items, (long long)occ * num_sms());
   if (grid <= 0) return MOE_OK;

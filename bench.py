@@ -428,7 +428,12 @@ def launches_per_step(cfg, shared: bool = False) -> int:
         n = 3                                         # norms, tensor-core screen, exact recompute
     else:
         n = 1                                         # small-T or tiled logits
-    n += 1 if T <= 256 else 4                         # top-k + plan (+ grid-wide select, scan, scatter)
+    if T <= 256:
+        # top-k + plan in one CTA; rows beyond its warps (32, or 16 above 256 experts) take a
+        # grid-wide top-k launch first
+        n += 2 if T > (32 if E <= 256 else 16) else 1
+    else:
+        n += 4                                        # grid-wide top-k, plan blocks, scan, scatter
     if not decode_router:
         n += 1                                        # MXFP8 quantisation (straight into plan order when wide)
     if fused_gemms(cfg):

@@ -416,7 +416,8 @@ __device__ __forceinline__ void anchored_weights(const float* __restrict__ srow,
   *w = __fdiv_rn(sc, sum);
 }
 
-// Top-k alone, one warp per token over the whole grid (the multi-block plan reads its result).
+// Top-k alone, one warp per token over the whole grid (the plan kernels read its result when the
+// rows outnumber one plan CTA's warps).
 template <int NI>
 __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restrict__ score,
                                                           const float* __restrict__ key, int T, int E, int k,
@@ -461,9 +462,10 @@ __global__ void __launch_bounds__(256) anchor_fixup_kernel(const float* __restri
 
 // Top-k and the whole plan for T <= kPlanBlock rows in one CTA (any multiple of 32 threads, one
 // token per warp at a time): selection (self-routed rows, then anchored rows), per-expert token
-// bitmasks (plan order inside an expert = token order), counts, offsets, scatter.
+// bitmasks (plan order inside an expert = token order), counts, offsets, scatter. Without
+// kSelect the choices come from topk_idx (written by topk_select_kernel; no anchors).
 // Shared scratch: mask [E * 8] u32, sidx [kPlanBlock * k] i16, scnt [E] i32, wsum [32] i32, total.
-template <int NI>
+template <int NI, bool kSelect = true>
 __device__ void plan_single_block(const float* __restrict__ score, const float* __restrict__ key,
                                   const uint8_t* __restrict__ dead, int T, int E, int k, int32_t* __restrict__ topk_idx,
                                   float* __restrict__ topk_w, int32_t* __restrict__ counts,
@@ -471,7 +473,9 @@ __device__ void plan_single_block(const float* __restrict__ score, const float* 
                                   int32_t* __restrict__ row_of_slot, const int32_t* __restrict__ anchor,
                                   uint32_t* status, uint32_t* mask, int16_t* sidx, int* scnt, int* wsum, int* total) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  for (int t = warp; t < T; t += nwarps) {
+  if (!kSelect)
+    for (int i = threadIdx.x; i < T * k; i += blockDim.x) sidx[i] = (int16_t)__ldcg(topk_idx + i);
+  for (int t = warp; kSelect && t < T; t += nwarps) {
     if (anchor_of(anchor, t, T, status) >= 0) continue;      // after every self-routed row
     int my_e = -1;
     float my_s = 0.f, sum = 0.f;
@@ -550,7 +554,7 @@ constexpr int plan_single_threads() { return NI <= 8 ? 1024 : 512; }
 template <int NI>
 inline int plan_single_launch_threads(int T) { return (NI <= 8 && T <= 8) ? 256 : plan_single_threads<NI>(); }
 
-template <int NI>
+template <int NI, bool kSelect = true>
 __global__ void __launch_bounds__(plan_single_threads<NI>()) topk_plan_single_kernel(const float* __restrict__ score,
                                                                const float* __restrict__ key,
                                                                const uint8_t* __restrict__ dead, int T, int E, int k,
@@ -570,8 +574,8 @@ __global__ void __launch_bounds__(plan_single_threads<NI>()) topk_plan_single_ke
   int* scnt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(sidx) + align_up((size_t)kPlanBlock * k * 2, 16));
   int* wsum = scnt + align_up((size_t)E * 4, 16) / 4;
   int* total = wsum + 32;
-  plan_single_block<NI>(score, key, dead, T, E, k, topk_idx, topk_w, counts, offsets, slot_of_row, row_of_slot,
-                        anchor, status, mask, sidx, scnt, wsum, total);
+  plan_single_block<NI, kSelect>(score, key, dead, T, E, k, topk_idx, topk_w, counts, offsets, slot_of_row,
+                                 row_of_slot, anchor, status, mask, sidx, scnt, wsum, total);
   // tile counters of the one-launch W13 + W2 GEMM (E per expert + 1 total; nullable): zero them
   // (that GEMM reads them only after this grid has completed)
   if (ready)
@@ -690,8 +694,20 @@ static int launch_topk_plan_ni(int nb, int E, size_t smem, cudaStream_t st, cons
                                int32_t* rank, int32_t* counts, int32_t* offsets, int32_t* slot_of_row,
                                int32_t* row_of_slot, const int32_t* anchor, uint32_t* status, uint32_t* ready) {
   if (ensure_smem_limit((const void*)topk_plan_single_kernel<NI>, 64 * 1024) ||
+      ensure_smem_limit((const void*)topk_plan_single_kernel<NI, false>, 64 * 1024) ||
       ensure_smem_limit((const void*)topk_plan_kernel, 64 * 1024))
     return MOE_ERR_CUDA;
+  if (nb == 1 && !anchor && T > plan_single_threads<NI>() / 32) {
+    // more rows than the plan CTA has warps: the selection runs on the whole GPU (one warp per row,
+    // all rows at once) and the one CTA only plans from its lists
+    const int sel_blocks = (int)std::min<long long>(((long long)T + 7) / 8, (long long)num_sms() * 8);
+    const int rc = launch_pdl(topk_select_kernel<NI>, dim3(sel_blocks), dim3(256), 0, st, score, key, T, E, k,
+                              topk_idx, topk_w, anchor, status);
+    if (rc) return rc;
+    return launch_pdl(topk_plan_single_kernel<NI, false>, dim3(1), dim3(plan_single_launch_threads<NI>(T)),
+                      plan_single_smem(E, k), st, score, key, dead, T, E, k, topk_idx, topk_w, counts, offsets,
+                      slot_of_row, row_of_slot, anchor, status, ready);
+  }
   if (nb == 1)
     return launch_pdl(topk_plan_single_kernel<NI>, dim3(1), dim3(plan_single_launch_threads<NI>(T)),
                       plan_single_smem(E, k),

@@ -429,9 +429,9 @@ def launches_per_step(cfg, shared: bool = False) -> int:
     else:
         n = 1                                         # small-T or tiled logits
     if T <= 256:
-        # top-k + plan in one CTA; rows beyond its warps (32, or 16 above 256 experts) take a
-        # grid-wide top-k launch first
-        n += 2 if T > (32 if E <= 256 else 16) else 1
+        # top-k + plan in one CTA; more than 24 rows (16 above 256 experts) take a grid-wide top-k
+        # launch first
+        n += 2 if T > (24 if E <= 256 else 16) else 1
     else:
         n += 4                                        # grid-wide top-k, plan blocks, scan, scatter
     if not decode_router:

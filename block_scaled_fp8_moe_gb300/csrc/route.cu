@@ -697,9 +697,10 @@ static int launch_topk_plan_ni(int nb, int E, size_t smem, cudaStream_t st, cons
       ensure_smem_limit((const void*)topk_plan_single_kernel<NI, false>, 64 * 1024) ||
       ensure_smem_limit((const void*)topk_plan_kernel, 64 * 1024))
     return MOE_ERR_CUDA;
-  if (nb == 1 && !anchor && T > plan_single_threads<NI>() / 32) {
-    // more rows than the plan CTA has warps: the selection runs on the whole GPU (one warp per row,
-    // all rows at once) and the one CTA only plans from its lists
+  if (nb == 1 && !anchor && T > std::min(24, plan_single_threads<NI>() / 32)) {
+    // many rows for the plan CTA's warps (at 32 rows its one round of selections already contend
+    // for one SM): the selection runs on the whole GPU (one warp per row, all rows at once) and
+    // the one CTA only plans from its lists
     const int sel_blocks = (int)std::min<long long>(((long long)T + 7) / 8, (long long)num_sms() * 8);
     const int rc = launch_pdl(topk_select_kernel<NI>, dim3(sel_blocks), dim3(256), 0, st, score, key, T, E, k,
                               topk_idx, topk_w, anchor, status);

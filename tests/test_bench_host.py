@@ -45,8 +45,8 @@ def test_decode_router_predicate_matches_the_library_constants():
             if _decode_router(T, H) and self_routed:
                 assert n == 2, (T, H)              # router (+ quant), GEMMs that route the rows themselves
             elif _decode_router(T, H):
-                # router (+ quant), top-k + plan (a grid-wide top-k first above 32 rows), W13, W2, combine
-                assert n == 5 - fused + (1 if T > 32 else 0), (T, H)
+                # router (+ quant), top-k + plan (a grid-wide top-k first above 24 rows), W13, W2, combine
+                assert n == 5 - fused + (1 if T > 24 else 0), (T, H)
             else:
                 assert n >= 6 - fused, (T, H)      # separate quantiser and a non-decode router
 

@@ -37,6 +37,7 @@ def _route_case(T, H, E, k, seed, dead_frac=0.0, ties=False, bias_scale=0.1):
     (1, 256, 8, 2), (4, 256, 8, 2), (6, 4096, 256, 8), (7, 512, 64, 6), (16, 256, 32, 4), (17, 256, 32, 4),
     (33, 384, 16, 3), (65, 128, 8, 8), (256, 256, 64, 8), (257, 256, 64, 8), (600, 512, 40, 5),
     (4, 8192, 32, 4), (11, 8192, 16, 2),      # decode router at its widest rows (128 chunks per row)
+    (28, 1024, 256, 8), (48, 4096, 256, 8),   # grid-wide top-k, then the one-CTA plan from its lists
 ])
 def test_route_bit_exact(T, H, E, k):
     plan, ref = _route_case(T, H, E, k, seed=T * 31 + E)

@@ -952,9 +952,9 @@ int launch_w13_w2_fused(const moe_shape* s, const uint8_t* xq, const uint8_t* xs
   if (rc) return rc;
   const long long slots = (long long)s->T * s->k;
   const long long max_items = (long long)(g13.MT + g2.MT) * ((slots + bn - 1) / bn + std::min<long long>(s->E, slots));
-  if (sp)
-    return bn == 16 ? launch_gemm_bn<16, 3>(t13, t13, t2, g13, g2, max_items, st)
-                    : launch_gemm_bn<32, 3>(t13, t13, t2, g13, g2, max_items, st);
+  // a self-routed batch (at most kSelfPlanMaxT rows, k <= E) has T k / E <= kSelfPlanMaxT rows per
+  // expert on average: always 16-row tiles
+  if (sp) return bn == 16 ? launch_gemm_bn<16, 3>(t13, t13, t2, g13, g2, max_items, st) : MOE_ERR_UNSUPPORTED_SHAPE;
   return bn == 16 ? launch_gemm_bn<16, 2>(t13, t13, t2, g13, g2, max_items, st)
                   : launch_gemm_bn<32, 2>(t13, t13, t2, g13, g2, max_items, st);
 }
